@@ -1,0 +1,7 @@
+"""CPU oracle for the block-causal attention path (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
+reference legs may import this package.  It shares no code with the CUDA path.
+"""
+from .attention import (cache_append, masked_attention, prefill, prefix_decode,  # noqa: F401
+                        query_positions, visibility, visible_pairs)
