@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Throughput of the block-causal attention hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole path over one request of the two-reference
+edit workload (B=1, 32 heads x 128, [t96][ref 4096][t32][ref 4096][t64]
+[target 4096], S=12480): schedule prep + block-causal prefill, prefix cache
+append, then one cached step (prefix decode of the 4096 target queries over
+8384 cached + 4096 own keys).
+
+metric: TFLOP/s counting only visible (q, k) pairs (4 * 128 * 32 flops each)
+of prefill + decode, divided by the time of the whole step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own independent request (weak scaling, no
+data-path collective); the per-step times are max-reduced over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-causal attn TFLOP/s (visible pairs) prefill+prefix-decode; % of BF16 peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "edit_2ref_1024_s12480"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16": float(p["bf16_tflops"]), "bf16_sustained": float(p["bf16_tflops_sustained"]),
+                "hbm": float(p["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- inputs
+
+class Problem:
+    """The workload's tensors, resident on the device (plus pinned host copies for e2e)."""
+
+    def __init__(self, dev, with_host=True):
+        from prefix_kv_gb300 import flops
+        from prefix_kv_gb300 import workloads as W
+        wl = W.by_name(WORKLOAD)
+        self.wl = wl
+        q, k, v = W.make_qkv(wl)
+        tr = torch.from_numpy(wl.target_rows())
+        self.H = wl.num_heads
+        self.S = wl.seq_lens[0]
+        self.N = wl.target_lens()[0]
+        self.P = wl.prefix_lens()[0]
+        self.scale = 1.0 / math.sqrt(128)
+        self.host = {
+            "q": q, "k": k, "v": v,
+            "q_tgt": q[tr].contiguous(), "k_tgt": k[tr].contiguous(), "v_tgt": v[tr].contiguous(),
+            "block_id": torch.from_numpy(wl.block_id()),
+            "cu": torch.from_numpy(wl.cu_seqlens()),
+            "cu_pre": torch.from_numpy(wl.cu_prefix()),
+            "cu_tgt": torch.from_numpy(wl.cu_target()),
+        }
+        if with_host:
+            self.pinned = {n: t.pin_memory() for n, t in self.host.items()}
+        self.dev = {n: t.to(dev) for n, t in self.host.items()}
+        d = self.dev
+        self.out = torch.empty_like(d["q"])
+        self.lse = torch.empty((self.H, self.S), dtype=torch.float32, device=dev)
+        self.dout = torch.empty_like(d["q_tgt"])
+        self.dlse = torch.empty((self.H, self.N), dtype=torch.float32, device=dev)
+        self.cache_k = torch.empty((1, self.H, self.P, 128), dtype=torch.bfloat16, device=dev)
+        self.cache_v = torch.empty_like(self.cache_k)
+        import prefix_kv_gb300 as bca
+        self.ws = torch.empty(bca.prefill_workspace_bytes(1, self.S, self.S), dtype=torch.uint8,
+                              device=dev)
+        self.status = bca.new_status(dev)
+        cu = wl.cu_seqlens()
+        self.pairs_prefill = flops.prefill_visible_pairs(wl.block_id(), cu, cu)
+        self.pairs_decode = flops.decode_visible_pairs(wl.cu_target(), wl.cu_prefix())
+        self.flops_prefill = flops.attention_flops(self.pairs_prefill, self.H)
+        self.flops_decode = flops.attention_flops(self.pairs_decode, self.H)
+        self.append_bytes = 2 * 2 * self.P * self.H * 128 * 2   # K and V, read + write
+
+    def step(self, d, events=None):
+        """The whole path through the binding; `events` = 4 CUDA events to split it."""
+        import prefix_kv_gb300 as bca
+        if events:
+            events[0].record()
+        bca.prefill(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"], self.S, self.S,
+                    self.scale, out=self.out, lse=self.lse, workspace=self.ws, status=self.status)
+        if events:
+            events[1].record()
+        bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], self.cache_k, self.cache_v,
+                                0, status=self.status)
+        if events:
+            events[2].record()
+        bca.prefix_decode(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"], d["k_tgt"],
+                          d["v_tgt"], d["cu_tgt"], self.N, self.P, self.scale, out=self.dout,
+                          lse=self.dlse, status=self.status)
+        if events:
+            events[3].record()
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(prob: "Problem", step_idx: int, target_s: float = 3.0):
+    """Time the CPU oracle on a bounded sample of the workload; returns (flops, seconds, desc)."""
+    import oracle
+    wl, h = prob.wl, step_idx % prob.H
+    host = prob.host
+    cu = wl.cu_seqlens()
+    S = prob.S
+    # prefill: blocks of query rows of one head, until about target_s / 2
+    from prefix_kv_gb300 import flops
+    e_rows = flops.row_ends(wl.block_id(), S)
+    t0 = time.perf_counter()
+    rows_done, pairs, n = 0, 0, 512
+    start = (step_idx * 1543) % S
+    while time.perf_counter() - t0 < target_s / 2 and rows_done < S:
+        r0 = (start + rows_done) % S
+        rows = np.arange(r0, min(S, r0 + n))
+        oracle.prefill(host["q"], host["k"], host["v"], wl.block_id(), cu, cu, prob.scale,
+                       rows=rows, heads=np.array([h]))
+        pairs += int(e_rows[rows].sum())
+        rows_done += len(rows)
+    t1 = time.perf_counter()
+    # decode: query rows of the same head
+    drows_done, dpairs = 0, 0
+    while time.perf_counter() - t1 < target_s / 2 and drows_done < prob.N:
+        rows = np.arange(drows_done, min(prob.N, drows_done + n))
+        P = prob.P
+        oracle.prefix_decode(host["q_tgt"], host["k"][:P], host["v"][:P], wl.cu_prefix(),
+                             host["k_tgt"], host["v_tgt"], wl.cu_target(), prob.scale,
+                             rows=rows, heads=np.array([h]))
+        dpairs += len(rows) * (P + prob.N)
+        drows_done += len(rows)
+    t2 = time.perf_counter()
+    fl = 4.0 * 128 * (pairs + dpairs)
+    desc = (f"head {h}: {rows_done} prefill rows + {drows_done} decode rows of {WORKLOAD} "
+            f"(float64 NumPy oracle with explicit mask)")
+    return fl, t2 - t0, desc
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = [i.get("num_threads") for i in info if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    peaks = load_peaks()
+
+    if args.impl == "reference":
+        return run_reference(args, rank, world, peaks)
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    from __graft_entry__ import build
+    if rank == 0 or world == 1:
+        build()
+    if dist is not None:
+        dist.barrier()
+        build()
+
+    import prefix_kv_gb300 as bca
+    prob = Problem(dev, with_host=not args.no_e2e)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    for _ in range(max(3, args.warmup)):
+        prob.step(prob.dev)
+    torch.cuda.synchronize()
+    code = bca.read_status(prob.status)
+    if code != 0:
+        raise SystemExit(f"device status {code} after warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()          # L2 flush between timed steps (outside the events)
+            prob.step(prob.dev, evs[i])
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    code = bca.read_status(prob.status)
+    if code != 0:
+        raise SystemExit(f"device status {code} after timed steps")
+
+    t_pre = [e[0].elapsed_time(e[1]) for e in evs]
+    t_app = [e[1].elapsed_time(e[2]) for e in evs]
+    t_dec = [e[2].elapsed_time(e[3]) for e in evs]
+    t_step = [e[0].elapsed_time(e[3]) for e in evs]
+    tot_ms = sum(t_step)
+    if dist is not None:
+        t = torch.tensor([tot_ms, sum(t_pre), sum(t_app), sum(t_dec)], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        tot_ms, s_pre, s_app, s_dec = t.tolist()
+    else:
+        s_pre, s_app, s_dec = sum(t_pre), sum(t_app), sum(t_dec)
+    K = args.steps
+    step_flops = prob.flops_prefill + prob.flops_decode
+    value = world * K * step_flops / (tot_ms * 1e-3) / 1e12
+    pre_tf = prob.flops_prefill / (s_pre / K * 1e-3) / 1e12
+    dec_tf = prob.flops_decode / (s_dec / K * 1e-3) / 1e12
+    app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9
+
+    # ---- e2e through the public API with host buffers -------------------------------
+    e2e = None
+    if not args.no_e2e:
+        d = {n: torch.empty_like(t) for n, t in prob.dev.items()}
+        h_out = torch.empty(prob.out.shape, dtype=prob.out.dtype).pin_memory()
+        h_lse = torch.empty(prob.lse.shape, dtype=torch.float32).pin_memory()
+        h_dout = torch.empty(prob.dout.shape, dtype=prob.dout.dtype).pin_memory()
+        h_dlse = torch.empty(prob.dlse.shape, dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in prob.pinned.values())
+        d2h = sum(t.numel() * t.element_size() for t in (h_out, h_lse, h_dout, h_dlse))
+
+        def e2e_step():
+            for n, t in prob.pinned.items():
+                d[n].copy_(t, non_blocking=True)
+            prob.step(d)
+            h_out.copy_(prob.out, non_blocking=True)
+            h_lse.copy_(prob.lse, non_blocking=True)
+            h_dout.copy_(prob.dout, non_blocking=True)
+            h_dlse.copy_(prob.dlse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, K // 2)
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev0.record()
+        for _ in range(n_e2e):
+            e2e_step()
+        ev1.record()
+        torch.cuda.synchronize()
+        e_ms = ev0.elapsed_time(ev1)
+        if dist is not None:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = t.item()
+        e2e = {"value": round(world * n_e2e * step_flops / (e_ms * 1e-3) / 1e12, 2),
+               "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_ms / n_e2e, 4), "steps": n_e2e}
+
+    # ---- CPU baseline: the oracle on a bounded sample (rank 0, N=1 only) -------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        fl, secs, desc = oracle_sample(prob, 0, target_s=args.cpu_seconds)
+        cpu = {"value": round(fl / secs / 1e12, 6), "unit": UNIT, "cores": cpu_threads(),
+               "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    roofline = {"bound": "tensor", "kernel": "bca_prefill (block-causal attention forward)",
+                "achieved": round(pre_tf, 2), "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": round(pre_tf / peaks["bf16"], 4),
+                "peak_source": f"{peaks['source']} bf16 dense burst",
+                "frac_of_sustained": round(pre_tf / peaks["bf16_sustained"], 4),
+                "traffic": None,
+                "algorithmic": f"{prob.flops_prefill:.4e} flop per launch "
+                               f"({prob.pairs_prefill} visible pairs/head x 32 heads x 512)"}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(tot_ms / K, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "seq_len": prob.S, "num_heads": prob.H,
+                   "head_dim": 128, "prefix_len": prob.P, "target_len": prob.N,
+                   "step": "schedule prep + prefill + cache append + prefix decode",
+                   "l2": "flushed (256 MiB write) between timed steps",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "pct_of_bf16_peak": round(100 * value / peaks["bf16"], 2),
+        "breakdown": {"prefill_ms": round(s_pre / K, 4), "prefill_tflops": round(pre_tf, 2),
+                      "append_ms": round(s_app / K, 4), "append_gbs": round(app_gbs, 1),
+                      "append_frac_of_hbm": round(app_gbs / peaks["hbm"], 4),
+                      "decode_ms": round(s_dec / K, 4), "decode_tflops": round(dec_tf, 2),
+                      "decode_frac": round(dec_tf / peaks["bf16"], 4)},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": 4 * K,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_reference(args, rank, world, peaks):
+    """The oracle as it stands on the host cores, each step a bounded sample."""
+    if rank != 0:
+        return
+    # the host-side problem only: this leg never touches a GPU
+    from prefix_kv_gb300 import workloads as W
+
+    class HostProblem:
+        pass
+    hp = HostProblem()
+    wl = W.by_name(WORKLOAD)
+    q, k, v = W.make_qkv(wl)
+    tr = torch.from_numpy(wl.target_rows())
+    hp.wl, hp.H, hp.S = wl, wl.num_heads, wl.seq_lens[0]
+    hp.N, hp.P, hp.scale = wl.target_lens()[0], wl.prefix_lens()[0], 1.0 / math.sqrt(128)
+    hp.host = {"q": q, "k": k, "v": v, "q_tgt": q[tr].contiguous(), "k_tgt": k[tr].contiguous(),
+               "v_tgt": v[tr].contiguous()}
+    for i in range(args.warmup):
+        oracle_sample(hp, i, target_s=1.0)
+    fl_tot, s_tot, desc = 0.0, 0.0, ""
+    for i in range(args.steps):
+        fl, secs, desc = oracle_sample(hp, args.warmup + i, target_s=2.0)
+        fl_tot += fl
+        s_tot += secs
+    value = fl_tot / s_tot / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * s_tot / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": 1, "seq_len": hp.S, "num_heads": hp.H,
+                   "head_dim": 128, "prefix_len": hp.P, "target_len": hp.N,
+                   "step": "bounded sample of prefill + prefix decode rows (oracle)"},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cpu_threads(),
+                         "kind": "oracle", "sample": "each step: " + desc},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

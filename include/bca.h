@@ -1,0 +1,157 @@
+/*
+ * bca.h -- block-causal attention with a prefix K/V cache, for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libbca_gb300.so.  Every pointer argument marked "device" is a CUDA
+ * device pointer owned by the caller; the library never allocates device
+ * memory except where an entry point says so.  All calls are asynchronous on
+ * the given stream (a cudaStream_t passed as void*; NULL = legacy default
+ * stream).  Host-side argument errors return a nonzero status before anything
+ * is launched.  Errors that can only be seen on the device (block ids,
+ * cu_seqlens contents, cache capacity, a bounded wait that ran out) are
+ * written to *status_dev (first error wins) when status_dev is not NULL; read
+ * them with bca_read_device_status().  status_dev must be zeroed by the
+ * caller before first use; the library only ever writes nonzero codes to it.
+ *
+ * Tensor conventions (all row-major, contiguous):
+ *   q, k, v, out   bf16 [total, H, 128]   token stride H*128 elements
+ *   lse            fp32 [H, total_q]      natural log, over scaled scores
+ *   cache_k/v      bf16 [num_layers][H][capacity][128]
+ *   block_id       int32 [total_k]        -1 = text, >= 0 = image block id
+ *   cu_seqlens_*   int32 [batch+1]        packed varlen offsets (device)
+ * Device pointers must be 16-byte aligned.  head_dim must be 128.
+ *
+ * Source of the operations (page title, section):
+ *   "Qwen-Image 2.1 deployment notes" (10100.com), "Block-Causal mask" and the
+ *   piecewise-attention paragraph; "Qwen-Image 2.1: Block-Causal Attention,
+ *   Prefix KV Cache, and Turbo" (flozi.net), sections "Block-causal attention
+ *   is the cache-enabling boundary", "Timestep-zero conditioning makes the
+ *   prefix invariant", "The prefix cache is a compute-for-memory trade" and
+ *   "Two exact attention paths"; SenseNova-U1 inference-infra notes,
+ *   "NEO-Unify 多模态 Prefill 的注意力" (per-M-block K-range extension).
+ */
+#ifndef BCA_GB300_H
+#define BCA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t bca_status;
+
+enum {
+  BCA_OK = 0,
+  BCA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, bad scale      */
+  BCA_ERR_UNSUPPORTED = 2,   /* head_dim != 128, too many image runs in one sequence   */
+  BCA_ERR_BLOCK_ID = 3,      /* id < -1, or one image id split over separate runs      */
+  BCA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than bca_prefill_workspace_bytes */
+  BCA_ERR_CAPACITY = 5,      /* cache overflow: cu_prefix[batch] > capacity            */
+  BCA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, ...)    */
+  BCA_ERR_TIMEOUT = 7,       /* a bounded device wait ran out; outputs are undefined   */
+  BCA_ERR_SEQLENS = 8        /* cu_seqlens not monotone, q_len > kv_len, or a length
+                                above max_seqlen_*                                     */
+};
+
+/* Human-readable name of a status code (static string). */
+const char* bca_status_string(bca_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t bca_version(void);
+
+/* Copies *status_dev to the host after synchronising `stream`; returns it
+ * (BCA_ERR_CUDA if the copy itself failed). */
+bca_status bca_read_device_status(const int32_t* status_dev, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Schedule preparation (the O(S) replacement of the O(S^2) mask).
+ *
+ * For every query row r of sequence b (q_len = cu_q[b+1]-cu_q[b], kv_len =
+ * cu_k[b+1]-cu_k[b], position p = kv_len - q_len + i: bottom-right alignment)
+ * the visible keys are exactly [0, e(r)), e(r) = p+1 for a text row and the
+ * exclusive end of p's image run for an image row ("an image block [a,b) sees
+ * everything before it plus its own block", 10100.com, "Block-Causal mask").
+ * Validates that every id >= 0 forms one contiguous run per sequence.
+ *
+ *   row_end  device int32 [total_q]  out: e(r), relative to the sequence's first key
+ *   tiles    device int32 [batch * tiles_per_seq * 4] out, tiles_per_seq =
+ *            ceil(max_seqlen_q / 128); record (b, m) = {k_hi = max e over
+ *            the tile's valid rows, k_min = min e, valid rows, 0}; all zero
+ *            for a tile past the sequence end or a sequence that failed
+ *            validation.
+ */
+bca_status bca_schedule_prep(const int32_t* block_id, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, int32_t batch, int32_t max_seqlen_q,
+                             int32_t* row_end, int32_t* tiles, int32_t* status_dev,
+                             void* stream);
+
+/* Bytes of device workspace bca_prefill needs (row_end + tile records). */
+size_t bca_prefill_workspace_bytes(int32_t batch, int32_t total_q, int32_t max_seqlen_q);
+
+/* ------------------------------------------------------------------------ */
+/* Block-causal multi-head attention forward over packed varlen sequences.
+ *
+ * visible(i, j) = (p_i >= j) or (bid[p_i] >= 0 and bid[p_i] == bid[j]) with
+ * p_i = kv_len - q_len + i (10100.com "Block-Causal mask"; flozi.net
+ * "Block-causal attention is the cache-enabling boundary"; bottom-right
+ * alignment from 10100.com's piecewise-attention paragraph).
+ *   out[r, h, :] = sum_j softmax_j(scale * q_r . k_j | visible) v_j      (bf16)
+ *   lse[h, r]    = ln sum_j exp(scale * q_r . k_j | visible)             (fp32)
+ * q: device bf16 [total_q, H, 128]; k, v: device bf16 [total_k, H, 128];
+ * block_id: device int32 [total_k]; cu_seqlens_q/k: device int32 [batch+1];
+ * out: device bf16 [total_q, H, 128]; lse: device fp32 [H, total_q];
+ * workspace: device, >= bca_prefill_workspace_bytes(batch, total_q, max_seqlen_q).
+ * A sequence that fails validation gets no output (its rows are left as they were).
+ */
+bca_status bca_prefill(const void* q, const void* k, const void* v, const int32_t* block_id,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
+                       int32_t batch, int32_t num_heads, int32_t head_dim,
+                       int32_t total_q, int32_t total_k, int32_t max_seqlen_q,
+                       int32_t max_seqlen_k, float softmax_scale, void* out, float* lse,
+                       void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                       void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Prefix-cache "decode" (cached denoising steps): the target queries of every
+ * sequence attend, with no mask, over [cached prefix K/V; their own K/V]
+ * (flozi.net "Timestep-zero conditioning makes the prefix invariant": later
+ * steps concatenate cached prefix K/V with fresh target K/V; "Two exact
+ * attention paths": cached steps need no block-causal mask).
+ *
+ * q_tgt, k_tgt, v_tgt: device bf16 [total_q, H, 128] packed by cu_seqlens_q;
+ * cache_k/v: device bf16 [num_layers][H][capacity][128]; sequence b's prefix
+ * is cache tokens cu_prefix[b] .. cu_prefix[b+1]-1 of layer `layer`;
+ * cu_prefix: device int32 [batch+1]; out/lse as in bca_prefill.
+ * max_prefix bounds cu_prefix[b+1]-cu_prefix[b].
+ */
+bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void* cache_v,
+                             int32_t layer, int32_t num_layers, int64_t capacity,
+                             const int32_t* cu_prefix, const void* k_tgt, const void* v_tgt,
+                             const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
+                             int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
+                             int32_t max_prefix, float softmax_scale, void* out, float* lse,
+                             int32_t* status_dev, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Prefix cache append (the "extract" step): clone the first
+ * cu_prefix[b+1]-cu_prefix[b] keys and values of every sequence b into cache
+ * tokens cu_prefix[b].. of layer `layer` (flozi.net "Timestep-zero
+ * conditioning makes the prefix invariant": the cache stores post-RoPE prefix
+ * K/V per layer as a clone of the slices, not a view; "The prefix cache is a
+ * compute-for-memory trade": two tensors per layer, H heads x 128 values).
+ * k, v: device bf16 [total_k, H, 128] packed by cu_seqlens_k; cache_k/v:
+ * device bf16 [num_layers][H][capacity][128].  Nothing is written when
+ * cu_prefix[batch] > capacity (BCA_ERR_CAPACITY) or a prefix is longer than
+ * its sequence (BCA_ERR_SEQLENS).
+ */
+bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* cu_seqlens_k,
+                                   const int32_t* cu_prefix, int32_t batch, int32_t num_heads,
+                                   int32_t head_dim, int32_t total_k, void* cache_k,
+                                   void* cache_v, int32_t layer, int32_t num_layers,
+                                   int64_t capacity, int32_t* status_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BCA_GB300_H */

@@ -122,7 +122,6 @@ def prefill(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, softmax_scale: float,
 
     Returns ``out [n_rows, n_heads, D]`` and ``lse [n_heads, n_rows]`` (float64).
     """
-    q, k, v = _f64(q), _f64(k), _f64(v)
     bid = _i64(block_id)
     cq, ck = _i64(cu_seqlens_q), _i64(cu_seqlens_k)
     H, D = q.shape[1], q.shape[2]
@@ -135,12 +134,12 @@ def prefill(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, softmax_scale: float,
         sel = np.nonzero(seq_of_row == b)[0]
         q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
         local = rows[sel] - q0
-        for c in range(0, sel.shape[0], ROW_CHUNK):
-            part = sel[c:c + ROW_CHUNK]
-            mask = visibility(bid[k0:k1], q1 - q0, local[c:c + ROW_CHUNK])
-            for hi, h in enumerate(heads):
-                o, l = masked_attention(q[rows[part], h], k[k0:k1, h], v[k0:k1, h], mask,
-                                        softmax_scale)
+        for hi, h in enumerate(heads):
+            kh, vh = _f64(k[k0:k1, h]), _f64(v[k0:k1, h])   # float64 per (sequence, head)
+            for c in range(0, sel.shape[0], ROW_CHUNK):
+                part = sel[c:c + ROW_CHUNK]
+                mask = visibility(bid[k0:k1], q1 - q0, local[c:c + ROW_CHUNK])
+                o, l = masked_attention(_f64(q[rows[part], h]), kh, vh, mask, softmax_scale)
                 out[part, hi] = o
                 lse[hi, part] = l
     return out, lse
@@ -154,11 +153,9 @@ def prefix_decode(q_tgt, k_prefix, v_prefix, cu_prefix, k_tgt, v_tgt, cu_seqlens
     k_prefix, v_prefix ``[total_prefix, H, D]`` packed by ``cu_prefix``.
     Returns ``out [n_rows, n_heads, D]`` and ``lse [n_heads, n_rows]``.
     """
-    q, kt, vt = _f64(q_tgt), _f64(k_tgt), _f64(v_tgt)
-    kp, vp = _f64(k_prefix), _f64(v_prefix)
     cq, cp = _i64(cu_seqlens_q), _i64(cu_prefix)
-    H, D = q.shape[1], q.shape[2]
-    rows = np.arange(q.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
+    H, D = q_tgt.shape[1], q_tgt.shape[2]
+    rows = np.arange(q_tgt.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
     heads = np.arange(H) if heads is None else np.asarray(heads, dtype=np.int64)
     out = np.zeros((rows.shape[0], heads.shape[0], D))
     lse = np.zeros((heads.shape[0], rows.shape[0]))
@@ -166,12 +163,12 @@ def prefix_decode(q_tgt, k_prefix, v_prefix, cu_prefix, k_tgt, v_tgt, cu_seqlens
     for b in np.unique(seq_of_row):
         sel = np.nonzero(seq_of_row == b)[0]
         for hi, h in enumerate(heads):
-            kk = np.concatenate([kp[cp[b]:cp[b + 1], h], kt[cq[b]:cq[b + 1], h]])
-            vv = np.concatenate([vp[cp[b]:cp[b + 1], h], vt[cq[b]:cq[b + 1], h]])
+            kk = np.concatenate([_f64(k_prefix[cp[b]:cp[b + 1], h]), _f64(k_tgt[cq[b]:cq[b + 1], h])])
+            vv = np.concatenate([_f64(v_prefix[cp[b]:cp[b + 1], h]), _f64(v_tgt[cq[b]:cq[b + 1], h])])
             for c in range(0, sel.shape[0], ROW_CHUNK):
                 part = sel[c:c + ROW_CHUNK]
                 mask = np.ones((part.shape[0], kk.shape[0]), dtype=bool)
-                o, l = masked_attention(q[rows[part], h], kk, vv, mask, softmax_scale)
+                o, l = masked_attention(_f64(q_tgt[rows[part], h]), kk, vv, mask, softmax_scale)
                 out[part, hi] = o
                 lse[hi, part] = l
     return out, lse

@@ -1,0 +1,165 @@
+"""Python binding of the C ABI (``include/bca.h``), for torch CUDA tensors.
+
+Argument marshalling only: shapes and dtypes are checked, outputs and the
+workspace are allocated with torch when not given, raw pointers and the
+current CUDA stream are handed to the library.  Every step of the computation
+runs in the library's kernels; there is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native
+
+HEAD_DIM = 128
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, dim: Optional[int] = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims, got {tuple(t.shape)}")
+
+
+def new_status(device=None) -> torch.Tensor:
+    """A zeroed device status word for the ``status_dev`` arguments."""
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_status(status: torch.Tensor, stream=None) -> int:
+    """Synchronise the stream and return the device status code (0 = ok)."""
+    return int(_native.load().bca_read_device_status(_ptr(status), _stream(stream)))
+
+
+def check_status(status: torch.Tensor, where: str = "device", stream=None) -> None:
+    _native.check(read_status(status, stream), where)
+
+
+def prefill_workspace_bytes(batch: int, total_q: int, max_seqlen_q: int) -> int:
+    return int(_native.load().bca_prefill_workspace_bytes(batch, total_q, max_seqlen_q))
+
+
+def schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, status=None,
+                  stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-row visible-key ends e(r) and per-tile records ``[B, tiles, 4]``."""
+    _need(block_id, "block_id", torch.int32, 1)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    batch = cu_seqlens_q.numel() - 1
+    total_q = int(cu_seqlens_q[-1].item()) if batch > 0 else 0
+    tiles_per_seq = (max_seqlen_q + 127) // 128
+    dev = block_id.device
+    row_end = torch.zeros(total_q, dtype=torch.int32, device=dev)
+    tiles = torch.zeros((batch, tiles_per_seq, 4), dtype=torch.int32, device=dev)
+    code = _native.load().bca_schedule_prep(_ptr(block_id), _ptr(cu_seqlens_q),
+                                            _ptr(cu_seqlens_k), batch, max_seqlen_q,
+                                            _ptr(row_end), _ptr(tiles), _ptr(status),
+                                            _stream(stream))
+    _native.check(code, "bca_schedule_prep")
+    return row_end, tiles
+
+
+def prefill(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+            max_seqlen_k: int, softmax_scale: Optional[float] = None, out=None, lse=None,
+            workspace=None, status=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Block-causal attention forward; returns ``(out [total_q, H, 128] bf16, lse [H, total_q] f32)``."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 3)
+    _need(block_id, "block_id", torch.int32, 1)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    if k.shape != (total_k, H, D) or v.shape != k.shape or block_id.numel() != total_k:
+        raise ValueError("k, v, block_id shapes do not match")
+    batch = cu_seqlens_q.numel() - 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    ws_bytes = prefill_workspace_bytes(batch, total_q, max_seqlen_q)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    code = _native.load().bca_prefill(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(block_id), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        batch, H, D, total_q, total_k, max_seqlen_q, max_seqlen_k, float(softmax_scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefill")
+    return out, lse
+
+
+def prefix_decode(q_tgt, cache_k, cache_v, layer: int, cu_prefix, k_tgt, v_tgt, cu_seqlens_q,
+                  max_seqlen_q: int, max_prefix: int, softmax_scale: Optional[float] = None,
+                  out=None, lse=None, status=None, stream=None):
+    """Target queries over [cached prefix; own K/V], no mask.  Cache ``[L, H, cap, 128]``."""
+    for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
+        _need(t, name, torch.bfloat16, 3)
+    _need(cache_k, "cache_k", torch.bfloat16, 4)
+    _need(cache_v, "cache_v", torch.bfloat16, 4)
+    _need(cu_prefix, "cu_prefix", torch.int32, 1)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    total_q, H, D = q_tgt.shape
+    L, Hc, cap, Dc = cache_k.shape
+    if (Hc, Dc) != (H, D) or cache_v.shape != cache_k.shape:
+        raise ValueError("cache shape does not match q_tgt")
+    if k_tgt.shape != q_tgt.shape or v_tgt.shape != q_tgt.shape:
+        raise ValueError("k_tgt / v_tgt shapes do not match q_tgt")
+    batch = cu_seqlens_q.numel() - 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q_tgt)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    code = _native.load().bca_prefix_decode(
+        _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), layer, L, cap, _ptr(cu_prefix), _ptr(k_tgt),
+        _ptr(v_tgt), _ptr(cu_seqlens_q), batch, H, D, total_q, max_seqlen_q, max_prefix,
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefix_decode")
+    return out, lse
+
+
+def prefix_cache_append(k, v, cu_seqlens_k, cu_prefix, cache_k, cache_v, layer: int,
+                        status=None, stream=None) -> None:
+    """Clone each sequence's prefix K/V into ``cache_{k,v}[layer]`` (``[L, H, cap, 128]``)."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _need(cu_prefix, "cu_prefix", torch.int32, 1)
+    _need(cache_k, "cache_k", torch.bfloat16, 4)
+    _need(cache_v, "cache_v", torch.bfloat16, 4)
+    total_k, H, D = k.shape
+    L, Hc, cap, Dc = cache_k.shape
+    if (Hc, Dc) != (H, D) or cache_v.shape != cache_k.shape or v.shape != k.shape:
+        raise ValueError("shapes do not match")
+    batch = cu_seqlens_k.numel() - 1
+    code = _native.load().bca_prefix_cache_append(
+        _ptr(k), _ptr(v), _ptr(cu_seqlens_k), _ptr(cu_prefix), batch, H, D, total_k,
+        _ptr(cache_k), _ptr(cache_v), layer, L, cap, _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefix_cache_append")

@@ -1,0 +1,547 @@
+// Block-causal attention forward (prefill) and prefix-cache decode for sm_103a.
+//
+// One CTA computes one work item (head h, 128-row query tile m, sequence b):
+//   for each 128-key tile j of the item's K range:
+//     S_j  = Q K_j^T                      tcgen05.mma, bf16 in smem -> fp32 in TMEM
+//     P_j  = exp2(S_j * scale*log2e - m)  softmax warps, one TMEM lane (row) per thread
+//     O   += P_j V_j                      tcgen05.mma, P from TMEM, V from smem
+// with the running max m and sum l kept per row in registers (online softmax).
+//
+// The K range of a prefill tile is [0, k_hi) where k_hi is the largest
+// visible-key end e(r) of the tile's rows: a text row sees [0, p+1), an image
+// row the keys up to the end of its image run (10100.com, "Block-Causal mask";
+// per-M-block K-range extension as in the SenseNova-U1 notes, "NEO-Unify 多模态
+// Prefill 的注意力").  Tiles entirely below min e(r) are mask-free; only the
+// boundary tiles evaluate `key < e(r)`.  Decode reads the cached prefix tiles
+// through one tensor map and the target tiles through another, and masks only
+// the ragged end of each ("Two exact attention paths": cached steps need no
+// block-causal mask).
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax / O correction / epilogue (thread t owns TMEM lane t = query row t)
+//   warp 4     TMA producer (Q once, then K_j, V_j into a ring of smem stages)
+//   warp 5     TMEM allocator and MMA issuer
+// TMEM columns: S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512).
+#include "common.cuh"
+#include "ptx.cuh"
+
+#include <cudaTypedefs.h>
+#include <mutex>
+
+namespace bca {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileBytes = kBlockN * kHeadDim * 2;  // 32 KB: 128 rows x 256 B
+constexpr int kHalfBytes = kTileBytes / 2;          // one 64-column (128 B) half
+constexpr int kThreads = 192;
+constexpr int kSoftmaxThreads = 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+
+struct FwdSmem {
+  uint8_t q[kTileBytes];
+  uint8_t kv[kStages][kTileBytes];
+  uint64_t q_full;
+  uint64_t kv_full[kStages];
+  uint64_t kv_empty[kStages];
+  uint64_t s_full[2];
+  uint64_t s_empty[2];
+  uint64_t p_full[2];
+  uint64_t o_done;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort;
+};
+constexpr size_t kSmemBytes = sizeof(FwdSmem) + 1024;  // + alignment slack
+
+struct FwdParams {
+  int num_heads;
+  int total_q;
+  int tiles_per_seq;
+  float scale_log2;
+  int64_t capacity;
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* row_end;
+  const PrefillTile* tiles;
+  const int32_t* cu_prefix;
+  __nv_bfloat16* out;
+  float* lse;
+  int32_t* status;
+};
+
+// K-major operand (Q, K): 128 rows x 128 bf16 stored as two 128-byte-swizzled
+// halves of 16 KB (columns 0-63, 64-127).  K-step kk covers columns 16kk..16kk+15.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
+  return smem_desc_sw128(base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
+}
+// MN-major operand (V as the B of O += P V): rows = keys (the K dimension),
+// 64-column halves along N (head dim) are 16 KB apart (LBO), 8-key groups are
+// 1024 B apart (SBO).  K-step kk covers keys 16kk..16kk+15.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
+  return smem_desc_sw128(base + kk * 2048, kHalfBytes, 1024);
+}
+
+template <bool kDecode>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_k2,
+                    const __grid_constant__ CUtensorMap tm_v2, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int h = blockIdx.x;
+  const int mt = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+  const int b = blockIdx.z;
+
+  // Another CTA already gave up waiting: do not start new work.
+  if (p.status != nullptr && *reinterpret_cast<volatile int32_t*>(p.status) == BCA_ERR_TIMEOUT)
+    return;
+
+  // ---- the work item (uniform over the CTA) ---------------------------------
+  const int q_seq0 = p.cu_q[b];
+  const int q_len = p.cu_q[b + 1] - q_seq0;
+  if (mt * kBlockM >= q_len) return;
+  const int q_row0 = q_seq0 + mt * kBlockM;
+  const int rows_valid = min(kBlockM, q_len - mt * kBlockM);
+
+  int nk;              // number of key tiles
+  int k_min = 0;       // prefill: tiles below k_min are mask-free for every row
+  int k_hi = 0;
+  int kv_seq0 = 0;     // prefill: first key of the sequence
+  int n_pre = 0;       // decode: prefix keys
+  int pre0 = 0;        // decode: first cache token of the prefix
+  int n_pre_tiles = 0;
+  if constexpr (!kDecode) {
+    const PrefillTile t = p.tiles[b * p.tiles_per_seq + mt];
+    k_hi = t.k_hi;
+    k_min = t.k_min;
+    if (k_hi <= 0) return;  // empty tile, or a sequence that failed validation
+    kv_seq0 = p.cu_k[b];
+    nk = (k_hi + kBlockN - 1) / kBlockN;
+  } else {
+    pre0 = p.cu_prefix[b];
+    const int pre1 = p.cu_prefix[b + 1];
+    n_pre = pre1 - pre0;
+    if (n_pre < 0 || pre0 < 0 || static_cast<int64_t>(pre1) > p.capacity) {
+      if (warp == 0 && lane == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+        report_status(p.status, n_pre < 0 ? BCA_ERR_SEQLENS : BCA_ERR_CAPACITY);
+      return;
+    }
+    n_pre_tiles = (n_pre + kBlockN - 1) / kBlockN;
+    nk = n_pre_tiles + (q_len + kBlockN - 1) / kBlockN;
+  }
+
+  // ---- set-up -----------------------------------------------------------------
+  if (warp == 4 && lane == 0) {
+    mbar_init(&sm.q_full, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.kv_full[s], 1);
+      mbar_init(&sm.kv_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.s_full[i], 1);
+      mbar_init(&sm.s_empty[i], kSoftmaxThreads);
+      mbar_init(&sm.p_full[i], kSoftmaxThreads);
+    }
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.drain, 1);
+    sm.abort = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    if constexpr (kDecode) {
+      tma_prefetch_desc(&tm_k2);
+      tma_prefetch_desc(&tm_v2);
+    }
+  }
+  if (warp == 5) {
+    tmem_alloc(&sm.tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_base;
+  volatile int* abort_flag = &sm.abort;
+
+  auto give_up = [&]() {
+    sm.abort = 1;
+    report_status(p.status, BCA_ERR_TIMEOUT);
+  };
+
+  if (warp == 4) {
+    // =========================== TMA producer ===========================
+    if (lane == 0) {
+      uint32_t armed = 0;   // bit s: stage s has been loaded at least once
+      uint32_t parity = 0;  // bit s: parity of the last load into stage s
+      mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
+      tma_load_3d(&tm_q, &sm.q_full, sm.q, 0, h, q_row0);
+      tma_load_3d(&tm_q, &sm.q_full, sm.q + kHalfBytes, 64, h, q_row0);
+      bool ok = true;
+      for (int i = 0; i < 2 * nk && ok; ++i) {
+        const int j = i >> 1;
+        const bool is_v = i & 1;
+        const int s = i % kStages;
+        const int r = i / kStages;
+        if (r > 0) {
+          if (!mbar_wait(&sm.kv_empty[s], (r - 1) & 1, abort_flag, kWaitLimitNs)) {
+            give_up();
+            ok = false;
+            break;
+          }
+        }
+        mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
+        armed |= 1u << s;
+        parity = (parity & ~(1u << s)) | (static_cast<uint32_t>(r & 1) << s);
+        uint8_t* dst = sm.kv[s];
+        if constexpr (!kDecode) {
+          const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+          const int tok = kv_seq0 + j * kBlockN;
+          tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
+          tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
+        } else {
+          if (j < n_pre_tiles) {
+            const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+            const int tok = pre0 + j * kBlockN;
+            tma_load_3d(m, &sm.kv_full[s], dst, 0, tok, h);
+            tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, tok, h);
+          } else {
+            const CUtensorMap* m = is_v ? &tm_v2 : &tm_k2;
+            const int tok = q_seq0 + (j - n_pre_tiles) * kBlockN;
+            tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
+            tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
+          }
+        }
+      }
+      // If anything went wrong, let every load in flight land before the CTA exits.
+      if (*abort_flag) {
+        for (int s = 0; s < kStages; ++s)
+          if (armed >> s & 1) mbar_wait(&sm.kv_full[s], parity >> s & 1, nullptr, kWaitLimitNs / 4);
+        mbar_wait(&sm.q_full, 0, nullptr, kWaitLimitNs / 4);
+      }
+    }
+  } else if (warp == 5) {
+    // =========================== MMA issuer ===========================
+    constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, kHeadDim, 0, 1);
+    const uint32_t q_base = smem_u32(sm.q);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, abort_flag, kWaitLimitNs));
+    for (int j = 0; j <= nk && ok; ++j) {
+      if (j < nk) {
+        const int i = 2 * j;
+        const int s = i % kStages;
+        ok = mbar_wait(&sm.kv_full[s], (i / kStages) & 1, abort_flag, kWaitLimitNs);
+        if (ok && j >= 2) ok = mbar_wait(&sm.s_empty[j & 1], ((j >> 1) - 1) & 1, abort_flag,
+                                         kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t k_base = smem_u32(sm.kv[s]);
+          const uint32_t d = tmem + kColS + (j & 1) * 128;
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            umma_ss(d, kmajor_desc(q_base, kk), kmajor_desc(k_base, kk), idesc_qk, kk > 0);
+          umma_commit(&sm.s_full[j & 1]);
+          umma_commit(&sm.kv_empty[s]);
+        }
+        __syncwarp();
+      }
+      if (j >= 1) {
+        const int jj = j - 1;
+        const int i = 2 * jj + 1;
+        const int s = i % kStages;
+        ok = mbar_wait(&sm.kv_full[s], (i / kStages) & 1, abort_flag, kWaitLimitNs);
+        if (ok) ok = mbar_wait(&sm.p_full[jj & 1], (jj >> 1) & 1, abort_flag, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        // Keys past the end of the tile's segment may hold anything (another
+        // sequence, unused cache capacity): zero those V rows so 0 * V stays 0.
+        int seg_left;
+        if constexpr (!kDecode) {
+          seg_left = k_hi - jj * kBlockN;
+        } else {
+          seg_left = jj < n_pre_tiles ? n_pre - jj * kBlockN
+                                      : q_len - (jj - n_pre_tiles) * kBlockN;
+        }
+        if (seg_left < kBlockN) {
+          uint8_t* vb = sm.kv[s];
+          const int nrows = kBlockN - seg_left;
+          for (int idx = lane; idx < nrows * 16; idx += 32) {
+            const int row = seg_left + (idx >> 4);
+            const int chunk = idx & 15;
+            *reinterpret_cast<uint4*>(vb + (chunk >> 3) * kHalfBytes + row * 128 +
+                                      (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+        }
+        tc_fence_after();
+        if (lane == 0) {
+          const uint32_t v_base = smem_u32(sm.kv[s]);
+          const uint32_t a = tmem + kColP + (jj & 1) * 64;
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk)
+            umma_ts(tmem + kColO, a + kk * 8, mnmajor_desc(v_base, kk), idesc_pv,
+                    (jj > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&sm.o_done);
+          umma_commit(&sm.kv_empty[s]);
+        }
+        __syncwarp();
+      }
+    }
+    if (!ok && lane == 0) give_up();
+    // Drain: every MMA this thread issued must finish before TMEM is released.
+    if (lane == 0) {
+      umma_commit(&sm.drain);
+      mbar_wait(&sm.drain, 0, nullptr, kWaitLimitNs);
+    }
+    __syncwarp();
+  } else {
+    // =========================== softmax warps ===========================
+    const int row = threadIdx.x;  // == TMEM lane
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const bool row_valid = row < rows_valid;
+    int e_row = 0;
+    if constexpr (!kDecode) e_row = row_valid ? p.row_end[q_row0 + row] : k_hi;
+    const float sl2 = p.scale_log2;
+    float m_run = -INFINITY;
+    float l_run = 0.f;
+    bool ok = true;
+
+    for (int j = 0; j < nk; ++j) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&sm.s_full[j & 1], (j >> 1) & 1, abort_flag, kWaitLimitNs));
+      if (!ok) break;
+      tc_fence_after();
+      float s[kBlockN];
+      {
+        uint32_t r[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(lane_addr + kColS + (j & 1) * 128 + c * 32, r);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sm.s_empty[j & 1]);
+
+      // ---- mask (boundary tiles only) ----
+      int lim;
+      bool need_mask;
+      if constexpr (!kDecode) {
+        lim = e_row - j * kBlockN;
+        need_mask = (j + 1) * kBlockN > k_min;
+      } else {
+        lim = j < n_pre_tiles ? n_pre - j * kBlockN : q_len - (j - n_pre_tiles) * kBlockN;
+        need_mask = lim < kBlockN;
+      }
+      if (need_mask) {
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c)
+          if (c >= lim) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
+      const float m_new = fmaxf(m_run, mx * sl2);
+      const float alpha = ex2_approx(m_run - m_new);
+      const float neg_m = -m_new;
+      float sum = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * c], sl2, neg_m));
+          const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * c + 1], sl2, neg_m));
+          sum += p0 + p1;
+          w[c] = pack_bf16x2(p0, p1);
+        }
+        tmem_st32(lane_addr + kColP + (j & 1) * 64 + half * 32, w);
+      }
+      tmem_st_wait();
+      l_run = l_run * alpha + sum;
+
+      if (j >= 1) {
+        ok = __all_sync(0xffffffffu,
+                        mbar_wait(&sm.o_done, (j - 1) & 1, abort_flag, kWaitLimitNs));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, alpha < 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld32(lane_addr + kColO + c * 32, r);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
+            tmem_st32(lane_addr + kColO + c * 32, r);
+          }
+          tmem_st_wait();
+        }
+      }
+      m_run = m_new;
+      tc_fence_before();
+      mbar_arrive(&sm.p_full[j & 1]);
+    }
+
+    if (ok) {
+      ok = __all_sync(0xffffffffu,
+                      mbar_wait(&sm.o_done, (nk - 1) & 1, abort_flag, kWaitLimitNs));
+    }
+    if (!ok) {
+      if (lane == 0) give_up();
+    } else {
+      tc_fence_after();
+      const float inv_l = 1.f / l_run;
+      __nv_bfloat16* orow =
+          p.out + (static_cast<size_t>(q_row0 + row) * p.num_heads + h) * kHeadDim;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld32(lane_addr + kColO + c * 32, r);
+        uint32_t w[16];
+#pragma unroll
+        for (int x = 0; x < 16; ++x)
+          w[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
+                             __uint_as_float(r[2 * x + 1]) * inv_l);
+        if (row_valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int x = 0; x < 4; ++x)
+            dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+        }
+      }
+      if (row_valid) {
+        p.lse[static_cast<size_t>(h) * p.total_q + q_row0 + row] =
+            (m_run + log2f(l_run)) * 0.69314718055994530942f;
+      }
+    }
+  }
+
+  // ---- teardown ------------------------------------------------------------------
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---- host side ---------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Packed [tokens, H, 128] bf16: dims (d, head, token); box (64, 1, 128).
+bool encode_packed(CUtensorMap* m, const void* base, int num_heads, int64_t tokens) {
+  auto fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(num_heads),
+                        static_cast<cuuint64_t>(tokens)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2),
+                           static_cast<cuuint64_t>(num_heads) * kHeadDim * 2};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kBlockN)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// One layer of the cache, [H][capacity][128] bf16: dims (d, token, head); box (64, 128, 1).
+bool encode_cache(CUtensorMap* m, const void* base, int num_heads, int64_t capacity) {
+  auto fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(capacity),
+                        static_cast<cuuint64_t>(num_heads)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim * 2),
+                           static_cast<cuuint64_t>(capacity) * kHeadDim * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBlockN), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
+  CUtensorMap tq, tk, tv, tk2, tv2;
+  bool ok = encode_packed(&tq, a.q, a.num_heads, a.total_q);
+  if (!decode) {
+    ok = ok && encode_packed(&tk, a.k, a.num_heads, a.total_k) &&
+         encode_packed(&tv, a.v, a.num_heads, a.total_k);
+    tk2 = tk;
+    tv2 = tv;
+  } else {
+    const int64_t map_cap = a.capacity > 0 ? a.capacity : 1;
+    ok = ok && encode_cache(&tk, a.k, a.num_heads, map_cap) &&
+         encode_cache(&tv, a.v, a.num_heads, map_cap) &&
+         encode_packed(&tk2, a.k2, a.num_heads, a.total_q) &&
+         encode_packed(&tv2, a.v2, a.num_heads, a.total_q);
+  }
+  if (!ok) return BCA_ERR_CUDA;
+
+  FwdParams p{};
+  p.num_heads = a.num_heads;
+  p.total_q = a.total_q;
+  p.tiles_per_seq = a.tiles_per_seq;
+  p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+  p.capacity = a.capacity;
+  p.cu_q = a.cu_q;
+  p.cu_k = a.cu_k;
+  p.row_end = a.row_end;
+  p.tiles = a.tiles;
+  p.cu_prefix = a.cu_prefix;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.status = a.status;
+
+  dim3 grid(a.num_heads, a.tiles_per_seq, a.batch);
+  cudaError_t err;
+  if (!decode) {
+    static bool attr_set = false;
+    if (!attr_set) {
+      err = cudaFuncSetAttribute(attn_fwd_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+      if (err != cudaSuccess) return BCA_ERR_CUDA;
+      attr_set = true;
+    }
+    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+  } else {
+    static bool attr_set = false;
+    if (!attr_set) {
+      err = cudaFuncSetAttribute(attn_fwd_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+      if (err != cudaSuccess) return BCA_ERR_CUDA;
+      attr_set = true;
+    }
+    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+  }
+  err = cudaGetLastError();
+  return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
+}  // namespace bca

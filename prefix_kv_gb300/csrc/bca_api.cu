@@ -1,0 +1,206 @@
+// The exported C ABI: argument validation, workspace carving and launches.
+#include "common.cuh"
+
+#include <cmath>
+
+namespace {
+
+using namespace bca;
+
+constexpr size_t kAlign = 256;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int tiles_for(int max_seqlen_q) { return (max_seqlen_q + kBlockM - 1) / kBlockM; }
+
+struct PrefillWorkspace {
+  int32_t* row_end;
+  PrefillTile* tiles;
+  size_t bytes;
+};
+
+PrefillWorkspace carve(void* base, int batch, int total_q, int max_seqlen_q) {
+  PrefillWorkspace w{};
+  const size_t row_bytes = round_up(static_cast<size_t>(total_q) * sizeof(int32_t));
+  const size_t tile_bytes =
+      round_up(static_cast<size_t>(batch) * tiles_for(max_seqlen_q) * sizeof(PrefillTile));
+  w.bytes = row_bytes + tile_bytes;
+  if (base != nullptr) {
+    w.row_end = static_cast<int32_t*>(base);
+    w.tiles = reinterpret_cast<PrefillTile*>(static_cast<uint8_t*>(base) + row_bytes);
+  }
+  return w;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bca_status_string(bca_status s) {
+  switch (s) {
+    case BCA_OK: return "ok";
+    case BCA_ERR_INVALID_ARG: return "invalid argument";
+    case BCA_ERR_UNSUPPORTED: return "unsupported (head_dim != 128 or too many image runs)";
+    case BCA_ERR_BLOCK_ID: return "invalid block ids (id < -1 or an id split over several runs)";
+    case BCA_ERR_WORKSPACE: return "workspace missing or too small";
+    case BCA_ERR_CAPACITY: return "prefix cache capacity exceeded";
+    case BCA_ERR_CUDA: return "CUDA runtime error";
+    case BCA_ERR_TIMEOUT: return "device wait timed out";
+    case BCA_ERR_SEQLENS: return "invalid cu_seqlens / lengths";
+    default: return "unknown status";
+  }
+}
+
+int32_t bca_version(void) { return 100; }
+
+bca_status bca_read_device_status(const int32_t* status_dev, void* stream) {
+  if (status_dev == nullptr) return BCA_ERR_INVALID_ARG;
+  int32_t h = 0;
+  auto s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&h, status_dev, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return BCA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return BCA_ERR_CUDA;
+  return h;
+}
+
+size_t bca_prefill_workspace_bytes(int32_t batch, int32_t total_q, int32_t max_seqlen_q) {
+  if (batch < 0 || total_q < 0 || max_seqlen_q < 0) return 0;
+  return carve(nullptr, batch, total_q, max_seqlen_q).bytes;
+}
+
+bca_status bca_schedule_prep(const int32_t* block_id, const int32_t* cu_seqlens_q,
+                             const int32_t* cu_seqlens_k, int32_t batch, int32_t max_seqlen_q,
+                             int32_t* row_end, int32_t* tiles, int32_t* status_dev,
+                             void* stream) {
+  if (batch < 0 || max_seqlen_q < 0) return BCA_ERR_INVALID_ARG;
+  if (batch == 0 || max_seqlen_q == 0) return BCA_OK;
+  if (!block_id || !cu_seqlens_q || !cu_seqlens_k || !row_end || !tiles)
+    return BCA_ERR_INVALID_ARG;
+  if (batch > 65535) return BCA_ERR_UNSUPPORTED;
+  cudaError_t e = launch_schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, batch,
+                                       tiles_for(max_seqlen_q), row_end,
+                                       reinterpret_cast<PrefillTile*>(tiles), status_dev,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
+bca_status bca_prefill(const void* q, const void* k, const void* v, const int32_t* block_id,
+                       const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k, int32_t batch,
+                       int32_t num_heads, int32_t head_dim, int32_t total_q, int32_t total_k,
+                       int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                       void* out, float* lse, void* workspace, size_t workspace_bytes,
+                       int32_t* status_dev, void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads <= 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
+      max_seqlen_k < 0 || max_seqlen_q > max_seqlen_k)
+    return BCA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BCA_ERR_INVALID_ARG;
+  if (batch == 0 || total_q == 0) return BCA_OK;
+  if (total_k == 0) return BCA_ERR_SEQLENS;
+  if (!q || !k || !v || !block_id || !cu_seqlens_q || !cu_seqlens_k || !out || !lse)
+    return BCA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return BCA_ERR_INVALID_ARG;
+  if (num_heads > 65535 || batch > 65535 || tiles_for(max_seqlen_q) > 65535)
+    return BCA_ERR_UNSUPPORTED;
+  PrefillWorkspace w = carve(workspace, batch, total_q, max_seqlen_q);
+  if (workspace == nullptr || workspace_bytes < w.bytes || !aligned16(workspace))
+    return BCA_ERR_WORKSPACE;
+
+  auto s = static_cast<cudaStream_t>(stream);
+  const int tps = tiles_for(max_seqlen_q);
+  if (launch_schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, batch, tps, w.row_end, w.tiles,
+                           status_dev, s) != cudaSuccess)
+    return BCA_ERR_CUDA;
+  AttnLaunch a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.lse = lse;
+  a.batch = batch;
+  a.num_heads = num_heads;
+  a.total_q = total_q;
+  a.total_k = total_k;
+  a.tiles_per_seq = tps;
+  a.softmax_scale = softmax_scale;
+  a.cu_q = cu_seqlens_q;
+  a.cu_k = cu_seqlens_k;
+  a.row_end = w.row_end;
+  a.tiles = w.tiles;
+  a.status = status_dev;
+  return launch_attention(a, /*decode=*/false, s);
+}
+
+bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void* cache_v,
+                             int32_t layer, int32_t num_layers, int64_t capacity,
+                             const int32_t* cu_prefix, const void* k_tgt, const void* v_tgt,
+                             const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
+                             int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
+                             int32_t max_prefix, float softmax_scale, void* out, float* lse,
+                             int32_t* status_dev, void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads <= 0 || total_q < 0 || max_seqlen_q < 0 || max_prefix < 0 ||
+      capacity < 0 || layer < 0 || num_layers <= 0 || layer >= num_layers)
+    return BCA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BCA_ERR_INVALID_ARG;
+  if (batch == 0 || total_q == 0) return BCA_OK;
+  if (!q_tgt || !k_tgt || !v_tgt || !cu_seqlens_q || !out || !lse || !cu_prefix)
+    return BCA_ERR_INVALID_ARG;
+  if (capacity > 0 && (!cache_k || !cache_v)) return BCA_ERR_INVALID_ARG;
+  if (!aligned16(q_tgt) || !aligned16(k_tgt) || !aligned16(v_tgt) || !aligned16(out) ||
+      !aligned16(cache_k) || !aligned16(cache_v))
+    return BCA_ERR_INVALID_ARG;
+  if (num_heads > 65535 || batch > 65535 || tiles_for(max_seqlen_q) > 65535)
+    return BCA_ERR_UNSUPPORTED;
+  const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
+  AttnLaunch a{};
+  a.q = q_tgt;
+  // An empty cache (capacity 0) is never read, since every prefix must then be
+  // empty; its tensor map is pointed at q_tgt only to keep the map valid.
+  a.k = capacity > 0 ? static_cast<const __nv_bfloat16*>(cache_k) + layer * layer_elems : q_tgt;
+  a.v = capacity > 0 ? static_cast<const __nv_bfloat16*>(cache_v) + layer * layer_elems : q_tgt;
+  a.k2 = k_tgt;
+  a.v2 = v_tgt;
+  a.out = out;
+  a.lse = lse;
+  a.batch = batch;
+  a.num_heads = num_heads;
+  a.total_q = total_q;
+  a.total_k = 0;
+  a.tiles_per_seq = tiles_for(max_seqlen_q);
+  a.capacity = capacity;
+  a.softmax_scale = softmax_scale;
+  a.cu_q = cu_seqlens_q;
+  a.cu_prefix = cu_prefix;
+  a.status = status_dev;
+  (void)max_prefix;
+  return launch_attention(a, /*decode=*/true, static_cast<cudaStream_t>(stream));
+}
+
+bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* cu_seqlens_k,
+                                   const int32_t* cu_prefix, int32_t batch, int32_t num_heads,
+                                   int32_t head_dim, int32_t total_k, void* cache_k,
+                                   void* cache_v, int32_t layer, int32_t num_layers,
+                                   int64_t capacity, int32_t* status_dev, void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads <= 0 || total_k < 0 || capacity < 0 || layer < 0 ||
+      num_layers <= 0 || layer >= num_layers)
+    return BCA_ERR_INVALID_ARG;
+  if (batch == 0) return BCA_OK;
+  if (!k || !v || !cu_seqlens_k || !cu_prefix) return BCA_ERR_INVALID_ARG;
+  if (capacity > 0 && (!cache_k || !cache_v)) return BCA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(cache_k) || !aligned16(cache_v))
+    return BCA_ERR_INVALID_ARG;
+  const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
+  cudaError_t e = launch_cache_append(
+      k, v, cu_seqlens_k, cu_prefix, batch, num_heads,
+      static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems,
+      static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, capacity, status_dev,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
+}  // extern "C"

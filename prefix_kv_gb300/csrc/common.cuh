@@ -1,0 +1,62 @@
+// Shared definitions of the CUDA side of the library.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "bca.h"
+
+namespace bca {
+
+constexpr int kHeadDim = 128;
+constexpr int kBlockM = 128;   // query rows per work tile
+constexpr int kBlockN = 128;   // keys per K/V tile
+
+// Bounded device waits give up after this long and report BCA_ERR_TIMEOUT.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+
+__device__ __forceinline__ void report_status(int32_t* status, int32_t code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+struct PrefillTile {  // one record per (sequence, 128-row query tile)
+  int32_t k_hi;       // max visible-key end over the tile's valid rows (0: no work)
+  int32_t k_min;      // min visible-key end over the tile's valid rows
+  int32_t rows;       // valid query rows in the tile
+  int32_t pad;
+};
+
+// ---- host-side launchers (defined in the .cu files) ----------------------------------
+cudaError_t launch_schedule_prep(const int32_t* block_id, const int32_t* cu_q, const int32_t* cu_k,
+                                 int batch, int tiles_per_seq, int32_t* row_end,
+                                 PrefillTile* tiles, int32_t* status, cudaStream_t stream);
+
+struct AttnLaunch {
+  // tensors
+  const void* q;          // [total_q, H, 128]
+  const void* k;          // prefill: [total_k, H, 128]; decode: cache layer slab [H][cap][128]
+  const void* v;
+  const void* k2;         // decode: target K [total_q, H, 128]
+  const void* v2;
+  void* out;
+  float* lse;
+  // sizes
+  int batch, num_heads, total_q, total_k, tiles_per_seq;
+  int64_t capacity;
+  float softmax_scale;
+  // metadata (device)
+  const int32_t* cu_q;
+  const int32_t* cu_k;
+  const int32_t* row_end;
+  const PrefillTile* tiles;
+  const int32_t* cu_prefix;
+  int32_t* status;
+};
+int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream);  // returns bca_status
+
+cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_k,
+                                const int32_t* cu_prefix, int batch, int num_heads,
+                                void* cache_k_layer, void* cache_v_layer, int64_t capacity,
+                                int32_t* status, cudaStream_t stream);
+
+}  // namespace bca
