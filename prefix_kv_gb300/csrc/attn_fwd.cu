@@ -1,11 +1,18 @@
 // Block-causal attention forward (prefill) and prefix-cache decode for sm_103a.
 //
-// One CTA computes one work item (head h, 128-row query tile m, sequence b):
-//   for each 128-key tile j of the item's K range:
-//     S_j  = Q K_j^T                      tcgen05.mma, bf16 in smem -> fp32 in TMEM
-//     P_j  = exp2(S_j * scale*log2e - m)  softmax warps, one TMEM lane (row) per thread
-//     O   += P_j V_j                      tcgen05.mma, P from TMEM, V from smem
-// with the running max m and sum l kept per row in registers (online softmax).
+// One CTA computes one work item: head h and two consecutive 128-row query
+// tiles (Q0, Q1) of sequence b, which share every K/V tile they both need.
+// For each 128-key tile j of the item's K range:
+//   S_i  = Q_i K_j^T                      tcgen05.mma, bf16 smem x smem -> fp32 TMEM
+//   P_i  = exp2(S_i * scale*log2e - m_i)  softmax warpgroup i, one TMEM lane (row) per thread
+//   O_i += P_i V_j                        tcgen05.mma, P_i read from TMEM, V_j from smem
+// The MMA warp issues PV0(j), S0(j+1), PV1(j), S1(j+1), ... so that while one
+// softmax warpgroup turns S into P the tensor core runs the other tile's MMAs.
+// Because S_i(j+1) is issued after PV_i(j), the commit that signals S_i(j+1)
+// also covers PV_i(j): the softmax may rescale O_i right after seeing S_i(j+1).
+// The running max is only moved when a row's max grows by more than 2^8
+// (log2 domain); otherwise the stale max is kept (exact, since O and l share
+// it), so O is rarely rescaled.
 //
 // The K range of a prefill tile is [0, k_hi) where k_hi is the largest
 // visible-key end e(r) of the tile's rows: a text row sees [0, p+1), an image
@@ -17,11 +24,16 @@
 // the ragged end of each ("Two exact attention paths": cached steps need no
 // block-causal mask).
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax / O correction / epilogue (thread t owns TMEM lane t = query row t)
-//   warp 4     TMA producer (Q once, then K_j, V_j into a ring of smem stages)
-//   warp 5     TMEM allocator and MMA issuer
-// TMEM columns: S0 [0,128) S1 [128,256) O [256,384) P0 [384,448) P1 [448,512).
+// Warp roles (384 threads, three warpgroups):
+//   warps 0-3  softmax + epilogue of Q0 (thread t owns TMEM lane t = query row t)
+//   warps 4-7  softmax + epilogue of Q1
+//   warp 8     TMEM allocator and MMA issuer
+//   warp 9     TMA producer (Q0, Q1 once, then K_j, V_j into a ring of smem stages)
+//   warps 10-11 idle
+// Launched at 168 registers per thread; the softmax warpgroups raise theirs to
+// 216 and the MMA/TMA warpgroup drops to 72 (2*128*216 + 128*72 = 384*168).
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_i is
+// written over the first 64 columns of S_i once S_i has been read.
 #include "common.cuh"
 #include "ptx.cuh"
 
@@ -31,29 +43,34 @@
 namespace bca {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kTileBytes = kBlockN * kHeadDim * 2;  // 32 KB: 128 rows x 256 B
 constexpr int kHalfBytes = kTileBytes / 2;          // one 64-column (128 B) half
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kRegsLaunch = 168, kRegsSoftmax = 216, kRegsControl = 72;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kThreads * kRegsLaunch, "register split");
+constexpr int kWarpMma = 8;
+constexpr int kWarpTma = 9;
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+constexpr uint32_t kColS = 0, kColO = 256;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 
 struct FwdSmem {
-  uint8_t q[kTileBytes];
+  uint8_t q[2][kTileBytes];
   uint8_t kv[kStages][kTileBytes];
   uint64_t q_full;
   uint64_t kv_full[kStages];
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
-  uint64_t s_empty[2];
   uint64_t p_full[2];
-  uint64_t o_done;
+  uint64_t o_final[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
 };
 constexpr size_t kSmemBytes = sizeof(FwdSmem) + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct FwdParams {
   int num_heads;
@@ -83,6 +100,10 @@ __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
   return smem_desc_sw128(base + kk * 2048, kHalfBytes, 1024);
 }
 
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitLimitNs));
+}
+
 template <bool kDecode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -97,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.x;
-  const int mt = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
+  const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
   const int b = blockIdx.z;
 
   // Another CTA already gave up waiting: do not start new work.
@@ -107,39 +128,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- the work item (uniform over the CTA) ---------------------------------
   const int q_seq0 = p.cu_q[b];
   const int q_len = p.cu_q[b + 1] - q_seq0;
-  if (mt * kBlockM >= q_len) return;
-  const int q_row0 = q_seq0 + mt * kBlockM;
-  const int rows_valid = min(kBlockM, q_len - mt * kBlockM);
+  int rows_valid[2], nkt[2];
+  int k_min[2] = {0, 0}, k_hi[2] = {0, 0};
+  for (int i = 0; i < 2; ++i) rows_valid[i] = min(kBlockM, max(0, q_len - (2 * pair + i) * kBlockM));
+  if (rows_valid[0] <= 0) return;
 
-  int nk;              // number of key tiles
-  int k_min = 0;       // prefill: tiles below k_min are mask-free for every row
-  int k_hi = 0;
   int kv_seq0 = 0;     // prefill: first key of the sequence
   int n_pre = 0;       // decode: prefix keys
   int pre0 = 0;        // decode: first cache token of the prefix
   int n_pre_tiles = 0;
   if constexpr (!kDecode) {
-    const PrefillTile t = p.tiles[b * p.tiles_per_seq + mt];
-    k_hi = t.k_hi;
-    k_min = t.k_min;
-    if (k_hi <= 0) return;  // empty tile, or a sequence that failed validation
+    for (int i = 0; i < 2; ++i) {
+      nkt[i] = 0;
+      const int m = 2 * pair + i;
+      if (rows_valid[i] > 0 && m < p.tiles_per_seq) {
+        const PrefillTile t = p.tiles[b * p.tiles_per_seq + m];
+        k_hi[i] = t.k_hi;
+        k_min[i] = t.k_min;
+        nkt[i] = (t.k_hi + kBlockN - 1) / kBlockN;
+      }
+    }
+    if (nkt[0] <= 0) return;  // empty tile, or a sequence that failed validation
     kv_seq0 = p.cu_k[b];
-    nk = (k_hi + kBlockN - 1) / kBlockN;
   } else {
     pre0 = p.cu_prefix[b];
     const int pre1 = p.cu_prefix[b + 1];
     n_pre = pre1 - pre0;
     if (n_pre < 0 || pre0 < 0 || static_cast<int64_t>(pre1) > p.capacity) {
-      if (warp == 0 && lane == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
         report_status(p.status, n_pre < 0 ? BCA_ERR_SEQLENS : BCA_ERR_CAPACITY);
       return;
     }
     n_pre_tiles = (n_pre + kBlockN - 1) / kBlockN;
-    nk = n_pre_tiles + (q_len + kBlockN - 1) / kBlockN;
+    const int n_all = n_pre_tiles + (q_len + kBlockN - 1) / kBlockN;
+    for (int i = 0; i < 2; ++i) nkt[i] = rows_valid[i] > 0 ? n_all : 0;
   }
+  const int nk = max(nkt[0], nkt[1]);
+  const int k_hi_all = max(k_hi[0], k_hi[1]);
 
   // ---- set-up -----------------------------------------------------------------
-  if (warp == 4 && lane == 0) {
+  if (warp == kWarpTma && lane == 0) {
     mbar_init(&sm.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
@@ -147,10 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
-      mbar_init(&sm.s_empty[i], kSoftmaxThreads);
       mbar_init(&sm.p_full[i], kSoftmaxThreads);
+      mbar_init(&sm.o_final[i], 1);
     }
-    mbar_init(&sm.o_done, 1);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -162,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_v2);
     }
   }
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
   }
@@ -176,27 +203,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     sm.abort = 1;
     report_status(p.status, BCA_ERR_TIMEOUT);
   };
+  // ring position of load `idx` (K_j = 2j, V_j = 2j + 1)
+  auto stage_of = [](int idx) { return idx % kStages; };
+  auto phase_of = [](int idx) { return static_cast<uint32_t>((idx / kStages) & 1); };
 
-  if (warp == 4) {
+  if (warp >= 8) {
+   regs_decrease<kRegsControl>();
+   if (warp == kWarpTma) {
     // =========================== TMA producer ===========================
     if (lane == 0) {
       uint32_t armed = 0;   // bit s: stage s has been loaded at least once
       uint32_t parity = 0;  // bit s: parity of the last load into stage s
-      mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-      tma_load_3d(&tm_q, &sm.q_full, sm.q, 0, h, q_row0);
-      tma_load_3d(&tm_q, &sm.q_full, sm.q + kHalfBytes, 64, h, q_row0);
-      bool ok = true;
-      for (int i = 0; i < 2 * nk && ok; ++i) {
+      const int n_q = rows_valid[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&sm.q_full, n_q * kTileBytes);
+      for (int i = 0; i < n_q; ++i) {
+        const int row0 = q_seq0 + (2 * pair + i) * kBlockM;
+        tma_load_3d(&tm_q, &sm.q_full, sm.q[i], 0, h, row0);
+        tma_load_3d(&tm_q, &sm.q_full, sm.q[i] + kHalfBytes, 64, h, row0);
+      }
+      for (int i = 0; i < 2 * nk; ++i) {
         const int j = i >> 1;
         const bool is_v = i & 1;
-        const int s = i % kStages;
+        const int s = stage_of(i);
         const int r = i / kStages;
-        if (r > 0) {
-          if (!mbar_wait(&sm.kv_empty[s], (r - 1) & 1, abort_flag, kWaitLimitNs)) {
-            give_up();
-            ok = false;
-            break;
-          }
+        if (r > 0 && !mbar_wait(&sm.kv_empty[s], (r - 1) & 1, abort_flag, kWaitLimitNs)) {
+          give_up();
+          break;
         }
         mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
         armed |= 1u << s;
@@ -207,18 +239,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int tok = kv_seq0 + j * kBlockN;
           tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
           tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
+        } else if (j < n_pre_tiles) {
+          const CUtensorMap* m = is_v ? &tm_v : &tm_k;
+          const int tok = pre0 + j * kBlockN;
+          tma_load_3d(m, &sm.kv_full[s], dst, 0, tok, h);
+          tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, tok, h);
         } else {
-          if (j < n_pre_tiles) {
-            const CUtensorMap* m = is_v ? &tm_v : &tm_k;
-            const int tok = pre0 + j * kBlockN;
-            tma_load_3d(m, &sm.kv_full[s], dst, 0, tok, h);
-            tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, tok, h);
-          } else {
-            const CUtensorMap* m = is_v ? &tm_v2 : &tm_k2;
-            const int tok = q_seq0 + (j - n_pre_tiles) * kBlockN;
-            tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
-            tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
-          }
+          const CUtensorMap* m = is_v ? &tm_v2 : &tm_k2;
+          const int tok = q_seq0 + (j - n_pre_tiles) * kBlockN;
+          tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
+          tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
         }
       }
       // If anything went wrong, let every load in flight land before the CTA exits.
@@ -228,75 +258,92 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(&sm.q_full, 0, nullptr, kWaitLimitNs / 4);
       }
     }
-  } else if (warp == 5) {
+   } else if (warp == kWarpMma) {
     // =========================== MMA issuer ===========================
     constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
     constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, kHeadDim, 0, 1);
-    const uint32_t q_base = smem_u32(sm.q);
-    bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.q_full, 0, abort_flag, kWaitLimitNs));
-    for (int j = 0; j <= nk && ok; ++j) {
-      if (j < nk) {
-        const int i = 2 * j;
-        const int s = i % kStages;
-        ok = mbar_wait(&sm.kv_full[s], (i / kStages) & 1, abort_flag, kWaitLimitNs);
-        if (ok && j >= 2) ok = mbar_wait(&sm.s_empty[j & 1], ((j >> 1) - 1) & 1, abort_flag,
-                                         kWaitLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
+    auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
+      const uint32_t q_base = smem_u32(sm.q[i]);
+      const uint32_t k_base = smem_u32(sm.kv[stage_of(2 * j)]);
+      const uint32_t d = tmem + kColS + i * 128;
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk)
+        umma_ss(d, kmajor_desc(q_base, kk), kmajor_desc(k_base, kk), idesc_qk, kk > 0);
+      umma_commit(&sm.s_full[i]);
+    };
+    auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j
+      const uint32_t v_base = smem_u32(sm.kv[stage_of(2 * j + 1)]);
+      const uint32_t a = tmem + kColS + i * 128;
+      const uint32_t d = tmem + kColO + i * 128;
+#pragma unroll
+      for (int kk = 0; kk < kBlockN / 16; ++kk)
+        umma_ts(d, a + kk * 8, mnmajor_desc(v_base, kk), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+      if (j == nkt[i] - 1) umma_commit(&sm.o_final[i]);
+    };
+
+    bool ok = warp_wait(&sm.q_full, 0, abort_flag);
+    if (ok && nk > 0) {
+      ok = warp_wait(&sm.kv_full[stage_of(0)], phase_of(0), abort_flag);
+      if (ok) {
         tc_fence_after();
         if (lane == 0) {
-          const uint32_t k_base = smem_u32(sm.kv[s]);
-          const uint32_t d = tmem + kColS + (j & 1) * 128;
-#pragma unroll
-          for (int kk = 0; kk < kHeadDim / 16; ++kk)
-            umma_ss(d, kmajor_desc(q_base, kk), kmajor_desc(k_base, kk), idesc_qk, kk > 0);
-          umma_commit(&sm.s_full[j & 1]);
-          umma_commit(&sm.kv_empty[s]);
+          for (int i = 0; i < 2; ++i)
+            if (nkt[i] > 0) issue_s(i, 0);
+          umma_commit(&sm.kv_empty[stage_of(0)]);
         }
         __syncwarp();
       }
-      if (j >= 1) {
-        const int jj = j - 1;
-        const int i = 2 * jj + 1;
-        const int s = i % kStages;
-        ok = mbar_wait(&sm.kv_full[s], (i / kStages) & 1, abort_flag, kWaitLimitNs);
-        if (ok) ok = mbar_wait(&sm.p_full[jj & 1], (jj >> 1) & 1, abort_flag, kWaitLimitNs);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        // Keys past the end of the tile's segment may hold anything (another
-        // sequence, unused cache capacity): zero those V rows so 0 * V stays 0.
-        int seg_left;
-        if constexpr (!kDecode) {
-          seg_left = k_hi - jj * kBlockN;
-        } else {
-          seg_left = jj < n_pre_tiles ? n_pre - jj * kBlockN
-                                      : q_len - (jj - n_pre_tiles) * kBlockN;
+    }
+    for (int j = 0; j < nk && ok; ++j) {
+      const int vi = 2 * j + 1;
+      ok = warp_wait(&sm.kv_full[stage_of(vi)], phase_of(vi), abort_flag);
+      if (!ok) break;
+      // Keys past the end of the tile's segment may hold anything (another
+      // sequence, unused cache capacity): zero those V rows so 0 * V stays 0.
+      int seg_left;
+      if constexpr (!kDecode) {
+        seg_left = k_hi_all - j * kBlockN;
+      } else {
+        seg_left = j < n_pre_tiles ? n_pre - j * kBlockN : q_len - (j - n_pre_tiles) * kBlockN;
+      }
+      if (seg_left < kBlockN) {
+        uint8_t* vb = sm.kv[stage_of(vi)];
+        const int nrows = kBlockN - seg_left;
+        for (int idx = lane; idx < nrows * 16; idx += 32) {
+          const int row = seg_left + (idx >> 4);
+          const int chunk = idx & 15;
+          *reinterpret_cast<uint4*>(vb + (chunk >> 3) * kHalfBytes + row * 128 +
+                                    (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
         }
-        if (seg_left < kBlockN) {
-          uint8_t* vb = sm.kv[s];
-          const int nrows = kBlockN - seg_left;
-          for (int idx = lane; idx < nrows * 16; idx += 32) {
-            const int row = seg_left + (idx >> 4);
-            const int chunk = idx & 15;
-            *reinterpret_cast<uint4*>(vb + (chunk >> 3) * kHalfBytes + row * 128 +
-                                      (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+      }
+      bool k_next_ready = false;
+      for (int i = 0; i < 2 && ok; ++i) {
+        if (j < nkt[i]) {
+          ok = warp_wait(&sm.p_full[i], j & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          if (lane == 0) issue_pv(i, j);
           __syncwarp();
         }
-        tc_fence_after();
-        if (lane == 0) {
-          const uint32_t v_base = smem_u32(sm.kv[s]);
-          const uint32_t a = tmem + kColP + (jj & 1) * 64;
-#pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk)
-            umma_ts(tmem + kColO, a + kk * 8, mnmajor_desc(v_base, kk), idesc_pv,
-                    (jj > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(&sm.o_done);
-          umma_commit(&sm.kv_empty[s]);
+        if (j + 1 < nkt[i]) {
+          if (!k_next_ready) {
+            ok = warp_wait(&sm.kv_full[stage_of(2 * j + 2)], phase_of(2 * j + 2), abort_flag);
+            if (!ok) break;
+            k_next_ready = true;
+          }
+          tc_fence_after();
+          if (lane == 0) issue_s(i, j + 1);
+          __syncwarp();
         }
-        __syncwarp();
       }
+      if (!ok) break;
+      if (lane == 0) {
+        umma_commit(&sm.kv_empty[stage_of(vi)]);                    // V_j consumed
+        if (k_next_ready) umma_commit(&sm.kv_empty[stage_of(2 * j + 2)]);  // K_{j+1} consumed
+      }
+      __syncwarp();
     }
     if (!ok && lane == 0) give_up();
     // Drain: every MMA this thread issued must finish before TMEM is released.
@@ -305,21 +352,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&sm.drain, 0, nullptr, kWaitLimitNs);
     }
     __syncwarp();
+   }
   } else {
-    // =========================== softmax warps ===========================
-    const int row = threadIdx.x;  // == TMEM lane
-    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    const bool row_valid = row < rows_valid;
+    regs_increase<kRegsSoftmax>();
+    // =========================== softmax warpgroups ===========================
+    const int qi = warp >> 2;               // which query tile
+    const int wq = warp & 3;                // TMEM lane group
+    const int row = wq * 32 + lane;         // == TMEM lane == row within the tile
+    const int n_tiles = nkt[qi];
+    const int row0 = q_seq0 + (2 * pair + qi) * kBlockM;
+    const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
+    const uint32_t s_addr = lane_addr + kColS + qi * 128;
+    const uint32_t o_addr = lane_addr + kColO + qi * 128;
+    const bool row_valid = row < rows_valid[qi];
     int e_row = 0;
-    if constexpr (!kDecode) e_row = row_valid ? p.row_end[q_row0 + row] : k_hi;
+    if constexpr (!kDecode) e_row = row_valid ? p.row_end[row0 + row] : k_hi[qi];
     const float sl2 = p.scale_log2;
-    float m_run = -INFINITY;
+    float m_ref = -INFINITY;   // running (possibly stale) max, log2 domain
     float l_run = 0.f;
     bool ok = true;
 
-    for (int j = 0; j < nk; ++j) {
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&sm.s_full[j & 1], (j >> 1) & 1, abort_flag, kWaitLimitNs));
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = warp_wait(&sm.s_full[qi], j & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
       float s[kBlockN];
@@ -327,20 +381,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t r[32];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          tmem_ld32(lane_addr + kColS + (j & 1) * 128 + c * 32, r);
+          tmem_ld32(s_addr + c * 32, r);
 #pragma unroll
           for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(&sm.s_empty[j & 1]);
-
       // ---- mask (boundary tiles only) ----
       int lim;
       bool need_mask;
       if constexpr (!kDecode) {
         lim = e_row - j * kBlockN;
-        need_mask = (j + 1) * kBlockN > k_min;
+        need_mask = (j + 1) * kBlockN > k_min[qi];
       } else {
         lim = j < n_pre_tiles ? n_pre - j * kBlockN : q_len - (j - n_pre_tiles) * kBlockN;
         need_mask = lim < kBlockN;
@@ -350,65 +401,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBlockN; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx = s[0];
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int c = 1; c < kBlockN; ++c) mx = fmaxf(mx, s[c]);
-      const float m_new = fmaxf(m_run, mx * sl2);
-      const float alpha = ex2_approx(m_run - m_new);
-      const float neg_m = -m_new;
-      float sum = 0.f;
+      for (int c = 4; c < kBlockN; c += 8) {
+        mx0 = fmax3(mx0, s[c], s[c + 1]);
+        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+      }
+      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const bool upd = mx > m_ref + kRescaleThreshold;
+      const float m_new = upd ? mx : m_ref;
+      const float alpha = upd ? ex2_approx(m_ref - m_new) : 1.f;
+      if (j > 0 && __any_sync(0xffffffffu, upd)) {
+        // O_i holds PV_i(0..j-1), all complete (covered by the S_i(j) commit)
+        const float2 a2 = make_float2(alpha, alpha);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c * 32, r);
+#pragma unroll
+          for (int x = 0; x < 32; x += 2) {
+            const float2 v = fmul2(make_float2(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), a2);
+            r[x] = __float_as_uint(v.x);
+            r[x + 1] = __float_as_uint(v.y);
+          }
+          tmem_st32(o_addr + c * 32, r);
+        }
+      }
+      m_ref = m_new;
+      const float2 sl2v = make_float2(sl2, sl2);
+      const float2 negm = make_float2(-m_ref, -m_ref);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t w[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2_approx(fmaf(s[half * 64 + 2 * c], sl2, neg_m));
-          const float p1 = ex2_approx(fmaf(s[half * 64 + 2 * c + 1], sl2, neg_m));
-          sum += p0 + p1;
-          w[c] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < 32; c += 2) {
+          const int base = half * 64 + 2 * c;
+          const float2 x0 = ffma2(make_float2(s[base], s[base + 1]), sl2v, negm);
+          const float2 x1 = ffma2(make_float2(s[base + 2], s[base + 3]), sl2v, negm);
+          const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+          const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+          acc0 = fadd2(acc0, p0);
+          acc1 = fadd2(acc1, p1);
+          w[c] = pack_bf16x2(p0.x, p0.y);
+          w[c + 1] = pack_bf16x2(p1.x, p1.y);
         }
-        tmem_st32(lane_addr + kColP + (j & 1) * 64 + half * 32, w);
+        tmem_st32(s_addr + half * 32, w);
       }
       tmem_st_wait();
-      l_run = l_run * alpha + sum;
-
-      if (j >= 1) {
-        ok = __all_sync(0xffffffffu,
-                        mbar_wait(&sm.o_done, (j - 1) & 1, abort_flag, kWaitLimitNs));
-        if (!ok) break;
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha < 1.f)) {
-#pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            uint32_t r[32];
-            tmem_ld32(lane_addr + kColO + c * 32, r);
-#pragma unroll
-            for (int x = 0; x < 32; ++x) r[x] = __float_as_uint(__uint_as_float(r[x]) * alpha);
-            tmem_st32(lane_addr + kColO + c * 32, r);
-          }
-          tmem_st_wait();
-        }
-      }
-      m_run = m_new;
+      l_run = l_run * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
       tc_fence_before();
-      mbar_arrive(&sm.p_full[j & 1]);
+      mbar_arrive(&sm.p_full[qi]);
     }
 
-    if (ok) {
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&sm.o_done, (nk - 1) & 1, abort_flag, kWaitLimitNs));
-    }
+    if (ok && n_tiles > 0) ok = warp_wait(&sm.o_final[qi], 0, abort_flag);
     if (!ok) {
       if (lane == 0) give_up();
-    } else {
+    } else if (n_tiles > 0) {
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       __nv_bfloat16* orow =
-          p.out + (static_cast<size_t>(q_row0 + row) * p.num_heads + h) * kHeadDim;
+          p.out + (static_cast<size_t>(row0 + row) * p.num_heads + h) * kHeadDim;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t r[32];
-        tmem_ld32(lane_addr + kColO + c * 32, r);
+        tmem_ld32(o_addr + c * 32, r);
         uint32_t w[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x)
@@ -422,8 +481,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_valid) {
-        p.lse[static_cast<size_t>(h) * p.total_q + q_row0 + row] =
-            (m_run + log2f(l_run)) * 0.69314718055994530942f;
+        p.lse[static_cast<size_t>(h) * p.total_q + row0 + row] =
+            (m_ref + log2f(l_run)) * 0.69314718055994530942f;
       }
     }
   }
@@ -431,7 +490,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- teardown ------------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -517,7 +576,7 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   p.lse = a.lse;
   p.status = a.status;
 
-  dim3 grid(a.num_heads, a.tiles_per_seq, a.batch);
+  dim3 grid(a.num_heads, (a.tiles_per_seq + 1) / 2, a.batch);
   cudaError_t err;
   if (!decode) {
     static bool attr_set = false;
