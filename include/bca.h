@@ -44,7 +44,7 @@ typedef int32_t bca_status;
 enum {
   BCA_OK = 0,
   BCA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, bad scale      */
-  BCA_ERR_UNSUPPORTED = 2,   /* head_dim != 128, too many image runs in one sequence   */
+  BCA_ERR_UNSUPPORTED = 2,   /* head_dim != 128, more than 1024 image runs in a sequence */
   BCA_ERR_BLOCK_ID = 3,      /* id < -1, or one image id split over separate runs      */
   BCA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than bca_prefill_workspace_bytes */
   BCA_ERR_CAPACITY = 5,      /* cache overflow: cu_prefix[batch] > capacity            */
@@ -72,7 +72,8 @@ bca_status bca_read_device_status(const int32_t* status_dev, void* stream);
  * the visible keys are exactly [0, e(r)), e(r) = p+1 for a text row and the
  * exclusive end of p's image run for an image row ("an image block [a,b) sees
  * everything before it plus its own block", 10100.com, "Block-Causal mask").
- * Validates that every id >= 0 forms one contiguous run per sequence.
+ * Validates that every id >= 0 forms one contiguous run per sequence (at most
+ * 1024 image runs per sequence; more gives BCA_ERR_UNSUPPORTED).
  *
  *   row_end  device int32 [total_q]  out: e(r), relative to the sequence's first key
  *   tiles    device int32 [batch * tiles_per_seq * 4] out, tiles_per_seq =

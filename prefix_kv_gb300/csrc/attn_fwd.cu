@@ -29,9 +29,10 @@
 //   warps 4-7  softmax + epilogue of Q1
 //   warp 8     TMEM allocator and MMA issuer
 //   warp 9     TMA producer (Q0, Q1 once, then K_j, V_j into a ring of smem stages)
-//   warps 10-11 idle
+//   warp 10    V tail fix-up (zeroes V rows past the end of a key segment)
+//   warp 11    idle
 // Launched at 168 registers per thread; the softmax warpgroups raise theirs to
-// 216 and the MMA/TMA warpgroup drops to 72 (2*128*216 + 128*72 = 384*168).
+// 208 and the control warpgroup drops to 88 (2*128*208 + 128*88 = 384*168).
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_i is
 // written over the first 64 columns of S_i once S_i has been read.
 #include "common.cuh"
@@ -47,10 +48,11 @@ constexpr int kStages = 5;
 constexpr int kTileBytes = kBlockN * kHeadDim * 2;  // 32 KB: 128 rows x 256 B
 constexpr int kHalfBytes = kTileBytes / 2;          // one 64-column (128 B) half
 constexpr int kThreads = 384;
-constexpr int kRegsLaunch = 168, kRegsSoftmax = 216, kRegsControl = 72;
+constexpr int kRegsLaunch = 168, kRegsSoftmax = 208, kRegsControl = 88;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kThreads * kRegsLaunch, "register split");
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;
+constexpr int kWarpFix = 10;
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -65,6 +67,8 @@ struct FwdSmem {
   uint64_t s_full[2];
   uint64_t p_full[2];
   uint64_t o_final[2];
+  uint64_t fix_req;     // MMA thread saw a tail V tile land: fix-up warp may zero it
+  uint64_t v_fixed;     // fix-up warp zeroed the tail rows of that V tile
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -165,6 +169,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int nk = max(nkt[0], nkt[1]);
   const int k_hi_all = max(k_hi[0], k_hi[1]);
+  // valid keys left in K/V tile j's segment (>= 128: the tile is full)
+  auto seg_left_of = [&](int j) {
+    if constexpr (!kDecode) {
+      return k_hi_all - j * kBlockN;
+    } else {
+      return j < n_pre_tiles ? n_pre - j * kBlockN : q_len - (j - n_pre_tiles) * kBlockN;
+    }
+  };
 
   // ---- set-up -----------------------------------------------------------------
   if (warp == kWarpTma && lane == 0) {
@@ -178,6 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sm.p_full[i], kSoftmaxThreads);
       mbar_init(&sm.o_final[i], 1);
     }
+    mbar_init(&sm.fix_req, 1);
+    mbar_init(&sm.v_fixed, 1);
     mbar_init(&sm.drain, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -260,98 +274,105 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
    } else if (warp == kWarpMma) {
     // =========================== MMA issuer ===========================
-    constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
-    constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, kHeadDim, 0, 1);
-    auto issue_s = [&](int i, int j) {  // S_i = Q_i K_j^T
-      const uint32_t q_base = smem_u32(sm.q[i]);
-      const uint32_t k_base = smem_u32(sm.kv[stage_of(2 * j)]);
-      const uint32_t d = tmem + kColS + i * 128;
+    // One thread issues everything; waits are single-thread so no warp-wide
+    // synchronisation sits between MMA groups.
+    if (lane == 0) {
+      constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
+      constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, kHeadDim, 0, 1);
+      // descriptor start fields are in 16-byte units; a stage is kTileBytes / 16 apart
+      const uint64_t desc_q[2] = {smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024),
+                                  smem_desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
+      const uint64_t desc_k0 = smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024);
+      const uint64_t desc_v0 = smem_desc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);
+      auto issue_s = [&](int i, int stage) {  // S_i = Q_i K^T
+        const uint64_t dk = desc_k0 + static_cast<uint64_t>(stage) * (kTileBytes >> 4);
+        const uint32_t d = tmem + kColS + i * 128;
 #pragma unroll
-      for (int kk = 0; kk < kHeadDim / 16; ++kk)
-        umma_ss(d, kmajor_desc(q_base, kk), kmajor_desc(k_base, kk), idesc_qk, kk > 0);
-      umma_commit(&sm.s_full[i]);
-    };
-    auto issue_pv = [&](int i, int j) {  // O_i += P_i V_j
-      const uint32_t v_base = smem_u32(sm.kv[stage_of(2 * j + 1)]);
-      const uint32_t a = tmem + kColS + i * 128;
-      const uint32_t d = tmem + kColO + i * 128;
+        for (int kk = 0; kk < kHeadDim / 16; ++kk) {
+          const uint64_t off = static_cast<uint64_t>((kk >> 2) * (kHalfBytes >> 4) + (kk & 3) * 2);
+          umma_ss(d, desc_q[i] + off, dk + off, idesc_qk, kk > 0);
+        }
+        umma_commit(&sm.s_full[i]);
+      };
+      auto issue_pv = [&](int i, int stage, int j) {  // O_i += P_i V
+        const uint64_t dv = desc_v0 + static_cast<uint64_t>(stage) * (kTileBytes >> 4);
+        const uint32_t a = tmem + kColS + i * 128;
+        const uint32_t d = tmem + kColO + i * 128;
 #pragma unroll
-      for (int kk = 0; kk < kBlockN / 16; ++kk)
-        umma_ts(d, a + kk * 8, mnmajor_desc(v_base, kk), idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-      if (j == nkt[i] - 1) umma_commit(&sm.o_final[i]);
-    };
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          umma_ts(d, a + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_pv,
+                  (j > 0 || kk > 0) ? 1u : 0u);
+        if (j == nkt[i] - 1) umma_commit(&sm.o_final[i]);
+      };
 
-    bool ok = warp_wait(&sm.q_full, 0, abort_flag);
-    if (ok && nk > 0) {
-      ok = warp_wait(&sm.kv_full[stage_of(0)], phase_of(0), abort_flag);
-      if (ok) {
-        tc_fence_after();
-        if (lane == 0) {
+      bool ok = mbar_wait(&sm.q_full, 0, abort_flag, kWaitLimitNs);
+      if (ok && nk > 0) {
+        ok = mbar_wait(&sm.kv_full[stage_of(0)], phase_of(0), abort_flag, kWaitLimitNs);
+        if (ok) {
           for (int i = 0; i < 2; ++i)
-            if (nkt[i] > 0) issue_s(i, 0);
+            if (nkt[i] > 0) issue_s(i, stage_of(0));
           umma_commit(&sm.kv_empty[stage_of(0)]);
         }
-        __syncwarp();
       }
-    }
-    for (int j = 0; j < nk && ok; ++j) {
-      const int vi = 2 * j + 1;
-      ok = warp_wait(&sm.kv_full[stage_of(vi)], phase_of(vi), abort_flag);
-      if (!ok) break;
-      // Keys past the end of the tile's segment may hold anything (another
-      // sequence, unused cache capacity): zero those V rows so 0 * V stays 0.
-      int seg_left;
-      if constexpr (!kDecode) {
-        seg_left = k_hi_all - j * kBlockN;
-      } else {
-        seg_left = j < n_pre_tiles ? n_pre - j * kBlockN : q_len - (j - n_pre_tiles) * kBlockN;
-      }
-      if (seg_left < kBlockN) {
-        uint8_t* vb = sm.kv[stage_of(vi)];
-        const int nrows = kBlockN - seg_left;
-        for (int idx = lane; idx < nrows * 16; idx += 32) {
-          const int row = seg_left + (idx >> 4);
-          const int chunk = idx & 15;
-          *reinterpret_cast<uint4*>(vb + (chunk >> 3) * kHalfBytes + row * 128 +
-                                    (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
+      int tails = 0;
+      for (int j = 0; j < nk && ok; ++j) {
+        const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
+        const bool has_next = j + 1 < nk;
+        ok = mbar_wait(&sm.kv_full[vs], phase_of(2 * j + 1), abort_flag, kWaitLimitNs);
+        if (ok && seg_left_of(j) < kBlockN) {  // the fix-up warp zeroes V rows past the segment
+          mbar_arrive(&sm.fix_req);
+          ok = mbar_wait(&sm.v_fixed, tails & 1, abort_flag, kWaitLimitNs);
+          ++tails;
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-      }
-      bool k_next_ready = false;
-      for (int i = 0; i < 2 && ok; ++i) {
-        if (j < nkt[i]) {
-          ok = warp_wait(&sm.p_full[i], j & 1, abort_flag);
-          if (!ok) break;
-          tc_fence_after();
-          if (lane == 0) issue_pv(i, j);
-          __syncwarp();
-        }
-        if (j + 1 < nkt[i]) {
-          if (!k_next_ready) {
-            ok = warp_wait(&sm.kv_full[stage_of(2 * j + 2)], phase_of(2 * j + 2), abort_flag);
+        if (ok && has_next)
+          ok = mbar_wait(&sm.kv_full[ks], phase_of(2 * j + 2), abort_flag, kWaitLimitNs);
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j < nkt[i]) {
+            ok = mbar_wait(&sm.p_full[i], j & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
-            k_next_ready = true;
+            tc_fence_after();
+            issue_pv(i, vs, j);
           }
-          tc_fence_after();
-          if (lane == 0) issue_s(i, j + 1);
-          __syncwarp();
+          if (j + 1 < nkt[i]) issue_s(i, ks);
         }
+        if (!ok) break;
+        umma_commit(&sm.kv_empty[vs]);                  // V_j consumed
+        if (has_next) umma_commit(&sm.kv_empty[ks]);    // K_{j+1} consumed
       }
-      if (!ok) break;
-      if (lane == 0) {
-        umma_commit(&sm.kv_empty[stage_of(vi)]);                    // V_j consumed
-        if (k_next_ready) umma_commit(&sm.kv_empty[stage_of(2 * j + 2)]);  // K_{j+1} consumed
-      }
-      __syncwarp();
-    }
-    if (!ok && lane == 0) give_up();
-    // Drain: every MMA this thread issued must finish before TMEM is released.
-    if (lane == 0) {
+      if (!ok) give_up();
+      // Drain: every MMA this thread issued must finish before TMEM is released.
       umma_commit(&sm.drain);
       mbar_wait(&sm.drain, 0, nullptr, kWaitLimitNs);
     }
     __syncwarp();
+   } else if (warp == kWarpFix) {
+    // ====================== V tail fix-up ======================
+    // Keys past the end of a tile's segment may hold anything (another
+    // sequence, unused cache capacity): zero those V rows so 0 * V stays 0.
+    // The request comes from the MMA thread after its own wait on the tile's
+    // kv_full phase, so this warp never polls a ring barrier phases behind.
+    int tails = 0;
+    for (int j = 0; j < nk; ++j) {
+      const int seg_left = seg_left_of(j);
+      if (seg_left >= kBlockN) continue;
+      const int vi = 2 * j + 1;
+      if (!warp_wait(&sm.fix_req, tails & 1, abort_flag)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      ++tails;
+      uint8_t* vb = sm.kv[stage_of(vi)];
+      const int nrows = kBlockN - seg_left;
+      for (int idx = lane; idx < nrows * 16; idx += 32) {
+        const int row = seg_left + (idx >> 4);
+        const int chunk = idx & 15;
+        *reinterpret_cast<uint4*>(vb + (chunk >> 3) * kHalfBytes + row * 128 + (chunk & 7) * 16) =
+            make_uint4(0, 0, 0, 0);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.v_fixed);
+    }
    }
   } else {
     regs_increase<kRegsSoftmax>();
@@ -378,13 +399,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       float s[kBlockN];
       {
-        uint32_t r[32];
+        uint32_t r[kBlockN];
+        tmem_ld128(s_addr, r);
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(s_addr + c * 32, r);
-#pragma unroll
-          for (int x = 0; x < 32; ++x) s[c * 32 + x] = __uint_as_float(r[x]);
-        }
+        for (int x = 0; x < kBlockN; ++x) s[x] = __uint_as_float(r[x]);
       }
       // ---- mask (boundary tiles only) ----
       int lim;
@@ -401,15 +419,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < kBlockN; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+      float mxa[8];
 #pragma unroll
-      for (int c = 4; c < kBlockN; c += 8) {
-        mx0 = fmax3(mx0, s[c], s[c + 1]);
-        mx1 = fmax3(mx1, s[c + 2], s[c + 3]);
-        mx2 = fmax3(mx2, s[c + 4], s[c + 5]);
-        mx3 = fmax3(mx3, s[c + 6], s[c + 7]);
+      for (int c = 0; c < 8; ++c) mxa[c] = fmaxf(s[c], s[c + 8]);
+#pragma unroll
+      for (int c = 16; c < kBlockN; c += 16) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mxa[u] = fmax3(mxa[u], s[c + u], s[c + 8 + u]);
       }
-      const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float mx = fmaxf(fmaxf(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5])),
+                             fmaxf(mxa[6], mxa[7])) * sl2;
       const bool upd = mx > m_ref + kRescaleThreshold;
       const float m_new = upd ? mx : m_ref;
       const float alpha = upd ? ex2_approx(m_ref - m_new) : 1.f;
@@ -432,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       m_ref = m_new;
       const float2 sl2v = make_float2(sl2, sl2);
       const float2 negm = make_float2(-m_ref, -m_ref);
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                       make_float2(0.f, 0.f)};
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t w[32];
@@ -443,15 +463,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float2 x1 = ffma2(make_float2(s[base + 2], s[base + 3]), sl2v, negm);
           const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
           const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-          acc0 = fadd2(acc0, p0);
-          acc1 = fadd2(acc1, p1);
+          acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], fadd2(p0, p1));
           w[c] = pack_bf16x2(p0.x, p0.y);
           w[c + 1] = pack_bf16x2(p1.x, p1.y);
         }
         tmem_st32(s_addr + half * 32, w);
       }
       tmem_st_wait();
-      l_run = l_run * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+      const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
+      const float2 asum = fadd2(a01, a23);
+      l_run = l_run * alpha + (asum.x + asum.y);
       tc_fence_before();
       mbar_arrive(&sm.p_full[qi]);
     }

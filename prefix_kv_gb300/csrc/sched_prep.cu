@@ -9,19 +9,23 @@
 // notes, "NEO-Unify 多模态 Prefill 的注意力") and k_min = min e (below it no key
 // tile needs a mask).
 //
-// One CTA per sequence:
-//   1. scan the block ids in chunks, collecting the (sorted) exclusive end of
-//      every image run and its id; reject ids < -1;
+// One CTA of 1024 threads per sequence:
+//   1. stage 8192 block ids at a time in shared memory, mark the last position
+//      of every image run (and reject ids < -1), and append the run ends, in
+//      order, to a shared list with a block-wide scan;
 //   2. reject an id that appears in two separate runs (flozi.net, "Block-causal
 //      attention is the cache-enabling boundary": each image has its own id);
-//   3. e per query row by binary search over the run ends; per-tile min/max.
+//   3. e per query row by binary search over the run ends; per-tile min / max.
 #include "common.cuh"
 
 namespace bca {
 namespace {
 
-constexpr int kPrepThreads = 512;
-constexpr int kMaxRuns = 4096;
+constexpr int kPrepThreads = 1024;
+constexpr int kPerThread = 8;
+constexpr int kChunk = kPrepThreads * kPerThread;  // positions or rows per pass
+constexpr int kMaxRuns = 1024;  // image runs per sequence (BCA_ERR_UNSUPPORTED above)
+constexpr int kWarps = kPrepThreads / 32;
 
 __device__ __forceinline__ int warp_incl_scan(int x) {
   const int lane = threadIdx.x & 31;
@@ -33,17 +37,37 @@ __device__ __forceinline__ int warp_incl_scan(int x) {
   return x;
 }
 
+// Exclusive prefix of `x` over the block; also returns the block total.
+__device__ __forceinline__ int block_excl_scan(int x, int* warp_buf, int& total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int incl = warp_incl_scan(x);
+  if (lane == 31) warp_buf[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int v = warp_buf[lane];
+    const int s = warp_incl_scan(v);
+    warp_buf[lane] = s - v;
+    if (lane == 31) warp_buf[kWarps] = s;
+  }
+  __syncthreads();
+  const int r = warp_buf[wid] + incl - x;
+  total = warp_buf[kWarps];
+  __syncthreads();
+  return r;
+}
+
 __global__ void __launch_bounds__(kPrepThreads)
     schedule_prep_kernel(const int32_t* __restrict__ bid, const int32_t* __restrict__ cu_q,
                          const int32_t* __restrict__ cu_k, int tiles_per_seq,
                          int32_t* __restrict__ row_end, PrefillTile* __restrict__ tiles,
                          int32_t* status) {
+  __shared__ int ids[kChunk + 1];
   __shared__ int run_end[kMaxRuns];
   __shared__ int run_id[kMaxRuns];
-  __shared__ int warp_sum[kPrepThreads / 32];
+  __shared__ int warp_buf[kWarps + 1];
+  __shared__ int red_max[kWarps], red_min[kWarps], red_cnt[kWarps];
   __shared__ int n_runs;
   __shared__ int err;
-  __shared__ int red_max[kPrepThreads / 32], red_min[kPrepThreads / 32], red_cnt[kPrepThreads / 32];
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x;
@@ -63,28 +87,46 @@ __global__ void __launch_bounds__(kPrepThreads)
 
   // ---- 1. image runs ------------------------------------------------------------
   if (err == 0) {
-    for (int base = 0; base < kv_len; base += kPrepThreads) {
-      const int j = base + tid;
-      const bool in = j < kv_len;
-      const int id = in ? bid[k0 + j] : -1;
-      if (in && id < -1) err = BCA_ERR_BLOCK_ID;
-      const bool is_end = in && id >= 0 && (j == kv_len - 1 || bid[k0 + j + 1] != id);
-      const int incl = warp_incl_scan(is_end ? 1 : 0);
-      if (lane == 31) warp_sum[wid] = incl;
+    for (int base = 0; base < kv_len; base += kChunk) {
+      const int n = min(kChunk + 1, kv_len - base);  // + one id past the chunk
+#pragma unroll
+      for (int u = 0; u < kPerThread; ++u) {
+        const int j = u * kPrepThreads + tid;
+        if (j < n) ids[j] = bid[k0 + base + j];
+      }
+      if (tid == 0 && kChunk < n) ids[kChunk] = bid[k0 + base + kChunk];
       __syncthreads();
-      if (wid == 0) {
-        const int v = lane < kPrepThreads / 32 ? warp_sum[lane] : 0;
-        const int s = warp_incl_scan(v);
-        if (lane < kPrepThreads / 32) warp_sum[lane] = s - v;  // exclusive offsets
+      // thread t looks at positions base + 8t .. base + 8t + 7
+      int cnt = 0;
+      unsigned ends = 0;
+#pragma unroll
+      for (int u = 0; u < kPerThread; ++u) {
+        const int jl = tid * kPerThread + u;
+        const int j = base + jl;
+        if (j < kv_len) {
+          const int id = ids[jl];
+          if (id < -1) err = BCA_ERR_BLOCK_ID;
+          if (id >= 0 && (j == kv_len - 1 || ids[jl + 1] != id)) {
+            ends |= 1u << u;
+            ++cnt;
+          }
+        }
+      }
+      int total;
+      int rank = n_runs + block_excl_scan(cnt, warp_buf, total);
+#pragma unroll
+      for (int u = 0; u < kPerThread; ++u) {
+        if (ends >> u & 1) {
+          const int jl = tid * kPerThread + u;
+          if (rank < kMaxRuns) {
+            run_end[rank] = base + jl + 1;
+            run_id[rank] = ids[jl];
+          }
+          ++rank;
+        }
       }
       __syncthreads();
-      const int rank = n_runs + warp_sum[wid] + incl - (is_end ? 1 : 0);
-      if (is_end && rank < kMaxRuns) {
-        run_end[rank] = j + 1;
-        run_id[rank] = id;
-      }
-      __syncthreads();
-      if (tid == kPrepThreads - 1) n_runs = rank + (is_end ? 1 : 0);
+      if (tid == 0) n_runs += total;
       __syncthreads();
     }
     if (tid == 0 && n_runs > kMaxRuns && err == 0) err = BCA_ERR_UNSUPPORTED;
@@ -110,12 +152,13 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
 
   // ---- 3. e per row, min / max per 128-row tile ------------------------------------
+  // pass u handles rows base + u*1024 + tid: each warp owns 32 consecutive rows,
+  // each 128-row tile is four consecutive warps.
   const int R = n_runs;
-  constexpr int kTilesPerPass = kPrepThreads / kBlockM;
-  for (int m0 = 0; m0 < tiles_per_seq; m0 += kTilesPerPass) {
-    const int m = m0 + tid / kBlockM;
-    const int i = m * kBlockM + (tid % kBlockM);
-    const bool valid = m < tiles_per_seq && i < q_len;
+  const int n_tiles_seq = (q_len + kBlockM - 1) / kBlockM;
+  for (int base = 0; base < tiles_per_seq * kBlockM; base += kPrepThreads) {
+    const int i = base + tid;
+    const bool valid = i < q_len;
     int e = 0;
     if (valid) {
       const int pos = kv_len - q_len + i;
@@ -147,16 +190,16 @@ __global__ void __launch_bounds__(kPrepThreads)
       red_cnt[wid] = cnt;
     }
     __syncthreads();
-    if (tid % kBlockM == 0 && m < tiles_per_seq) {
-      const int w0 = tid / 32;
+    const int m = (base + tid * kBlockM) / kBlockM;  // thread t < 8 writes tile base/128 + t
+    if (tid < kPrepThreads / kBlockM && m < tiles_per_seq) {
       int tmax = 0, tmin = 0x7fffffff, tcnt = 0;
-      for (int w = w0; w < w0 + kBlockM / 32; ++w) {
+      for (int w = tid * 4; w < tid * 4 + 4; ++w) {
         tmax = max(tmax, red_max[w]);
         tmin = min(tmin, red_min[w]);
         tcnt += red_cnt[w];
       }
       tiles[b * tiles_per_seq + m] =
-          tcnt > 0 ? PrefillTile{tmax, tmin, tcnt, 0} : PrefillTile{0, 0, 0, 0};
+          (tcnt > 0 && m < n_tiles_seq) ? PrefillTile{tmax, tmin, tcnt, 0} : PrefillTile{0, 0, 0, 0};
     }
     __syncthreads();
   }
