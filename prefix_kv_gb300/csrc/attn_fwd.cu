@@ -10,9 +10,10 @@
 // softmax warpgroup turns S into P the tensor core runs the other tile's MMAs.
 // Because S_i(j+1) is issued after PV_i(j), the commit that signals S_i(j+1)
 // also covers PV_i(j): the softmax may rescale O_i right after seeing S_i(j+1).
-// The running max is only moved when a row's max grows by more than 2^8
-// (log2 domain); otherwise the stale max is kept (exact, since O and l share
-// it), so O is rarely rescaled.
+// The reference max is taken exactly on the first K tile; afterwards P is
+// formed against it directly and the max is only recomputed (with O and l
+// rescaled) for a tile whose row sum would exceed 2^16.  O and l share the
+// reference, so out = O / l is exact, and most tiles take no max at all.
 //
 // The K range of a prefill tile is [0, k_hi) where k_hi is the largest
 // visible-key end e(r) of the tile's rows: a text row sees [0, p+1), an image
@@ -56,7 +57,7 @@ constexpr int kWarpFix = 10;
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
+constexpr float kSumLimit = 65536.0f;  // largest accepted tile row sum relative to m_ref
 
 struct FwdSmem {
   uint8_t q[2][kTileBytes];
@@ -317,27 +318,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tails = 0;
       for (int j = 0; j < nk && ok; ++j) {
         const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
-        const bool has_next = j + 1 < nk;
         ok = mbar_wait(&sm.kv_full[vs], phase_of(2 * j + 1), abort_flag, kWaitLimitNs);
         if (ok && seg_left_of(j) < kBlockN) {  // the fix-up warp zeroes V rows past the segment
           mbar_arrive(&sm.fix_req);
           ok = mbar_wait(&sm.v_fixed, tails & 1, abort_flag, kWaitLimitNs);
           ++tails;
         }
-        if (ok && has_next)
-          ok = mbar_wait(&sm.kv_full[ks], phase_of(2 * j + 2), abort_flag, kWaitLimitNs);
+        bool k_next_ready = false;
         for (int i = 0; i < 2 && ok; ++i) {
           if (j < nkt[i]) {
             ok = mbar_wait(&sm.p_full[i], j & 1, abort_flag, kWaitLimitNs);
             if (!ok) break;
             tc_fence_after();
             issue_pv(i, vs, j);
+            // each ring stage is released right after the last MMA that reads it
+            if (i == 1 || j >= nkt[1]) umma_commit(&sm.kv_empty[vs]);           // V_j
           }
-          if (j + 1 < nkt[i]) issue_s(i, ks);
+          if (j + 1 < nkt[i]) {
+            if (!k_next_ready) {
+              ok = mbar_wait(&sm.kv_full[ks], phase_of(2 * j + 2), abort_flag, kWaitLimitNs);
+              if (!ok) break;
+              k_next_ready = true;
+            }
+            issue_s(i, ks);
+            if (i == 1 || j + 1 >= nkt[1]) umma_commit(&sm.kv_empty[ks]);       // K_{j+1}
+          }
         }
-        if (!ok) break;
-        umma_commit(&sm.kv_empty[vs]);                  // V_j consumed
-        if (has_next) umma_commit(&sm.kv_empty[ks]);    // K_{j+1} consumed
       }
       if (!ok) give_up();
       // Drain: every MMA this thread issued must finish before TMEM is released.
@@ -389,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int e_row = 0;
     if constexpr (!kDecode) e_row = row_valid ? p.row_end[row0 + row] : k_hi[qi];
     const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;   // running (possibly stale) max, log2 domain
+    float m_ref = -INFINITY;   // reference max of the row, log2 domain
     float l_run = 0.f;
     bool ok = true;
 
@@ -397,13 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = warp_wait(&sm.s_full[qi], j & 1, abort_flag);
       if (!ok) break;
       tc_fence_after();
-      float s[kBlockN];
-      {
-        uint32_t r[kBlockN];
-        tmem_ld128(s_addr, r);
-#pragma unroll
-        for (int x = 0; x < kBlockN; ++x) s[x] = __uint_as_float(r[x]);
-      }
+      // S row as 64 register pairs: sp[c] = columns (2c, 2c+1)
+      uint64_t sp[kBlockN / 2];
+      tmem_ld128_pairs(s_addr, sp);
       // ---- mask (boundary tiles only) ----
       int lim;
       bool need_mask;
@@ -416,63 +418,75 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (need_mask) {
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c)
-          if (c >= lim) s[c] = -INFINITY;
+        for (int c = 0; c < kBlockN / 2; ++c) {
+          const float lo = 2 * c < lim ? lo_f(sp[c]) : -INFINITY;
+          const float hi = 2 * c + 1 < lim ? hi_f(sp[c]) : -INFINITY;
+          sp[c] = pack2f(lo, hi);
+        }
       }
-      float mxa[8];
+      // Row max of the tile (log2 domain).
+      auto tile_max = [&]() {
+        float mxa[8];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) mxa[c] = fmaxf(s[c], s[c + 8]);
+        for (int u = 0; u < 8; ++u) mxa[u] = fmaxf(lo_f(sp[u]), hi_f(sp[u]));
 #pragma unroll
-      for (int c = 16; c < kBlockN; c += 16) {
+        for (int c = 8; c < kBlockN / 2; c += 8) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) mxa[u] = fmax3(mxa[u], s[c + u], s[c + 8 + u]);
-      }
-      const float mx = fmaxf(fmaxf(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5])),
-                             fmaxf(mxa[6], mxa[7])) * sl2;
-      const bool upd = mx > m_ref + kRescaleThreshold;
-      const float m_new = upd ? mx : m_ref;
-      const float alpha = upd ? ex2_approx(m_ref - m_new) : 1.f;
-      if (j > 0 && __any_sync(0xffffffffu, upd)) {
+          for (int u = 0; u < 8; ++u) mxa[u] = fmax3(mxa[u], lo_f(sp[c + u]), hi_f(sp[c + u]));
+        }
+        return fmaxf(fmaxf(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5])),
+                     fmaxf(mxa[6], mxa[7])) * sl2;
+      };
+      // P = exp2(S * scale*log2e - m_ref) -> bf16 into the first 64 columns of S_i;
+      // returns the row sum of the fp32 values.
+      auto write_p = [&]() {
+        const uint64_t sl2v = pack2f(sl2, sl2);
+        const uint64_t negm = pack2f(-m_ref, -m_ref);
+        uint64_t acc[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t w[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const uint64_t x = ffma2_b64(sp[half * 32 + c], sl2v, negm);
+            const float p0 = ex2_approx(lo_f(x)), p1 = ex2_approx(hi_f(x));
+            acc[c & 3] = fadd2_b64(acc[c & 3], pack2f(p0, p1));
+            w[c] = pack_bf16x2(p0, p1);
+          }
+          tmem_st32(s_addr + half * 32, w);
+        }
+        tmem_st_wait();
+        const uint64_t asum = fadd2_b64(fadd2_b64(acc[0], acc[1]), fadd2_b64(acc[2], acc[3]));
+        return lo_f(asum) + hi_f(asum);
+      };
+      // The reference max m_ref is the exact row max after the first tile and is
+      // only moved when a tile would make the row sum large (> 2^16 relative to
+      // it): O and l share the reference, so out = O / l is exact either way and
+      // in the common case no max needs to be taken at all.
+      float alpha = 1.f;
+      if (j == 0) m_ref = tile_max();   // key 0 is visible to every row: finite
+      float tsum = write_p();
+      if (j > 0 && __any_sync(0xffffffffu, !(tsum <= kSumLimit))) {
+        const float m_new = fmaxf(m_ref, tile_max());
+        alpha = ex2_approx(m_ref - m_new);
         // O_i holds PV_i(0..j-1), all complete (covered by the S_i(j) commit)
-        const float2 a2 = make_float2(alpha, alpha);
+        const uint64_t a2 = pack2f(alpha, alpha);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
           tmem_ld32(o_addr + c * 32, r);
 #pragma unroll
           for (int x = 0; x < 32; x += 2) {
-            const float2 v = fmul2(make_float2(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), a2);
-            r[x] = __float_as_uint(v.x);
-            r[x + 1] = __float_as_uint(v.y);
+            const uint64_t v = fmul2_b64(pack2f(__uint_as_float(r[x]), __uint_as_float(r[x + 1])), a2);
+            r[x] = __float_as_uint(lo_f(v));
+            r[x + 1] = __float_as_uint(hi_f(v));
           }
           tmem_st32(o_addr + c * 32, r);
         }
+        m_ref = m_new;
+        tsum = write_p();
       }
-      m_ref = m_new;
-      const float2 sl2v = make_float2(sl2, sl2);
-      const float2 negm = make_float2(-m_ref, -m_ref);
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                       make_float2(0.f, 0.f)};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t w[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int base = half * 64 + 2 * c;
-          const float2 x0 = ffma2(make_float2(s[base], s[base + 1]), sl2v, negm);
-          const float2 x1 = ffma2(make_float2(s[base + 2], s[base + 3]), sl2v, negm);
-          const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-          const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-          acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], fadd2(p0, p1));
-          w[c] = pack_bf16x2(p0.x, p0.y);
-          w[c + 1] = pack_bf16x2(p1.x, p1.y);
-        }
-        tmem_st32(s_addr + half * 32, w);
-      }
-      tmem_st_wait();
-      const float2 a01 = fadd2(acc[0], acc[1]), a23 = fadd2(acc[2], acc[3]);
-      const float2 asum = fadd2(a01, a23);
-      l_run = l_run * alpha + (asum.x + asum.y);
+      l_run = l_run * alpha + tsum;
       tc_fence_before();
       mbar_arrive(&sm.p_full[qi]);
     }

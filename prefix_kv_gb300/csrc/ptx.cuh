@@ -32,14 +32,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// A waiting thread may be suspended up to this long per try (it resumes as
+// soon as the phase completes), so waiting warps do not spin on issue slots.
+constexpr uint32_t kTryWaitSuspendNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kTryWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -208,6 +212,18 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, uint32_t (&x)[128]) {
       : "r"(taddr)
       : "memory");
 }
+// As tmem_ld128, returning the 128 columns as 64 aligned register pairs
+// (x[i] = columns 2i, 2i+1) so packed f32x2 arithmetic needs no moves.
+__device__ __forceinline__ void tmem_ld128_pairs(uint32_t taddr, uint64_t (&x)[64]) {
+  asm volatile(
+      "{\n\t.reg .b32 r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15, r16, r17, r18, r19, r20, r21, r22, r23, r24, r25, r26, r27, r28, r29, r30, r31, r32, r33, r34, r35, r36, r37, r38, r39, r40, r41, r42, r43, r44, r45, r46, r47, r48, r49, r50, r51, r52, r53, r54, r55, r56, r57, r58, r59, r60, r61, r62, r63, r64, r65, r66, r67, r68, r69, r70, r71, r72, r73, r74, r75, r76, r77, r78, r79, r80, r81, r82, r83, r84, r85, r86, r87, r88, r89, r90, r91, r92, r93, r94, r95, r96, r97, r98, r99, r100, r101, r102, r103, r104, r105, r106, r107, r108, r109, r110, r111, r112, r113, r114, r115, r116, r117, r118, r119, r120, r121, r122, r123, r124, r125, r126, r127;\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x128.b32 {r0, r1, r2, r3, r4, r5, r6, r7, r8, r9, r10, r11, r12, r13, r14, r15, r16, r17, r18, r19, r20, r21, r22, r23, r24, r25, r26, r27, r28, r29, r30, r31, r32, r33, r34, r35, r36, r37, r38, r39, r40, r41, r42, r43, r44, r45, r46, r47, r48, r49, r50, r51, r52, r53, r54, r55, r56, r57, r58, r59, r60, r61, r62, r63, r64, r65, r66, r67, r68, r69, r70, r71, r72, r73, r74, r75, r76, r77, r78, r79, r80, r81, r82, r83, r84, r85, r86, r87, r88, r89, r90, r91, r92, r93, r94, r95, r96, r97, r98, r99, r100, r101, r102, r103, r104, r105, r106, r107, r108, r109, r110, r111, r112, r113, r114, r115, r116, r117, r118, r119, r120, r121, r122, r123, r124, r125, r126, r127}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;\n\t"
+      "mov.b64 %0, {r0, r1};\n\tmov.b64 %1, {r2, r3};\n\tmov.b64 %2, {r4, r5};\n\tmov.b64 %3, {r6, r7};\n\tmov.b64 %4, {r8, r9};\n\tmov.b64 %5, {r10, r11};\n\tmov.b64 %6, {r12, r13};\n\tmov.b64 %7, {r14, r15};\n\tmov.b64 %8, {r16, r17};\n\tmov.b64 %9, {r18, r19};\n\tmov.b64 %10, {r20, r21};\n\tmov.b64 %11, {r22, r23};\n\tmov.b64 %12, {r24, r25};\n\tmov.b64 %13, {r26, r27};\n\tmov.b64 %14, {r28, r29};\n\tmov.b64 %15, {r30, r31};\n\tmov.b64 %16, {r32, r33};\n\tmov.b64 %17, {r34, r35};\n\tmov.b64 %18, {r36, r37};\n\tmov.b64 %19, {r38, r39};\n\tmov.b64 %20, {r40, r41};\n\tmov.b64 %21, {r42, r43};\n\tmov.b64 %22, {r44, r45};\n\tmov.b64 %23, {r46, r47};\n\tmov.b64 %24, {r48, r49};\n\tmov.b64 %25, {r50, r51};\n\tmov.b64 %26, {r52, r53};\n\tmov.b64 %27, {r54, r55};\n\tmov.b64 %28, {r56, r57};\n\tmov.b64 %29, {r58, r59};\n\tmov.b64 %30, {r60, r61};\n\tmov.b64 %31, {r62, r63};\n\tmov.b64 %32, {r64, r65};\n\tmov.b64 %33, {r66, r67};\n\tmov.b64 %34, {r68, r69};\n\tmov.b64 %35, {r70, r71};\n\tmov.b64 %36, {r72, r73};\n\tmov.b64 %37, {r74, r75};\n\tmov.b64 %38, {r76, r77};\n\tmov.b64 %39, {r78, r79};\n\tmov.b64 %40, {r80, r81};\n\tmov.b64 %41, {r82, r83};\n\tmov.b64 %42, {r84, r85};\n\tmov.b64 %43, {r86, r87};\n\tmov.b64 %44, {r88, r89};\n\tmov.b64 %45, {r90, r91};\n\tmov.b64 %46, {r92, r93};\n\tmov.b64 %47, {r94, r95};\n\tmov.b64 %48, {r96, r97};\n\tmov.b64 %49, {r98, r99};\n\tmov.b64 %50, {r100, r101};\n\tmov.b64 %51, {r102, r103};\n\tmov.b64 %52, {r104, r105};\n\tmov.b64 %53, {r106, r107};\n\tmov.b64 %54, {r108, r109};\n\tmov.b64 %55, {r110, r111};\n\tmov.b64 %56, {r112, r113};\n\tmov.b64 %57, {r114, r115};\n\tmov.b64 %58, {r116, r117};\n\tmov.b64 %59, {r118, r119};\n\tmov.b64 %60, {r120, r121};\n\tmov.b64 %61, {r122, r123};\n\tmov.b64 %62, {r124, r125};\n\tmov.b64 %63, {r126, r127};\n\t}"
+      : "=l"(x[0]), "=l"(x[1]), "=l"(x[2]), "=l"(x[3]), "=l"(x[4]), "=l"(x[5]), "=l"(x[6]), "=l"(x[7]), "=l"(x[8]), "=l"(x[9]), "=l"(x[10]), "=l"(x[11]), "=l"(x[12]), "=l"(x[13]), "=l"(x[14]), "=l"(x[15]), "=l"(x[16]), "=l"(x[17]), "=l"(x[18]), "=l"(x[19]), "=l"(x[20]), "=l"(x[21]), "=l"(x[22]), "=l"(x[23]), "=l"(x[24]), "=l"(x[25]), "=l"(x[26]), "=l"(x[27]), "=l"(x[28]), "=l"(x[29]), "=l"(x[30]), "=l"(x[31]), "=l"(x[32]), "=l"(x[33]), "=l"(x[34]), "=l"(x[35]), "=l"(x[36]), "=l"(x[37]), "=l"(x[38]), "=l"(x[39]), "=l"(x[40]), "=l"(x[41]), "=l"(x[42]), "=l"(x[43]), "=l"(x[44]), "=l"(x[45]), "=l"(x[46]), "=l"(x[47]), "=l"(x[48]), "=l"(x[49]), "=l"(x[50]), "=l"(x[51]), "=l"(x[52]), "=l"(x[53]), "=l"(x[54]), "=l"(x[55]), "=l"(x[56]), "=l"(x[57]), "=l"(x[58]), "=l"(x[59]), "=l"(x[60]), "=l"(x[61]), "=l"(x[62]), "=l"(x[63])
+      : "r"(taddr)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -249,6 +265,27 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
       : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
   return d;
 }
+__device__ __forceinline__ uint64_t ffma2_b64(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2_b64(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t fmul2_b64(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack2f(float lo, float hi) {
+  return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo_f(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
