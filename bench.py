@@ -50,6 +50,33 @@ def load_peaks():
         return {"bf16": 1900.0, "bf16_sustained": 1700.0, "hbm": 6800.0, "source": "fallback"}
 
 
+ATTN_SOURCES = ["prefix_kv_gb300/csrc/attn_fwd.cu", "prefix_kv_gb300/csrc/ptx.cuh",
+                "prefix_kv_gb300/csrc/common.cuh"]
+ATTN_PROFILE = "profiles/attn_fwd_edit_2ref_s12480.md"
+
+
+def profiled_traffic():
+    """DRAM bytes per prefill launch from the committed ncu summary, or None when the
+    attention sources changed since that capture (their sha256 no longer matches)."""
+    import hashlib
+    try:
+        h = hashlib.sha256()
+        for f in ATTN_SOURCES:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        fields = {}
+        with open(os.path.join(ROOT, ATTN_PROFILE)) as fh:
+            for line in fh:
+                if ":" in line and not line.startswith(("#", " ", "|", "*")):
+                    k, v = line.split(":", 1)
+                    fields[k.strip()] = v.strip()
+        if fields.get("source_sha256") != h.hexdigest():
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 class ClockSampler:
     """Samples SM clocks and throttle reasons with nvidia-smi during the timed region."""
 
@@ -366,7 +393,8 @@ def main():
                 "frac": round(pre_tf / peaks["bf16"], 4),
                 "peak_source": f"{peaks['source']} bf16 dense burst",
                 "frac_of_sustained": round(pre_tf / peaks["bf16_sustained"], 4),
-                "traffic": None,
+                "traffic": profiled_traffic(),
+                "traffic_source": ATTN_PROFILE,
                 "algorithmic": f"{prob.flops_prefill:.4e} flop per launch "
                                f"({prob.pairs_prefill} visible pairs/head x 32 heads x 512)"}
     line = {

@@ -65,7 +65,6 @@ __global__ void __launch_bounds__(kPrepThreads)
   __shared__ int run_end[kMaxRuns];
   __shared__ int run_id[kMaxRuns];
   __shared__ int warp_buf[kWarps + 1];
-  __shared__ int red_max[kWarps], red_min[kWarps], red_cnt[kWarps];
   __shared__ int n_runs;
   __shared__ int err;
 
@@ -152,54 +151,70 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
 
   // ---- 3. e per row, min / max per 128-row tile ------------------------------------
-  // pass u handles rows base + u*1024 + tid: each warp owns 32 consecutive rows,
-  // each 128-row tile is four consecutive warps.
+  // A pass covers 8192 rows: sub-pass u handles rows base + u*1024 + tid, so each
+  // warp owns 32 consecutive rows and each 128-row tile is four consecutive warps
+  // of one sub-pass.  All eight block-id loads of a thread are issued up front.
+  __shared__ int red[3][kPerThread][kWarps];
   const int R = n_runs;
   const int n_tiles_seq = (q_len + kBlockM - 1) / kBlockM;
-  for (int base = 0; base < tiles_per_seq * kBlockM; base += kPrepThreads) {
-    const int i = base + tid;
-    const bool valid = i < q_len;
-    int e = 0;
-    if (valid) {
-      const int pos = kv_len - q_len + i;
-      const int id = bid[k0 + pos];
-      if (id < 0) {
-        e = pos + 1;
-      } else {  // first run end > pos
-        int lo = 0, hi = R;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (run_end[mid] > pos) hi = mid; else lo = mid + 1;
-        }
-        e = run_end[lo];
-      }
-      row_end[q0 + i] = e;
-    }
-    int vmax = valid ? e : 0;
-    int vmin = valid ? e : 0x7fffffff;
-    int cnt = valid ? 1 : 0;
+  for (int base = 0; base < tiles_per_seq * kBlockM; base += kChunk) {
+    int ids_row[kPerThread];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-      vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
-      cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+    for (int u = 0; u < kPerThread; ++u) {
+      const int i = base + u * kPrepThreads + tid;
+      ids_row[u] = i < q_len ? bid[k0 + kv_len - q_len + i] : -1;
     }
-    if (lane == 0) {
-      red_max[wid] = vmax;
-      red_min[wid] = vmin;
-      red_cnt[wid] = cnt;
+#pragma unroll
+    for (int u = 0; u < kPerThread; ++u) {
+      const int i = base + u * kPrepThreads + tid;
+      const bool valid = i < q_len;
+      int e = 0;
+      if (valid) {
+        const int pos = kv_len - q_len + i;
+        if (ids_row[u] < 0) {
+          e = pos + 1;
+        } else {  // first run end > pos
+          int lo = 0, hi = R;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (run_end[mid] > pos) hi = mid; else lo = mid + 1;
+          }
+          e = run_end[lo];
+        }
+        row_end[q0 + i] = e;
+      }
+      int vmax = valid ? e : 0;
+      int vmin = valid ? e : 0x7fffffff;
+      int cnt = valid ? 1 : 0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+        vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+      }
+      if (lane == 0) {
+        red[0][u][wid] = vmax;
+        red[1][u][wid] = vmin;
+        red[2][u][wid] = cnt;
+      }
     }
     __syncthreads();
-    const int m = (base + tid * kBlockM) / kBlockM;  // thread t < 8 writes tile base/128 + t
-    if (tid < kPrepThreads / kBlockM && m < tiles_per_seq) {
-      int tmax = 0, tmin = 0x7fffffff, tcnt = 0;
-      for (int w = tid * 4; w < tid * 4 + 4; ++w) {
-        tmax = max(tmax, red_max[w]);
-        tmin = min(tmin, red_min[w]);
-        tcnt += red_cnt[w];
+    // 64 tiles per pass: thread t < 64 reduces sub-pass t/8, warps 4*(t%8) .. +3
+    if (tid < kChunk / kBlockM) {
+      const int u = tid / (kPrepThreads / kBlockM);
+      const int w0 = (tid % (kPrepThreads / kBlockM)) * (kBlockM / 32);
+      const int m = (base + u * kPrepThreads) / kBlockM + tid % (kPrepThreads / kBlockM);
+      if (m < tiles_per_seq) {
+        int tmax = 0, tmin = 0x7fffffff, tcnt = 0;
+        for (int w = w0; w < w0 + kBlockM / 32; ++w) {
+          tmax = max(tmax, red[0][u][w]);
+          tmin = min(tmin, red[1][u][w]);
+          tcnt += red[2][u][w];
+        }
+        tiles[b * tiles_per_seq + m] = (tcnt > 0 && m < n_tiles_seq)
+                                           ? PrefillTile{tmax, tmin, tcnt, 0}
+                                           : PrefillTile{0, 0, 0, 0};
       }
-      tiles[b * tiles_per_seq + m] =
-          (tcnt > 0 && m < n_tiles_seq) ? PrefillTile{tmax, tmin, tcnt, 0} : PrefillTile{0, 0, 0, 0};
     }
     __syncthreads();
   }
