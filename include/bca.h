@@ -113,6 +113,29 @@ bca_status bca_prefill(const void* q, const void* k, const void* v, const int32_
                        void* workspace, size_t workspace_bytes, int32_t* status_dev,
                        void* stream);
 
+/* Same computation as bca_prefill, for callers that cannot allocate device
+ * memory or pass a workspace: for example a plugin inside a runtime that owns
+ * all GPU memory in a pre-planned arena, or a loop that must not take
+ * cudaMalloc's implicit synchronisation.  The pages have no counterpart of
+ * this call; it only changes where the schedule scratch lives.
+ *
+ * The scratch is a fixed 2 MiB array in the library's own device memory, held
+ * by every GPU that loads the library until the process exits.  Problems with
+ * total_q > 262144 or batch * ceil(max_seqlen_q / 128) > 65536 are rejected
+ * with BCA_ERR_WORKSPACE.  The first call on each device looks up the array's
+ * device address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  The call allocates nothing.  All
+ * calls share the array: calls whose kernels may overlap on the GPU (other
+ * streams or host threads) race and must be serialised by the caller.
+ * Arguments, layouts and errors are otherwise those of bca_prefill.
+ */
+bca_status bca_prefill_noalloc(const void* q, const void* k, const void* v,
+                               const int32_t* block_id, const int32_t* cu_seqlens_q,
+                               const int32_t* cu_seqlens_k, int32_t batch, int32_t num_heads,
+                               int32_t head_dim, int32_t total_q, int32_t total_k,
+                               int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                               void* out, float* lse, int32_t* status_dev, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Prefix-cache "decode" (cached denoising steps): the target queries of every
  * sequence attend, with no mask, over [cached prefix K/V; their own K/V]
