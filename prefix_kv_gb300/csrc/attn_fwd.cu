@@ -168,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_all = n_pre_tiles + (q_len + kBlockN - 1) / kBlockN;
     for (int i = 0; i < 2; ++i) nkt[i] = rows_valid[i] > 0 ? n_all : 0;
   }
+  // Row ends never decrease along a sequence, so a present Q1 needs at least as
+  // many key tiles as Q0; keep that invariant explicitly (extra tiles would be
+  // fully masked), since ring stages are released by Q1's softmax (below).
+  if (nkt[1] > 0 && nkt[1] < nkt[0]) nkt[1] = nkt[0];
   const int nk = max(nkt[0], nkt[1]);
   const int k_hi_all = max(k_hi[0], k_hi[1]);
   // valid keys left in K/V tile j's segment (>= 128: the tile is full)
@@ -312,7 +316,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok) {
           for (int i = 0; i < 2; ++i)
             if (nkt[i] > 0) issue_s(i, stage_of(0));
-          umma_commit(&sm.kv_empty[stage_of(0)]);
         }
       }
       int tails = 0;
@@ -331,8 +334,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             issue_pv(i, vs, j);
-            // each ring stage is released right after the last MMA that reads it
-            if (i == 1 || j >= nkt[1]) umma_commit(&sm.kv_empty[vs]);           // V_j
           }
           if (j + 1 < nkt[i]) {
             if (!k_next_ready) {
@@ -341,7 +342,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               k_next_ready = true;
             }
             issue_s(i, ks);
-            if (i == 1 || j + 1 >= nkt[1]) umma_commit(&sm.kv_empty[ks]);       // K_{j+1}
           }
         }
       }
@@ -392,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_addr = lane_addr + kColS + qi * 128;
     const uint32_t o_addr = lane_addr + kColO + qi * 128;
     const bool row_valid = row < rows_valid[qi];
+    const bool releaser = qi == 1 || nkt[1] == 0;
     int e_row = 0;
     if constexpr (!kDecode) e_row = row_valid ? p.row_end[row0 + row] : k_hi[qi];
     const float sl2 = p.scale_log2;
@@ -402,6 +403,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_tiles; ++j) {
       ok = warp_wait(&sm.s_full[qi], j & 1, abort_flag);
       if (!ok) break;
+      // The commit behind S_qi(j) covers every MMA issued before it.  For the
+      // last tile in issue order (Q1, or Q0 alone) that includes all readers
+      // of V_{j-1} and K_j, so their ring stages can be handed back to the
+      // producer here, without a commit on the MMA thread's critical path.
+      if (releaser && wq == 0 && lane == 0) {
+        if (j > 0) mbar_arrive(&sm.kv_empty[stage_of(2 * j - 1)]);   // V_{j-1}
+        mbar_arrive(&sm.kv_empty[stage_of(2 * j)]);                  // K_j
+      }
       tc_fence_after();
       // S row as 64 register pairs: sp[c] = columns (2c, 2c+1)
       uint64_t sp[kBlockN / 2];
