@@ -88,6 +88,8 @@ struct FwdParams {
   const int32_t* row_end;
   const PrefillTile* tiles;
   const int32_t* cu_prefix;
+  int decode_pairs_per_seq;   // decode: tile pairs per sequence (grid decoding)
+  int decode_split_from;      // decode: first item split into single-tile items
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
@@ -122,9 +124,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int h = blockIdx.x;
-  const int pair = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);
-  const int b = blockIdx.z;
+  // Work item: head h, sequence b and its query tiles m_base .. m_base + n_qt - 1.
+  // Prefill: a 3-D grid of (head, tile pair, sequence), costliest pairs first.
+  // Decode: a 1-D list of equal-cost tile pairs; the pairs of a last, partly
+  // filled wave are split into single-tile items so that wave ends sooner.
+  int h, b, m_base, n_qt;
+  if constexpr (!kDecode) {
+    h = blockIdx.x;
+    m_base = 2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y));
+    b = blockIdx.z;
+    n_qt = 2;
+  } else {
+    const int L = blockIdx.x;
+    int item = L, sub = 0;
+    n_qt = 2;
+    if (L >= p.decode_split_from) {
+      item = p.decode_split_from + (L - p.decode_split_from) / 2;
+      sub = (L - p.decode_split_from) & 1;
+      n_qt = 1;
+    }
+    h = item % p.num_heads;
+    const int rest = item / p.num_heads;
+    m_base = 2 * (rest % p.decode_pairs_per_seq) + sub;
+    b = rest / p.decode_pairs_per_seq;
+  }
 
   // Another CTA already gave up waiting: do not start new work.
   if (p.status != nullptr && *reinterpret_cast<volatile int32_t*>(p.status) == BCA_ERR_TIMEOUT)
@@ -135,7 +158,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_len = p.cu_q[b + 1] - q_seq0;
   int rows_valid[2], nkt[2];
   int k_min[2] = {0, 0}, k_hi[2] = {0, 0};
-  for (int i = 0; i < 2; ++i) rows_valid[i] = min(kBlockM, max(0, q_len - (2 * pair + i) * kBlockM));
+  for (int i = 0; i < 2; ++i)
+    rows_valid[i] = i < n_qt ? min(kBlockM, max(0, q_len - (m_base + i) * kBlockM)) : 0;
   if (rows_valid[0] <= 0) return;
 
   int kv_seq0 = 0;     // prefill: first key of the sequence
@@ -145,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (!kDecode) {
     for (int i = 0; i < 2; ++i) {
       nkt[i] = 0;
-      const int m = 2 * pair + i;
+      const int m = m_base + i;
       if (rows_valid[i] > 0 && m < p.tiles_per_seq) {
         const PrefillTile t = p.tiles[b * p.tiles_per_seq + m];
         k_hi[i] = t.k_hi;
@@ -160,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pre1 = p.cu_prefix[b + 1];
     n_pre = pre1 - pre0;
     if (n_pre < 0 || pre0 < 0 || static_cast<int64_t>(pre1) > p.capacity) {
-      if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0)
+      if (threadIdx.x == 0 && h == 0 && m_base == 0)
         report_status(p.status, n_pre < 0 ? BCA_ERR_SEQLENS : BCA_ERR_CAPACITY);
       return;
     }
@@ -236,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_q = rows_valid[1] > 0 ? 2 : 1;
       mbar_arrive_expect_tx(&sm.q_full, n_q * kTileBytes);
       for (int i = 0; i < n_q; ++i) {
-        const int row0 = q_seq0 + (2 * pair + i) * kBlockM;
+        const int row0 = q_seq0 + (m_base + i) * kBlockM;
         tma_load_3d(&tm_q, &sm.q_full, sm.q[i], 0, h, row0);
         tma_load_3d(&tm_q, &sm.q_full, sm.q[i] + kHalfBytes, 64, h, row0);
       }
@@ -387,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;                // TMEM lane group
     const int row = wq * 32 + lane;         // == TMEM lane == row within the tile
     const int n_tiles = nkt[qi];
-    const int row0 = q_seq0 + (2 * pair + qi) * kBlockM;
+    const int row0 = q_seq0 + (m_base + qi) * kBlockM;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_addr = lane_addr + kColS + qi * 128;
     const uint32_t o_addr = lane_addr + kColO + qi * 128;
@@ -621,6 +645,26 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   p.status = a.status;
 
   dim3 grid(a.num_heads, (a.tiles_per_seq + 1) / 2, a.batch);
+  if (decode) {
+    // Equal-cost pair items; when the last wave would be at most half full,
+    // its pairs become single-tile items (two CTAs each, ~0.7x the time).
+    static int sms = 0;
+    if (sms == 0) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 1;
+    }
+    const int pps = (a.tiles_per_seq + 1) / 2;
+    const int64_t items = static_cast<int64_t>(a.num_heads) * pps * a.batch;
+    const int64_t tail = items % sms;
+    const int64_t split_from = (tail > 0 && 2 * tail <= sms) ? items - tail : items;
+    const int64_t ctas = split_from + 2 * (items - split_from);
+    if (ctas > 0x7fffffff) return BCA_ERR_UNSUPPORTED;
+    p.decode_pairs_per_seq = pps;
+    p.decode_split_from = static_cast<int>(split_from);
+    grid = dim3(static_cast<unsigned>(ctas), 1, 1);
+  }
   cudaError_t err;
   if (!decode) {
     static bool attr_set = false;
