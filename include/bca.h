@@ -64,6 +64,16 @@ int32_t bca_version(void);
  * (BCA_ERR_CUDA if the copy itself failed). */
 bca_status bca_read_device_status(const int32_t* status_dev, void* stream);
 
+/* Self-test of the bounded device waits (no counterpart on the pages).  Launches
+ * one CTA whose threads wait on an mbarrier that is never completed: one warp
+ * with limit_ns (1 ns .. 1 s), the others with 50x that limit.  The first
+ * gives up after limit_ns and writes BCA_ERR_TIMEOUT to *status_dev; the
+ * others must see its abort flag and return at once, so the kernel ends after
+ * about limit_ns.  If elapsed_ns_dev is not NULL the device-measured duration
+ * (ns) is written there.  Faults nothing; the context stays usable. */
+bca_status bca_selftest_wait_timeout(uint64_t limit_ns, int32_t* status_dev,
+                                     uint64_t* elapsed_ns_dev, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Schedule preparation (the O(S) replacement of the O(S^2) mask).
  *
