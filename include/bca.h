@@ -185,6 +185,28 @@ bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* 
                                    void* cache_v, int32_t layer, int32_t num_layers,
                                    int64_t capacity, int32_t* status_dev, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* FP8 E4M3 prefix cache ("Qwen-Image 2.1 deployment notes", prefix-cache
+ * section: the prefix cache is stored as FP8 E4M3 with one FP32 scale per token
+ * and attention head, quantising K and V, or V only).  Each (token, head) row
+ * of 128 values is scaled by its absolute maximum onto the E4M3 range, in fp32:
+ *   scale = amax / 448;  code = E4M3(x * (448 / amax)), round to nearest even,
+ *   saturating at +-448 (an all-zero row gets scale 0 and zero codes);
+ * a dequantised value is bf16(fp32(value(code)) * scale).
+ *   BCA_FP8_V : cache_k is bf16 [L][H][cap][128] (copied as in
+ *               bca_prefix_cache_append), cache_v holds E4M3 codes
+ *               uint8 [L][H][cap][128], scale_v fp32 [L][H][cap]; scale_k unused.
+ *   BCA_FP8_KV: cache_k and cache_v hold E4M3 codes, scale_k and scale_v fp32.
+ * Addressing, validation and errors are those of bca_prefix_cache_append. */
+enum { BCA_FP8_V = 1, BCA_FP8_KV = 2 };
+
+bca_status bca_prefix_cache_append_fp8(const void* k, const void* v, const int32_t* cu_seqlens_k,
+                                       const int32_t* cu_prefix, int32_t batch, int32_t num_heads,
+                                       int32_t head_dim, int32_t total_k, int32_t mode,
+                                       void* cache_k, void* cache_v, float* scale_k,
+                                       float* scale_v, int32_t layer, int32_t num_layers,
+                                       int64_t capacity, int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -49,7 +49,8 @@ _POS_CODES, _POS_VALS = _all_finite_values()
 
 def e4m3_encode(x) -> np.ndarray:
     """Round float values to E4M3 codes: nearest, ties to the even code
-    (mantissa LSB 0), magnitudes above 448 saturate to 448, NaN -> 0x7F."""
+    (mantissa LSB 0), magnitudes above 448 saturate to 448, the sign is kept
+    (negative values that round to zero give -0, code 0x80), NaN -> 0x7F."""
     x = np.asarray(x, dtype=np.float64)
     out = np.zeros(x.shape, dtype=np.uint8)
     mag = np.minimum(np.abs(x), E4M3_MAX)
@@ -60,7 +61,8 @@ def e4m3_encode(x) -> np.ndarray:
     d_hi = _POS_VALS[hi] - mag
     pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (_POS_CODES[lo] & 1 == 1) & (hi != lo))
     code = np.where(pick_hi, _POS_CODES[hi], _POS_CODES[lo]).astype(np.uint8)
-    code = np.where(np.signbit(x) & (code != 0), code | 0x80, code).astype(np.uint8)
+    # rounding keeps the sign, also for a value that rounds to zero (-0 = 0x80)
+    code = np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
     code = np.where(np.isnan(x), np.uint8(0x7F), code)
     out[...] = code
     return out

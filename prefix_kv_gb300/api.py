@@ -163,3 +163,37 @@ def prefix_cache_append(k, v, cu_seqlens_k, cu_prefix, cache_k, cache_v, layer: 
         _ptr(k), _ptr(v), _ptr(cu_seqlens_k), _ptr(cu_prefix), batch, H, D, total_k,
         _ptr(cache_k), _ptr(cache_v), layer, L, cap, _ptr(status), _stream(stream))
     _native.check(code, "bca_prefix_cache_append")
+
+
+FP8_MODES = {"v": 1, "kv": 2}
+
+
+def prefix_cache_append_fp8(k, v, cu_seqlens_k, cu_prefix, cache_k, cache_v, scale_k, scale_v,
+                            layer: int, mode: str = "v", status=None, stream=None) -> None:
+    """Quantising append into an FP8 E4M3 cache.
+
+    mode "v": cache_k bf16 ``[L, H, cap, 128]``, cache_v uint8 codes, scale_v fp32
+    ``[L, H, cap]`` (scale_k may be None).  mode "kv": cache_k and cache_v uint8
+    codes, scale_k and scale_v fp32.
+    """
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _need(cu_prefix, "cu_prefix", torch.int32, 1)
+    m = FP8_MODES[mode]
+    _need(cache_k, "cache_k", torch.uint8 if mode == "kv" else torch.bfloat16, 4)
+    _need(cache_v, "cache_v", torch.uint8, 4)
+    _need(scale_v, "scale_v", torch.float32, 3)
+    if mode == "kv":
+        _need(scale_k, "scale_k", torch.float32, 3)
+    total_k, H, D = k.shape
+    L, Hc, cap, Dc = cache_v.shape
+    if (Hc, Dc) != (H, D) or tuple(cache_k.shape) != tuple(cache_v.shape) or \
+            tuple(scale_v.shape) != (L, H, cap):
+        raise ValueError("cache shapes do not match")
+    batch = cu_seqlens_k.numel() - 1
+    code = _native.load().bca_prefix_cache_append_fp8(
+        _ptr(k), _ptr(v), _ptr(cu_seqlens_k), _ptr(cu_prefix), batch, H, D, total_k, m,
+        _ptr(cache_k), _ptr(cache_v), _ptr(scale_k), _ptr(scale_v), layer, L, cap, _ptr(status),
+        _stream(stream))
+    _native.check(code, "bca_prefix_cache_append_fp8")

@@ -203,4 +203,34 @@ bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* 
   return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
 }
 
+bca_status bca_prefix_cache_append_fp8(const void* k, const void* v, const int32_t* cu_seqlens_k,
+                                       const int32_t* cu_prefix, int32_t batch, int32_t num_heads,
+                                       int32_t head_dim, int32_t total_k, int32_t mode,
+                                       void* cache_k, void* cache_v, float* scale_k,
+                                       float* scale_v, int32_t layer, int32_t num_layers,
+                                       int64_t capacity, int32_t* status_dev, void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (mode != BCA_FP8_V && mode != BCA_FP8_KV) return BCA_ERR_INVALID_ARG;
+  if (batch < 0 || num_heads <= 0 || total_k < 0 || capacity < 0 || layer < 0 ||
+      num_layers <= 0 || layer >= num_layers)
+    return BCA_ERR_INVALID_ARG;
+  if (batch == 0) return BCA_OK;
+  if (!k || !v || !cu_seqlens_k || !cu_prefix) return BCA_ERR_INVALID_ARG;
+  const bool quant_k = mode == BCA_FP8_KV;
+  if (capacity > 0 && (!cache_k || !cache_v || !scale_v || (quant_k && !scale_k)))
+    return BCA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(cache_k) || !aligned16(cache_v) ||
+      (reinterpret_cast<uintptr_t>(scale_v) & 3u) || (reinterpret_cast<uintptr_t>(scale_k) & 3u))
+    return BCA_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(num_heads) * capacity;   // per layer
+  const size_t k_bytes = quant_k ? 1 : 2;
+  cudaError_t e = launch_cache_append_fp8(
+      k, v, cu_seqlens_k, cu_prefix, batch, num_heads, quant_k,
+      static_cast<uint8_t*>(cache_k) + layer * rows * kHeadDim * k_bytes,
+      static_cast<uint8_t*>(cache_v) + layer * rows * kHeadDim,
+      quant_k ? scale_k + layer * rows : nullptr, scale_v + layer * rows, capacity, status_dev,
+      static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -112,3 +112,130 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_
 }
 
 }  // namespace bca
+
+// ---------------------------------------------------------------------------
+// FP8 E4M3 variant ("Qwen-Image 2.1 deployment notes", prefix-cache section:
+// FP8 E4M3 with one FP32 scale per token and head, quantising K and V or V
+// only).  Each (token, head) row of 128 values is scaled by its absmax onto
+// the E4M3 range: scale = amax / 448, code = E4M3(x * (448 / amax)), rounded
+// to nearest even and saturating, all arithmetic in fp32.  16 threads share a
+// row (8 values each) and reduce amax with warp shuffles.
+namespace bca {
+namespace {
+
+__device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Quantises the 8 bf16 values of one thread; returns the 8 codes as a uint2.
+__device__ __forceinline__ uint2 quantize8(uint4 raw, float* scale_out) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  *scale_out = amax / 448.0f;
+  const float inv = amax > 0.f ? 448.0f / amax : 0.f;
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    c[i] = e4m3x2(x[2 * i] * inv, x[2 * i + 1] * inv);
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+template <bool kQuantK>
+__global__ void __launch_bounds__(256)
+    cache_append_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                            const int32_t* __restrict__ cu_k, const int32_t* __restrict__ cu_prefix,
+                            int batch, int num_heads, void* __restrict__ ck, uint2* __restrict__ cv,
+                            float* __restrict__ sk, float* __restrict__ sv, int64_t capacity,
+                            int32_t* status) {
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < batch; i += blockDim.x) {
+    const int pl = cu_prefix[i + 1] - cu_prefix[i];
+    const int kl = cu_k[i + 1] - cu_k[i];
+    if (pl < 0 || pl > kl || cu_prefix[i] < 0) s_bad = BCA_ERR_SEQLENS;
+  }
+  if (threadIdx.x == 0 && static_cast<int64_t>(cu_prefix[batch]) > capacity)
+    s_bad = BCA_ERR_CAPACITY;
+  __syncthreads();
+  if (s_bad != 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report_status(status, s_bad);
+    return;
+  }
+  const int p0 = cu_prefix[0];
+  const int64_t rows = static_cast<int64_t>(cu_prefix[batch] - p0) * num_heads;
+  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  const int lane16 = threadIdx.x & 15;
+  // two rows per warp (16 lanes each); all 32 lanes stay together for the shuffles
+  for (int64_t r2 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       r2 * 2 < rows; r2 += warps) {
+    const int64_t row = r2 * 2 + ((threadIdx.x >> 4) & 1);
+    const bool live = row < rows;
+    const int64_t rr = live ? row : rows - 1;
+    const int c = static_cast<int>(rr / num_heads) + p0;       // cache token
+    const int hh = static_cast<int>(rr % num_heads);
+    int lo = 0, hi = batch - 1;                                  // sequence of c
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu_prefix[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    const int64_t src_tok = static_cast<int64_t>(cu_k[lo]) + (c - cu_prefix[lo]);
+    const int64_t src = (src_tok * num_heads + hh) * 16 + lane16;
+    const int64_t dst_row = static_cast<int64_t>(hh) * capacity + c;
+    float scale_v, scale_k;
+    const uint2 qv = quantize8(__ldcs(v + src), &scale_v);
+    if (live) {
+      cv[dst_row * 16 + lane16] = qv;
+      if (lane16 == 0) sv[dst_row] = scale_v;
+    }
+    const uint4 kraw = __ldcs(k + src);
+    if constexpr (kQuantK) {
+      const uint2 qk = quantize8(kraw, &scale_k);
+      if (live) {
+        static_cast<uint2*>(ck)[dst_row * 16 + lane16] = qk;
+        if (lane16 == 0) sk[dst_row] = scale_k;
+      }
+    } else {
+      if (live) static_cast<uint4*>(ck)[dst_row * 16 + lane16] = kraw;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t* cu_k,
+                                    const int32_t* cu_prefix, int batch, int num_heads,
+                                    bool quant_k, void* cache_k_layer, void* cache_v_layer,
+                                    float* scale_k_layer, float* scale_v_layer, int64_t capacity,
+                                    int32_t* status, cudaStream_t stream) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = sms * 8;
+  if (quant_k) {
+    cache_append_fp8_kernel<true><<<grid, 256, 0, stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
+        num_heads, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
+        scale_v_layer, capacity, status);
+  } else {
+    cache_append_fp8_kernel<false><<<grid, 256, 0, stream>>>(
+        static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
+        num_heads, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
+        scale_v_layer, capacity, status);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace bca

@@ -59,4 +59,10 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_
                                 void* cache_k_layer, void* cache_v_layer, int64_t capacity,
                                 int32_t* status, cudaStream_t stream);
 
+cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t* cu_k,
+                                    const int32_t* cu_prefix, int batch, int num_heads,
+                                    bool quant_k, void* cache_k_layer, void* cache_v_layer,
+                                    float* scale_k_layer, float* scale_v_layer, int64_t capacity,
+                                    int32_t* status, cudaStream_t stream);
+
 }  // namespace bca

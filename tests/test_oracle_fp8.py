@@ -20,6 +20,8 @@ from oracle import fp8
     (1.2, 0x3A),                     # nearest is 1.25
     (464.0, 0x7E), (1e9, 0x7E),      # saturate to 448
     (240.0, 0x77),                   # 1.875 * 2^7
+    (-0.25 * 2.0 ** -9, 0x80),       # rounds to zero, keeps the sign: -0
+    (-0.0, 0x80),
 ])
 def test_e4m3_hand_worked(x, code):
     assert int(fp8.e4m3_encode(np.array([x]))[0]) == code
@@ -36,7 +38,7 @@ def test_e4m3_value_table():
     # every code round-trips
     codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
     back = fp8.e4m3_encode(fp8.e4m3_value(codes))
-    assert np.array_equal(back[codes != 0x80], codes[codes != 0x80])   # -0 encodes as +0
+    assert np.array_equal(back, codes)                                  # -0 keeps its sign
 
 
 def test_e4m3_matches_torch_float8():
@@ -45,8 +47,7 @@ def test_e4m3_matches_torch_float8():
     x = np.clip(x, -448, 448).astype(np.float32)
     ours = fp8.e4m3_encode(x)
     theirs = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
-    # torch writes -0 for tiny negatives; compare values
-    assert np.array_equal(fp8.e4m3_value(ours), fp8.e4m3_value(theirs))
+    assert np.array_equal(ours, theirs)                                 # codes, signed zeros included
 
 
 def test_quantize_rows_properties():
