@@ -207,6 +207,24 @@ bca_status bca_prefix_cache_append_fp8(const void* k, const void* v, const int32
                                        float* scale_v, int32_t layer, int32_t num_layers,
                                        int64_t capacity, int32_t* status_dev, void* stream);
 
+/* Prefix-cache decode over an FP8 E4M3 cache written by
+ * bca_prefix_cache_append_fp8 in the same mode ("Qwen-Image 2.1 deployment
+ * notes", prefix-cache section).  Every cached key/value element enters the
+ * attention as its dequantised value bf16(fp32(value(code)) * scale) of the
+ * append call; target K/V stay bf16.  mode, cache_k, cache_v, scale_k and
+ * scale_v are laid out as in bca_prefix_cache_append_fp8 (scale_k is not read
+ * in BCA_FP8_V mode; scales need 4-byte alignment, caches 16-byte).  All other
+ * arguments, layouts and errors are those of bca_prefix_decode; an unknown
+ * mode is BCA_ERR_INVALID_ARG. */
+bca_status bca_prefix_decode_fp8(const void* q_tgt, const void* cache_k, const void* cache_v,
+                                 int32_t mode, const float* scale_k, const float* scale_v,
+                                 int32_t layer, int32_t num_layers, int64_t capacity,
+                                 const int32_t* cu_prefix, const void* k_tgt, const void* v_tgt,
+                                 const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
+                                 int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
+                                 int32_t max_prefix, float softmax_scale, void* out, float* lse,
+                                 int32_t* status_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -4,7 +4,8 @@ The compute lives in ``lib/libbca_gb300.so`` (C ABI declared in ``include/bca.h`
 this package is its thin Python binding plus the seeded workload generator.
 """
 from .api import (check_status, new_status, prefill, prefill_workspace_bytes,  # noqa: F401
-                  prefix_cache_append, prefix_cache_append_fp8, prefix_decode, read_status, schedule_prep)
+                  prefix_cache_append, prefix_cache_append_fp8, prefix_decode, prefix_decode_fp8,
+                  read_status, schedule_prep)
 
-__all__ = ["prefill", "prefix_decode", "prefix_cache_append", "prefix_cache_append_fp8", "schedule_prep",
+__all__ = ["prefill", "prefix_decode", "prefix_decode_fp8", "prefix_cache_append", "prefix_cache_append_fp8", "schedule_prep",
            "prefill_workspace_bytes", "new_status", "read_status", "check_status"]

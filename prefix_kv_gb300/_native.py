@@ -32,6 +32,9 @@ SIGNATURES = {
     "bca_prefix_decode": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
                                   c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_f32, c_vp,
                                   c_vp, c_vp, c_vp]),
+    "bca_prefix_decode_fp8": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, c_i64,
+                                      c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                      c_i32, c_f32, c_vp, c_vp, c_vp, c_vp]),
     "bca_prefix_cache_append_fp8": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
                                             c_i32, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i64,
                                             c_vp, c_vp]),

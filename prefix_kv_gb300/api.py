@@ -191,9 +191,53 @@ def prefix_cache_append_fp8(k, v, cu_seqlens_k, cu_prefix, cache_k, cache_v, sca
     if (Hc, Dc) != (H, D) or tuple(cache_k.shape) != tuple(cache_v.shape) or \
             tuple(scale_v.shape) != (L, H, cap):
         raise ValueError("cache shapes do not match")
+    if mode == "kv" and tuple(scale_k.shape) != (L, H, cap):
+        raise ValueError("scale_k shape does not match the cache")
     batch = cu_seqlens_k.numel() - 1
     code = _native.load().bca_prefix_cache_append_fp8(
         _ptr(k), _ptr(v), _ptr(cu_seqlens_k), _ptr(cu_prefix), batch, H, D, total_k, m,
         _ptr(cache_k), _ptr(cache_v), _ptr(scale_k), _ptr(scale_v), layer, L, cap, _ptr(status),
         _stream(stream))
     _native.check(code, "bca_prefix_cache_append_fp8")
+
+
+def prefix_decode_fp8(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: int, cu_prefix, k_tgt,
+                      v_tgt, cu_seqlens_q, max_seqlen_q: int, max_prefix: int,
+                      softmax_scale: Optional[float] = None, mode: str = "v", out=None, lse=None,
+                      status=None, stream=None):
+    """``prefix_decode`` over an FP8 E4M3 cache written by ``prefix_cache_append_fp8``
+    in the same ``mode`` (cache and scale layouts as there)."""
+    for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
+        _need(t, name, torch.bfloat16, 3)
+    m = FP8_MODES[mode]
+    _need(cache_k, "cache_k", torch.uint8 if mode == "kv" else torch.bfloat16, 4)
+    _need(cache_v, "cache_v", torch.uint8, 4)
+    _need(scale_v, "scale_v", torch.float32, 3)
+    if mode == "kv":
+        _need(scale_k, "scale_k", torch.float32, 3)
+    _need(cu_prefix, "cu_prefix", torch.int32, 1)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    total_q, H, D = q_tgt.shape
+    L, Hc, cap, Dc = cache_v.shape
+    if (Hc, Dc) != (H, D) or tuple(cache_k.shape) != tuple(cache_v.shape) or \
+            tuple(scale_v.shape) != (L, H, cap) or \
+            (mode == "kv" and tuple(scale_k.shape) != (L, H, cap)):
+        raise ValueError("cache shapes do not match q_tgt")
+    if k_tgt.shape != q_tgt.shape or v_tgt.shape != q_tgt.shape:
+        raise ValueError("k_tgt / v_tgt shapes do not match q_tgt")
+    batch = cu_seqlens_q.numel() - 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q_tgt)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    code = _native.load().bca_prefix_decode_fp8(
+        _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), m, _ptr(scale_k) if mode == "kv" else None,
+        _ptr(scale_v), layer, L, cap, _ptr(cu_prefix), _ptr(k_tgt), _ptr(v_tgt),
+        _ptr(cu_seqlens_q), batch, H, D, total_q, max_seqlen_q, max_prefix,
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefix_decode_fp8")
+    return out, lse

@@ -51,6 +51,10 @@ struct AttnLaunch {
   const PrefillTile* tiles;
   const int32_t* cu_prefix;
   int32_t* status;
+  // decode over an FP8 cache: 0 = bf16 cache, BCA_FP8_V or BCA_FP8_KV
+  int fp8_mode;
+  const float* scale_k;     // [H][capacity] of the layer (BCA_FP8_KV)
+  const float* scale_v;     // [H][capacity] of the layer
 };
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream);  // returns bca_status
 

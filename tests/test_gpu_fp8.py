@@ -5,10 +5,11 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import prefix_kv_gb300 as bca
 from oracle import fp8
 from prefix_kv_gb300 import workloads as W
-from gpu_cases import DEV
+from gpu_cases import DEV, SCALE, assert_close
 
 pytestmark = pytest.mark.gpu
 
@@ -65,3 +66,111 @@ def test_append_fp8_rejects_overflow():
                                 torch.tensor([0, 9], dtype=torch.int32, device=DEV),
                                 ck, cv, sk, sv, 0, mode="kv", status=st)
     assert bca.read_status(st) == 5 and (cv == 0).all()
+
+
+# ---------------------------------------------------------------- decode over the FP8 cache
+
+def _dequantized(x):
+    """The oracle's dequantised copy of packed bf16 rows [n, H, 128]."""
+    codes, scales = fp8.quantize_rows(x)
+    return torch.from_numpy(fp8.dequantize_rows(codes, scales)).to(torch.bfloat16)
+
+
+class Fp8DecodeCase:
+    """Prefix decode inputs with the prefix held in an FP8 cache that the oracle's
+    quantising append wrote.  Capacity past the last prefix holds NaN codes and
+    NaN scales: only the prefix rows may be read."""
+
+    def __init__(self, qt, kt, vt, kp, vp, cu_q, cu_p, mode, layers=2, layer=1):
+        self.qt, self.kt, self.vt, self.kp, self.vp = qt, kt, vt, kp, vp
+        self.cu_q = np.asarray(cu_q, np.int32)
+        self.cu_p = np.asarray(cu_p, np.int32)
+        self.mode, self.layer = mode, layer
+        H = qt.shape[1]
+        cap = int(self.cu_p[-1]) + 64
+        kshape = (layers, H, cap, 128)
+        caches = {"k": np.full(kshape, 0x7F if mode == "kv" else 0x7FC0,
+                               np.uint8 if mode == "kv" else np.uint16),
+                  "v": np.full(kshape, 0x7F, np.uint8),
+                  "sk": np.full(kshape[:3], np.nan, np.float32),
+                  "sv": np.full(kshape[:3], np.nan, np.float32)}
+        fp8.cache_append_fp8(kp, vp, self.cu_p, self.cu_p, mode, layer, caches)
+        self.caches = caches
+        self.max_q = int(np.diff(self.cu_q).max())
+        self.max_pre = int(np.diff(self.cu_p).max())
+
+    @classmethod
+    def from_workload(cls, wl, mode):
+        q, k, v = W.make_qkv(wl)
+        tr, pr = wl.target_rows(), wl.prefix_rows()
+        return cls(q[tr].contiguous(), k[tr].contiguous(), v[tr].contiguous(), k[pr].contiguous(),
+                   v[pr].contiguous(), wl.cu_target(), wl.cu_prefix(), mode)
+
+    def run(self, status=None):
+        c = self.caches
+        ck = torch.from_numpy(c["k"]) if self.mode == "kv" else \
+            torch.from_numpy(c["k"].view(np.int16)).view(torch.bfloat16)
+        d = lambda t: t.to(DEV)
+        ti = lambda a: torch.from_numpy(a).to(DEV)
+        return bca.prefix_decode_fp8(
+            d(self.qt), d(ck), ti(c["v"]), ti(c["sk"]) if self.mode == "kv" else None, ti(c["sv"]),
+            self.layer, ti(self.cu_p), d(self.kt), d(self.vt), ti(self.cu_q), self.max_q,
+            self.max_pre, SCALE, mode=self.mode, status=status)
+
+    def reference(self, quantised=True, rows=None, heads=None):
+        kp, vp = self.kp, self.vp
+        if quantised:
+            vp = _dequantized(vp)
+            if self.mode == "kv":
+                kp = _dequantized(kp)
+        return oracle.prefix_decode(self.qt, kp, vp, self.cu_p, self.kt, self.vt, self.cu_q, SCALE,
+                                    rows=rows, heads=heads)
+
+
+def _ragged(seed, pre, tgt, mode, H=3):
+    kp = (W.randn_bf16((sum(pre), H, 128), seed).float() * 2).to(torch.bfloat16)
+    vp = W.randn_bf16((sum(pre), H, 128), seed + 100)
+    if sum(pre) > 3:
+        vp[3, 0] = 0                                   # an all-zero row (scale 0)
+    qt = W.randn_bf16((sum(tgt), H, 128), seed + 200)
+    kt = W.randn_bf16((sum(tgt), H, 128), seed + 300)
+    vt = W.randn_bf16((sum(tgt), H, 128), seed + 400)
+    cu_p = np.concatenate([[0], np.cumsum(pre)])
+    cu_q = np.concatenate([[0], np.cumsum(tgt)])
+    return Fp8DecodeCase(qt, kt, vt, kp, vp, cu_q, cu_p, mode)
+
+
+@pytest.mark.parametrize("mode", ["v", "kv"])
+@pytest.mark.parametrize("seed,pre,tgt", [
+    (71, [24, 0, 300, 129], [16, 200, 1, 256]),
+    (72, [1000], [130]),
+    (73, [128, 256], [128, 384]),
+])
+def test_decode_fp8_ragged(mode, seed, pre, tgt):
+    case = _ragged(seed, pre, tgt, mode)
+    st = bca.new_status(DEV)
+    out, lse = case.run(status=st)
+    assert bca.read_status(st) == 0
+    assert_close(out, lse, *case.reference(), what=f"fp8 {mode} decode{seed}")
+
+
+@pytest.mark.parametrize("mode", ["v", "kv"])
+def test_decode_fp8_full_size_edit(mode):
+    wl = W.edit_two_ref()
+    case = Fp8DecodeCase.from_workload(wl, mode)
+    out, lse = case.run()
+    heads = np.array([3, 20])
+    assert_close(out, lse, *case.reference(heads=heads), heads=heads, what=f"{wl.name} fp8 {mode}")
+
+
+def test_decode_fp8_v_only_closer_than_kv():
+    """Quantising V alone perturbs the output less than quantising K and V
+    (both measured against the unquantised cache)."""
+    heads = np.array([1])
+    errs = {}
+    for mode in ("v", "kv"):
+        case = _ragged(74, [700, 333], [256, 100], mode)
+        out, _ = case.run()
+        ref, _ = case.reference(quantised=False, heads=heads)
+        errs[mode] = float(np.abs(out.float().cpu().numpy()[:, heads] - ref).mean())
+    assert 0 < errs["v"] < errs["kv"]
