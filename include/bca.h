@@ -207,15 +207,41 @@ bca_status bca_prefix_cache_append_fp8(const void* k, const void* v, const int32
                                        float* scale_v, int32_t layer, int32_t num_layers,
                                        int64_t capacity, int32_t* status_dev, void* stream);
 
+/* Expansion of one layer of an E4M3 cache back to bf16: for the rows
+ * cu_prefix[0] .. cu_prefix[batch]-1 of every head, out[h][t][d] =
+ * bf16(fp32(value(codes[layer][h][t][d])) * scales[layer][h][t]), the
+ * dequantised value defined above, rounded to nearest even.
+ * codes: device uint8 [num_layers][H][capacity][128]; scales: device fp32
+ * [num_layers][H][capacity]; out: device bf16 [H][capacity][128] for the one
+ * layer (rows outside the range are not written).  cu_prefix: device int32
+ * [batch+1].  When cu_prefix[batch] > capacity (BCA_ERR_CAPACITY) or the range
+ * is negative (BCA_ERR_SEQLENS) nothing is written.  Pointers 16-byte aligned
+ * (scales 4-byte). */
+bca_status bca_prefix_cache_dequant_fp8(const void* codes, const float* scales,
+                                        const int32_t* cu_prefix, int32_t batch,
+                                        int32_t num_heads, int32_t head_dim, int32_t layer,
+                                        int32_t num_layers, int64_t capacity, void* out,
+                                        int32_t* status_dev, void* stream);
+
+/* Workspace bytes bca_prefix_decode_fp8 needs: one bf16 layer [H][capacity][128]
+ * (256-byte rounded) per quantised tensor, i.e. one for BCA_FP8_V and two for
+ * BCA_FP8_KV; 0 for invalid arguments. */
+size_t bca_prefix_decode_fp8_workspace_bytes(int32_t mode, int32_t num_heads, int32_t head_dim,
+                                             int64_t capacity);
+
 /* Prefix-cache decode over an FP8 E4M3 cache written by
  * bca_prefix_cache_append_fp8 in the same mode ("Qwen-Image 2.1 deployment
  * notes", prefix-cache section).  Every cached key/value element enters the
- * attention as its dequantised value bf16(fp32(value(code)) * scale) of the
- * append call; target K/V stay bf16.  mode, cache_k, cache_v, scale_k and
- * scale_v are laid out as in bca_prefix_cache_append_fp8 (scale_k is not read
- * in BCA_FP8_V mode; scales need 4-byte alignment, caches 16-byte).  All other
- * arguments, layouts and errors are those of bca_prefix_decode; an unknown
- * mode is BCA_ERR_INVALID_ARG. */
+ * attention as its dequantised value bf16(fp32(value(code)) * scale); target
+ * K/V stay bf16.  The quantised tensors of the layer are first expanded
+ * (bca_prefix_cache_dequant_fp8) into `workspace`, device memory of at least
+ * bca_prefix_decode_fp8_workspace_bytes (16-byte aligned, else
+ * BCA_ERR_WORKSPACE), then attended exactly as by bca_prefix_decode; the
+ * workspace is scratch, free again once the stream passes the call.  mode,
+ * cache_k, cache_v, scale_k and scale_v are laid out as in
+ * bca_prefix_cache_append_fp8 (scale_k is not read in BCA_FP8_V mode).  All
+ * other arguments, layouts and errors are those of bca_prefix_decode; an
+ * unknown mode is BCA_ERR_INVALID_ARG. */
 bca_status bca_prefix_decode_fp8(const void* q_tgt, const void* cache_k, const void* cache_v,
                                  int32_t mode, const float* scale_k, const float* scale_v,
                                  int32_t layer, int32_t num_layers, int64_t capacity,
@@ -223,7 +249,8 @@ bca_status bca_prefix_decode_fp8(const void* q_tgt, const void* cache_k, const v
                                  const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
                                  int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
                                  int32_t max_prefix, float softmax_scale, void* out, float* lse,
-                                 int32_t* status_dev, void* stream);
+                                 void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                                 void* stream);
 
 #ifdef __cplusplus
 }

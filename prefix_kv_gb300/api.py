@@ -201,12 +201,42 @@ def prefix_cache_append_fp8(k, v, cu_seqlens_k, cu_prefix, cache_k, cache_v, sca
     _native.check(code, "bca_prefix_cache_append_fp8")
 
 
+def prefix_decode_fp8_workspace_bytes(mode: str, num_heads: int, capacity: int,
+                                      head_dim: int = 128) -> int:
+    return int(_native.load().bca_prefix_decode_fp8_workspace_bytes(FP8_MODES[mode], num_heads,
+                                                                    head_dim, capacity))
+
+
+def prefix_cache_dequant_fp8(codes, scales, cu_prefix, layer: int, out=None, status=None,
+                             stream=None):
+    """bf16 ``[H, cap, 128]`` expansion of rows ``cu_prefix[0]..cu_prefix[-1]`` of one
+    layer of an E4M3 cache (codes uint8 ``[L, H, cap, 128]``, scales fp32 ``[L, H, cap]``)."""
+    _need(codes, "codes", torch.uint8, 4)
+    _need(scales, "scales", torch.float32, 3)
+    _need(cu_prefix, "cu_prefix", torch.int32, 1)
+    L, H, cap, D = codes.shape
+    if tuple(scales.shape) != (L, H, cap):
+        raise ValueError("scales shape does not match the codes")
+    if out is None:
+        out = torch.empty((H, cap, D), dtype=torch.bfloat16, device=codes.device)
+    _need(out, "out", torch.bfloat16, 3)
+    if tuple(out.shape) != (H, cap, D):
+        raise ValueError("out must be [H, cap, 128]")
+    code = _native.load().bca_prefix_cache_dequant_fp8(
+        _ptr(codes), _ptr(scales), _ptr(cu_prefix), cu_prefix.numel() - 1, H, D, layer, L, cap,
+        _ptr(out), _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefix_cache_dequant_fp8")
+    return out
+
+
 def prefix_decode_fp8(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: int, cu_prefix, k_tgt,
                       v_tgt, cu_seqlens_q, max_seqlen_q: int, max_prefix: int,
                       softmax_scale: Optional[float] = None, mode: str = "v", out=None, lse=None,
-                      status=None, stream=None):
+                      workspace=None, status=None, stream=None):
     """``prefix_decode`` over an FP8 E4M3 cache written by ``prefix_cache_append_fp8``
-    in the same ``mode`` (cache and scale layouts as there)."""
+    in the same ``mode`` (cache and scale layouts as there).  ``workspace``: a
+    device uint8 tensor of ``prefix_decode_fp8_workspace_bytes`` bytes (allocated
+    here when omitted)."""
     for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
         _need(t, name, torch.bfloat16, 3)
     m = FP8_MODES[mode]
@@ -234,10 +264,14 @@ def prefix_decode_fp8(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: int, cu_
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
     _need(out, "out", torch.bfloat16, 3)
     _need(lse, "lse", torch.float32, 2)
+    if workspace is None:
+        workspace = torch.empty(prefix_decode_fp8_workspace_bytes(mode, H, cap, D),
+                                dtype=torch.uint8, device=q_tgt.device)
     code = _native.load().bca_prefix_decode_fp8(
         _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), m, _ptr(scale_k) if mode == "kv" else None,
         _ptr(scale_v), layer, L, cap, _ptr(cu_prefix), _ptr(k_tgt), _ptr(v_tgt),
         _ptr(cu_seqlens_q), batch, H, D, total_q, max_seqlen_q, max_prefix,
-        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream))
     _native.check(code, "bca_prefix_decode_fp8")
     return out, lse

@@ -54,7 +54,6 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kThreads * kRegsLau
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;
 constexpr int kWarpFix = 10;
-constexpr int kWarpConv2 = 11;   // second E4M3 converter (decode over an FP8 cache)
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -65,8 +64,6 @@ struct FwdSmem {
   uint8_t kv[kStages][kTileBytes];
   uint64_t q_full;
   uint64_t kv_full[kStages];
-  uint64_t raw_full[kStages];   // an E4M3 cache tile landed (decode over an FP8 cache)
-  uint64_t conv_half[kStages];  // warp 11 expanded its half of that tile
   uint64_t kv_empty[kStages];
   uint64_t s_full[2];
   uint64_t p_full[2];
@@ -91,8 +88,6 @@ struct FwdParams {
   const int32_t* row_end;
   const PrefillTile* tiles;
   const int32_t* cu_prefix;
-  const float* scale_k;       // FP8 decode: per-(head, token) scales of this layer
-  const float* scale_v;
   int decode_pairs_per_seq;   // decode: tile pairs per sequence (grid decoding)
   int decode_split_from;      // decode: first item split into single-tile items
   __nv_bfloat16* out;
@@ -116,19 +111,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitLimitNs));
 }
 
-// Kernel modes: prefill, or prefix decode over a bf16 / FP8-V / FP8-K+V cache.
-constexpr int kModePrefill = 0, kModeDecode = 1, kModeDecodeFp8V = 2, kModeDecodeFp8KV = 3;
-
-template <int kMode>
+template <bool kDecode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_k2,
                     const __grid_constant__ CUtensorMap tm_v2, const FwdParams p) {
-  constexpr bool kDecode = kMode != kModePrefill;
-  constexpr bool kFp8V = kMode == kModeDecodeFp8V || kMode == kModeDecodeFp8KV;  // V cache in E4M3
-  constexpr bool kFp8K = kMode == kModeDecodeFp8KV;                              // K cache in E4M3
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -217,19 +206,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       return j < n_pre_tiles ? n_pre - j * kBlockN : q_len - (j - n_pre_tiles) * kBlockN;
     }
   };
-  // V tiles whose rows past the segment end are zeroed by the fix-up warp
-  // (E4M3 cache tiles are zeroed by the converter warps as they expand them)
-  auto needs_fixup = [&](int j) {
-    return seg_left_of(j) < kBlockN && !(kFp8V && j < n_pre_tiles);
-  };
 
   // ---- set-up -----------------------------------------------------------------
   if (warp == kWarpTma && lane == 0) {
     mbar_init(&sm.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.raw_full[s], 1);
-      mbar_init(&sm.conv_half[s], 1);
       mbar_init(&sm.kv_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -275,7 +257,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t armed = 0;   // bit s: stage s has been loaded at least once
       uint32_t parity = 0;  // bit s: parity of the last load into stage s
-      uint32_t armed_raw = 0, parity_raw = 0, raw_flip = 0;  // the same for raw_full
       const int n_q = rows_valid[1] > 0 ? 2 : 1;
       mbar_arrive_expect_tx(&sm.q_full, n_q * kTileBytes);
       for (int i = 0; i < n_q; ++i) {
@@ -292,25 +273,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           give_up();
           break;
         }
-        uint8_t* dst = sm.kv[s];
-        if constexpr (kFp8V) {
-          if (j < n_pre_tiles && (is_v || kFp8K)) {
-            // E4M3 cache tile: 128 rows x 128 B into the upper half of the stage;
-            // the converter warps expand it in place and complete kv_full[s]
-            mbar_arrive_expect_tx(&sm.raw_full[s], kTileBytes / 2);
-            armed &= ~(1u << s);   // the stage's previous load has been consumed
-            armed_raw |= 1u << s;
-            parity_raw = (parity_raw & ~(1u << s)) | (raw_flip & (1u << s));
-            raw_flip ^= 1u << s;
-            tma_load_3d(is_v ? &tm_v : &tm_k, &sm.raw_full[s], dst + kHalfBytes, 0,
-                        pre0 + j * kBlockN, h);
-            continue;
-          }
-        }
         mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
-        armed_raw &= ~(1u << s);
         armed |= 1u << s;
         parity = (parity & ~(1u << s)) | (static_cast<uint32_t>(r & 1) << s);
+        uint8_t* dst = sm.kv[s];
         if constexpr (!kDecode) {
           const CUtensorMap* m = is_v ? &tm_v : &tm_k;
           const int tok = kv_seq0 + j * kBlockN;
@@ -330,11 +296,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // If anything went wrong, let every load in flight land before the CTA exits.
       if (*abort_flag) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kStages; ++s)
           if (armed >> s & 1) mbar_wait(&sm.kv_full[s], parity >> s & 1, nullptr, kWaitLimitNs / 4);
-          if (armed_raw >> s & 1)
-            mbar_wait(&sm.raw_full[s], parity_raw >> s & 1, nullptr, kWaitLimitNs / 4);
-        }
         mbar_wait(&sm.q_full, 0, nullptr, kWaitLimitNs / 4);
       }
     }
@@ -383,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < nk && ok; ++j) {
         const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
         ok = mbar_wait(&sm.kv_full[vs], phase_of(2 * j + 1), abort_flag, kWaitLimitNs);
-        if (ok && needs_fixup(j)) {            // the fix-up warp zeroes V rows past the segment
+        if (ok && seg_left_of(j) < kBlockN) {  // the fix-up warp zeroes V rows past the segment
           mbar_arrive(&sm.fix_req);
           ok = mbar_wait(&sm.v_fixed, tails & 1, abort_flag, kWaitLimitNs);
           ++tails;
@@ -412,97 +375,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&sm.drain, 0, nullptr, kWaitLimitNs);
     }
     __syncwarp();
-   } else if (kFp8V && (warp == kWarpFix || warp == kWarpConv2)) {
-    // ====================== E4M3 cache tile expansion ======================
-    // Warps 10 and 11 expand every E4M3 cache tile, in load order, into the
-    // bf16 layout the MMAs read: x_hat = bf16(fp32(value(code)) * scale) per
-    // element, rows past the prefix end set to zero.  The 16 KB of codes sit
-    // in the upper half of the 32 KB stage, so the bf16 rows of the lower half
-    // never overlap them and each bf16 row of the upper half overlaps only its
-    // own code row: every warp reads its four rows before writing them.
-    // Warp 10 also zero-fills the tails of bf16 (target) V tiles on request.
-    const int cw = warp - kWarpFix;                 // 0 or 1: rows 64*cw .. 64*cw + 63
-    uint32_t raw_par = 0;                           // bit s: parity of the next raw_full wait
-    uint32_t conv_par = 0;                          // the same for conv_half (warp 10)
-    int tails = 0;
-    bool ok = true;
-    for (int i = 0; i < 2 * nk && ok; ++i) {
-      const int j = i >> 1;
-      const bool is_v = i & 1;
-      const int s = stage_of(i);
-      if (j < n_pre_tiles && (is_v || kFp8K)) {
-        const int seg_left = seg_left_of(j);
-        // this warp's 64 row scales, two per lane, fetched before the wait
-        const int row_lo = cw * (kBlockN / 2);
-        const float* sc_base = (is_v ? p.scale_v : p.scale_k) +
-                               static_cast<int64_t>(h) * p.capacity + pre0 + j * kBlockN + row_lo;
-        const float sc_a = row_lo + lane < seg_left ? sc_base[lane] : 0.f;
-        const float sc_b = row_lo + 32 + lane < seg_left ? sc_base[32 + lane] : 0.f;
-        ok = warp_wait(&sm.raw_full[s], raw_par >> s & 1, abort_flag);
-        raw_par ^= 1u << s;
-        if (!ok) break;
-        uint8_t* stg = sm.kv[s];
-        const int c8 = lane & 7;
-        const int half = c8 >> 2;
-        const int chunk0 = 2 * (c8 & 3);
-#pragma unroll 4
-        for (int it = 0; it < kBlockN / 2 / 4; ++it) {
-          const int lr = it * 4 + (lane >> 3);          // row within this warp's 64
-          const int r = row_lo + lr;
-          const uint4 raw = *reinterpret_cast<const uint4*>(stg + kHalfBytes + r * 128 + c8 * 16);
-          const float sc = __shfl_sync(0xffffffffu, lr < 32 ? sc_a : sc_b, lr & 31);
-          __syncwarp();    // the four rows are read before any of them is rewritten
-          uint32_t o[8];
-          if (r < seg_left) {
-            const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int q2 = 0; q2 < 4; ++q2) {
-#pragma unroll
-              for (int hb = 0; hb < 2; ++hb) {
-                const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(w[q2] >> (16 * hb)));
-                o[2 * q2 + hb] = pack_bf16x2(f.x * sc, f.y * sc);
-              }
-            }
-          } else {
-            // keys past the prefix end (other sequences' tokens, unused capacity)
-#pragma unroll
-            for (int q = 0; q < 8; ++q) o[q] = 0u;
-          }
-          uint8_t* rowp = stg + half * kHalfBytes + r * 128;
-          *reinterpret_cast<uint4*>(rowp + ((chunk0 ^ (r & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(rowp + (((chunk0 + 1) ^ (r & 7)) * 16)) =
-              make_uint4(o[4], o[5], o[6], o[7]);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (cw == 1) {
-          if (lane == 0) mbar_arrive(&sm.conv_half[s]);
-        } else {
-          // warp 11 cannot complete two phases of conv_half[s] before this
-          // wait: its next tile in stage s needs this tile's kv_full first
-          ok = warp_wait(&sm.conv_half[s], conv_par >> s & 1, abort_flag);
-          conv_par ^= 1u << s;
-          if (!ok) break;
-          if (lane == 0) mbar_arrive(&sm.kv_full[s]);
-        }
-      } else if (cw == 0 && is_v && needs_fixup(j)) {
-        ok = warp_wait(&sm.fix_req, tails & 1, abort_flag);
-        if (!ok) break;
-        ++tails;
-        const int seg_left = seg_left_of(j);
-        uint8_t* vb = sm.kv[s];
-        for (int idx = lane; idx < (kBlockN - seg_left) * 16; idx += 32) {
-          const int row = seg_left + (idx >> 4);
-          const int chunk = idx & 15;
-          *reinterpret_cast<uint4*>(vb + (chunk >> 3) * kHalfBytes + row * 128 + (chunk & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.v_fixed);
-      }
-    }
-    if (!ok && lane == 0) give_up();
    } else if (warp == kWarpFix) {
     // ====================== V tail fix-up ======================
     // Keys past the end of a tile's segment may hold anything (another
@@ -512,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int tails = 0;
     for (int j = 0; j < nk; ++j) {
       const int seg_left = seg_left_of(j);
-      if (!needs_fixup(j)) continue;
+      if (seg_left >= kBlockN) continue;
       const int vi = 2 * j + 1;
       if (!warp_wait(&sm.fix_req, tails & 1, abort_flag)) {
         if (lane == 0) give_up();
@@ -738,38 +610,6 @@ bool encode_cache(CUtensorMap* m, const void* base, int num_heads, int64_t capac
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// One layer of an E4M3 cache, [H][capacity][128] bytes: dims (d, token, head);
-// box (128, 128, 1), no swizzle (the converter warps read it row by row).
-bool encode_cache_fp8(CUtensorMap* m, const void* base, int num_heads, int64_t capacity) {
-  auto fn = get_encode_fn();
-  if (fn == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(capacity),
-                        static_cast<cuuint64_t>(num_heads)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim),
-                           static_cast<cuuint64_t>(capacity) * kHeadDim};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(kBlockN), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <int kMode>
-cudaError_t launch_mode(dim3 grid, cudaStream_t stream, const CUtensorMap& tq,
-                        const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tk2,
-                        const CUtensorMap& tv2, const FwdParams& p) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t err = cudaFuncSetAttribute(
-        attn_fwd_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        static_cast<int>(kSmemBytes));
-    if (err != cudaSuccess) return err;
-    attr_set = true;
-  }
-  attn_fwd_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
-  return cudaGetLastError();
-}
-
 }  // namespace
 
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
@@ -782,12 +622,8 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     tv2 = tv;
   } else {
     const int64_t map_cap = a.capacity > 0 ? a.capacity : 1;
-    const bool k8 = a.fp8_mode == BCA_FP8_KV, v8 = a.fp8_mode != 0;
-    ok = ok &&
-         (k8 ? encode_cache_fp8(&tk, a.k, a.num_heads, map_cap)
-             : encode_cache(&tk, a.k, a.num_heads, map_cap)) &&
-         (v8 ? encode_cache_fp8(&tv, a.v, a.num_heads, map_cap)
-             : encode_cache(&tv, a.v, a.num_heads, map_cap)) &&
+    ok = ok && encode_cache(&tk, a.k, a.num_heads, map_cap) &&
+         encode_cache(&tv, a.v, a.num_heads, map_cap) &&
          encode_packed(&tk2, a.k2, a.num_heads, a.total_q) &&
          encode_packed(&tv2, a.v2, a.num_heads, a.total_q);
   }
@@ -804,8 +640,6 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   p.row_end = a.row_end;
   p.tiles = a.tiles;
   p.cu_prefix = a.cu_prefix;
-  p.scale_k = a.scale_k;
-  p.scale_v = a.scale_v;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.status = a.status;
@@ -832,10 +666,28 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     grid = dim3(static_cast<unsigned>(ctas), 1, 1);
   }
   cudaError_t err;
-  if (!decode) err = launch_mode<kModePrefill>(grid, stream, tq, tk, tv, tk2, tv2, p);
-  else if (a.fp8_mode == BCA_FP8_KV) err = launch_mode<kModeDecodeFp8KV>(grid, stream, tq, tk, tv, tk2, tv2, p);
-  else if (a.fp8_mode == BCA_FP8_V) err = launch_mode<kModeDecodeFp8V>(grid, stream, tq, tk, tv, tk2, tv2, p);
-  else err = launch_mode<kModeDecode>(grid, stream, tq, tk, tv, tk2, tv2, p);
+  if (!decode) {
+    static bool attr_set = false;
+    if (!attr_set) {
+      err = cudaFuncSetAttribute(attn_fwd_kernel<false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+      if (err != cudaSuccess) return BCA_ERR_CUDA;
+      attr_set = true;
+    }
+    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+  } else {
+    static bool attr_set = false;
+    if (!attr_set) {
+      err = cudaFuncSetAttribute(attn_fwd_kernel<true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+      if (err != cudaSuccess) return BCA_ERR_CUDA;
+      attr_set = true;
+    }
+    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+  }
+  err = cudaGetLastError();
   return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
 }
 

@@ -38,44 +38,19 @@ PrefillWorkspace carve(void* base, int batch, int total_q, int max_seqlen_q) {
 
 namespace {
 
-// Shared by the bf16 and FP8 decode entry points; fp8_mode 0 = bf16 cache.
-bca_status decode_impl(const void* q_tgt, const void* cache_k, const void* cache_v, int fp8_mode,
-                       const float* scale_k, const float* scale_v, int32_t layer,
-                       int32_t num_layers, int64_t capacity, const int32_t* cu_prefix,
-                       const void* k_tgt, const void* v_tgt, const int32_t* cu_seqlens_q,
-                       int32_t batch, int32_t num_heads, int32_t head_dim, int32_t total_q,
-                       int32_t max_seqlen_q, int32_t max_prefix, float softmax_scale, void* out,
-                       float* lse, int32_t* status_dev, void* stream) {
-  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
-  if (batch < 0 || num_heads <= 0 || total_q < 0 || max_seqlen_q < 0 || max_prefix < 0 ||
-      capacity < 0 || layer < 0 || num_layers <= 0 || layer >= num_layers)
-    return BCA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BCA_ERR_INVALID_ARG;
-  if (batch == 0 || total_q == 0) return BCA_OK;
-  if (!q_tgt || !k_tgt || !v_tgt || !cu_seqlens_q || !out || !lse || !cu_prefix)
-    return BCA_ERR_INVALID_ARG;
-  const bool k8 = fp8_mode == BCA_FP8_KV, v8 = fp8_mode != 0;
-  if (capacity > 0 && (!cache_k || !cache_v || (v8 && !scale_v) || (k8 && !scale_k)))
-    return BCA_ERR_INVALID_ARG;
-  if (!aligned16(q_tgt) || !aligned16(k_tgt) || !aligned16(v_tgt) || !aligned16(out) ||
-      !aligned16(cache_k) || !aligned16(cache_v) ||
-      (reinterpret_cast<uintptr_t>(scale_v) & 3u) || (reinterpret_cast<uintptr_t>(scale_k) & 3u))
-    return BCA_ERR_INVALID_ARG;
-  if (num_heads > 65535 || batch > 65535 || tiles_for(max_seqlen_q) > 65535)
-    return BCA_ERR_UNSUPPORTED;
-  const size_t rows = static_cast<size_t>(num_heads) * capacity;   // (head, token) rows per layer
-  const size_t k_bytes = k8 ? 1 : 2, v_bytes = v8 ? 1 : 2;
+// Decode over one layer's bf16 K and V ([H][capacity][128] each).
+bca_status decode_layer(const void* q_tgt, const void* k_layer, const void* v_layer,
+                        int64_t capacity, const int32_t* cu_prefix, const void* k_tgt,
+                        const void* v_tgt, const int32_t* cu_seqlens_q, int32_t batch,
+                        int32_t num_heads, int32_t total_q, int32_t max_seqlen_q,
+                        float softmax_scale, void* out, float* lse, int32_t* status_dev,
+                        cudaStream_t stream) {
   AttnLaunch a{};
   a.q = q_tgt;
   // An empty cache (capacity 0) is never read, since every prefix must then be
   // empty; its tensor maps are pointed at q_tgt only to keep them valid.
-  a.k = capacity > 0 ? static_cast<const uint8_t*>(cache_k) + layer * rows * kHeadDim * k_bytes
-                     : q_tgt;
-  a.v = capacity > 0 ? static_cast<const uint8_t*>(cache_v) + layer * rows * kHeadDim * v_bytes
-                     : q_tgt;
-  a.fp8_mode = capacity > 0 ? fp8_mode : 0;
-  a.scale_k = k8 && capacity > 0 ? scale_k + layer * rows : nullptr;
-  a.scale_v = v8 && capacity > 0 ? scale_v + layer * rows : nullptr;
+  a.k = capacity > 0 ? k_layer : q_tgt;
+  a.v = capacity > 0 ? v_layer : q_tgt;
   a.k2 = k_tgt;
   a.v2 = v_tgt;
   a.out = out;
@@ -90,8 +65,37 @@ bca_status decode_impl(const void* q_tgt, const void* cache_k, const void* cache
   a.cu_q = cu_seqlens_q;
   a.cu_prefix = cu_prefix;
   a.status = status_dev;
-  (void)max_prefix;
-  return launch_attention(a, /*decode=*/true, static_cast<cudaStream_t>(stream));
+  return launch_attention(a, /*decode=*/true, stream);
+}
+
+// Argument checks shared by the decode entry points.
+bca_status check_decode_args(const void* q_tgt, const void* cache_k, const void* cache_v,
+                             int32_t layer, int32_t num_layers, int64_t capacity,
+                             const int32_t* cu_prefix, const void* k_tgt, const void* v_tgt,
+                             const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
+                             int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
+                             int32_t max_prefix, float softmax_scale, void* out, float* lse) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads <= 0 || total_q < 0 || max_seqlen_q < 0 || max_prefix < 0 ||
+      capacity < 0 || layer < 0 || num_layers <= 0 || layer >= num_layers)
+    return BCA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BCA_ERR_INVALID_ARG;
+  if (batch == 0 || total_q == 0) return BCA_OK;
+  if (!q_tgt || !k_tgt || !v_tgt || !cu_seqlens_q || !out || !lse || !cu_prefix)
+    return BCA_ERR_INVALID_ARG;
+  if (capacity > 0 && (!cache_k || !cache_v)) return BCA_ERR_INVALID_ARG;
+  if (!aligned16(q_tgt) || !aligned16(k_tgt) || !aligned16(v_tgt) || !aligned16(out) ||
+      !aligned16(cache_k) || !aligned16(cache_v))
+    return BCA_ERR_INVALID_ARG;
+  if (num_heads > 65535 || batch > 65535 || tiles_for(max_seqlen_q) > 65535)
+    return BCA_ERR_UNSUPPORTED;
+  return BCA_OK;
+}
+
+// Bytes of one layer of a bf16 cache, rounded up to 256.
+size_t bf16_layer_bytes(int32_t num_heads, int64_t capacity) {
+  const size_t b = static_cast<size_t>(num_heads) * static_cast<size_t>(capacity) * kHeadDim * 2;
+  return (b + 255) & ~static_cast<size_t>(255);
 }
 
 }  // namespace
@@ -201,9 +205,45 @@ bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void*
                              int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
                              int32_t max_prefix, float softmax_scale, void* out, float* lse,
                              int32_t* status_dev, void* stream) {
-  return decode_impl(q_tgt, cache_k, cache_v, 0, nullptr, nullptr, layer, num_layers, capacity,
-                     cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads, head_dim, total_q,
-                     max_seqlen_q, max_prefix, softmax_scale, out, lse, status_dev, stream);
+  bca_status st = check_decode_args(q_tgt, cache_k, cache_v, layer, num_layers, capacity,
+                                    cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads,
+                                    head_dim, total_q, max_seqlen_q, max_prefix, softmax_scale,
+                                    out, lse);
+  if (st != BCA_OK || batch == 0 || total_q == 0) return st;
+  const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
+  return decode_layer(q_tgt, static_cast<const __nv_bfloat16*>(cache_k) + layer * layer_elems,
+                      static_cast<const __nv_bfloat16*>(cache_v) + layer * layer_elems, capacity,
+                      cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads, total_q,
+                      max_seqlen_q, softmax_scale, out, lse, status_dev,
+                      static_cast<cudaStream_t>(stream));
+}
+
+size_t bca_prefix_decode_fp8_workspace_bytes(int32_t mode, int32_t num_heads, int32_t head_dim,
+                                             int64_t capacity) {
+  if ((mode != BCA_FP8_V && mode != BCA_FP8_KV) || head_dim != kHeadDim || num_heads <= 0 ||
+      capacity < 0)
+    return 0;
+  return (mode == BCA_FP8_KV ? 2 : 1) * bf16_layer_bytes(num_heads, capacity);
+}
+
+bca_status bca_prefix_cache_dequant_fp8(const void* codes, const float* scales,
+                                        const int32_t* cu_prefix, int32_t batch,
+                                        int32_t num_heads, int32_t head_dim, int32_t layer,
+                                        int32_t num_layers, int64_t capacity, void* out,
+                                        int32_t* status_dev, void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads <= 0 || capacity < 0 || layer < 0 || num_layers <= 0 ||
+      layer >= num_layers)
+    return BCA_ERR_INVALID_ARG;
+  if (batch == 0 || capacity == 0) return BCA_OK;
+  if (!codes || !scales || !cu_prefix || !out) return BCA_ERR_INVALID_ARG;
+  if (!aligned16(codes) || !aligned16(out) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+    return BCA_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(num_heads) * capacity;   // (head, token) rows per layer
+  const cudaError_t e = launch_cache_dequant_fp8(
+      static_cast<const uint8_t*>(codes) + layer * rows * kHeadDim, scales + layer * rows,
+      cu_prefix, batch, num_heads, capacity, out, status_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
 }
 
 bca_status bca_prefix_decode_fp8(const void* q_tgt, const void* cache_k, const void* cache_v,
@@ -213,12 +253,45 @@ bca_status bca_prefix_decode_fp8(const void* q_tgt, const void* cache_k, const v
                                  const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
                                  int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
                                  int32_t max_prefix, float softmax_scale, void* out, float* lse,
-                                 int32_t* status_dev, void* stream) {
+                                 void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                                 void* stream) {
   if (mode != BCA_FP8_V && mode != BCA_FP8_KV) return BCA_ERR_INVALID_ARG;
-  return decode_impl(q_tgt, cache_k, cache_v, mode, scale_k, scale_v, layer, num_layers,
-                     capacity, cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads, head_dim,
-                     total_q, max_seqlen_q, max_prefix, softmax_scale, out, lse, status_dev,
-                     stream);
+  bca_status st = check_decode_args(q_tgt, cache_k, cache_v, layer, num_layers, capacity,
+                                    cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads,
+                                    head_dim, total_q, max_seqlen_q, max_prefix, softmax_scale,
+                                    out, lse);
+  if (st != BCA_OK || batch == 0 || total_q == 0) return st;
+  const bool k8 = mode == BCA_FP8_KV;
+  if (capacity > 0 && (!scale_v || (k8 && !scale_k))) return BCA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(scale_v) & 3u) || (reinterpret_cast<uintptr_t>(scale_k) & 3u))
+    return BCA_ERR_INVALID_ARG;
+  const size_t need = bca_prefix_decode_fp8_workspace_bytes(mode, num_heads, head_dim, capacity);
+  if (capacity > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return BCA_ERR_WORKSPACE;
+  auto s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(num_heads) * capacity;
+  const void* k_layer = nullptr;
+  const void* v_layer = nullptr;
+  if (capacity > 0) {
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    void* v_exp = ws;
+    st = bca_prefix_cache_dequant_fp8(cache_v, scale_v, cu_prefix, batch, num_heads, head_dim,
+                                      layer, num_layers, capacity, v_exp, status_dev, stream);
+    if (st != BCA_OK) return st;
+    v_layer = v_exp;
+    if (k8) {
+      void* k_exp = ws + bf16_layer_bytes(num_heads, capacity);
+      st = bca_prefix_cache_dequant_fp8(cache_k, scale_k, cu_prefix, batch, num_heads, head_dim,
+                                        layer, num_layers, capacity, k_exp, status_dev, stream);
+      if (st != BCA_OK) return st;
+      k_layer = k_exp;
+    } else {
+      k_layer = static_cast<const __nv_bfloat16*>(cache_k) + layer * rows * kHeadDim;
+    }
+  }
+  return decode_layer(q_tgt, k_layer, v_layer, capacity, cu_prefix, k_tgt, v_tgt, cu_seqlens_q,
+                      batch, num_heads, total_q, max_seqlen_q, softmax_scale, out, lse,
+                      status_dev, s);
 }
 
 bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* cu_seqlens_k,

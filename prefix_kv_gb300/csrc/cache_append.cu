@@ -13,6 +13,7 @@
 // Validation (capacity, prefix <= sequence) is done by every thread before it
 // writes anything, so a failing call writes nothing.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace bca {
 namespace {
@@ -235,6 +236,68 @@ cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t*
         num_heads, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
         scale_v_layer, capacity, status);
   }
+  return cudaGetLastError();
+}
+
+}  // namespace bca
+
+// ---------------------------------------------------------------------------
+// Expansion of the E4M3 cache back to bf16 for attention: every element of
+// the stored prefix rows becomes bf16(fp32(value(code)) * scale), the
+// dequantised value of the append's format, written in the bf16 cache layout.
+// HBM-bound: a row is 128 code bytes plus one scale in, 256 bytes out; eight
+// threads share a row, 16 codes each (one 16-byte load, two 16-byte stores).
+namespace bca {
+namespace {
+
+__global__ void __launch_bounds__(256)
+    cache_dequant_fp8_kernel(const uint4* __restrict__ codes, const float* __restrict__ scales,
+                             const int32_t* __restrict__ cu_prefix, int batch, int num_heads,
+                             int64_t capacity, uint4* __restrict__ out, int32_t* status) {
+  const int p0 = cu_prefix[0], p1 = cu_prefix[batch];
+  if (p0 < 0 || p1 < p0 || static_cast<int64_t>(p1) > capacity) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      report_status(status, p1 > capacity ? BCA_ERR_CAPACITY : BCA_ERR_SEQLENS);
+    return;
+  }
+  const int64_t tokens = p1 - p0;
+  const int64_t chunks = tokens * num_heads * 8;        // 16-code chunks to expand
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+       c += stride) {
+    const int64_t row_in = c >> 3;                       // (head, token) row among the prefix rows
+    const int hh = static_cast<int>(row_in / tokens);
+    const int64_t row = static_cast<int64_t>(hh) * capacity + p0 + (row_in - hh * tokens);
+    const int x = static_cast<int>(c & 7);
+    const uint4 raw = __ldcs(codes + row * 8 + x);
+    const float sc = __ldg(scales + row);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(w[q] >> (16 * hb)));
+        o[2 * q + hb] = pack_bf16x2(f.x * sc, f.y * sc);
+      }
+    }
+    out[row * 16 + 2 * x] = make_uint4(o[0], o[1], o[2], o[3]);
+    out[row * 16 + 2 * x + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_dequant_fp8(const void* codes_layer, const float* scales_layer,
+                                     const int32_t* cu_prefix, int batch, int num_heads,
+                                     int64_t capacity, void* out_layer, int32_t* status,
+                                     cudaStream_t stream) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cache_dequant_fp8_kernel<<<sms * 8, 256, 0, stream>>>(
+      static_cast<const uint4*>(codes_layer), scales_layer, cu_prefix, batch, num_heads, capacity,
+      static_cast<uint4*>(out_layer), status);
   return cudaGetLastError();
 }
 

@@ -51,10 +51,6 @@ struct AttnLaunch {
   const PrefillTile* tiles;
   const int32_t* cu_prefix;
   int32_t* status;
-  // decode over an FP8 cache: 0 = bf16 cache, BCA_FP8_V or BCA_FP8_KV
-  int fp8_mode;
-  const float* scale_k;     // [H][capacity] of the layer (BCA_FP8_KV)
-  const float* scale_v;     // [H][capacity] of the layer
 };
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream);  // returns bca_status
 
@@ -68,5 +64,12 @@ cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t*
                                     bool quant_k, void* cache_k_layer, void* cache_v_layer,
                                     float* scale_k_layer, float* scale_v_layer, int64_t capacity,
                                     int32_t* status, cudaStream_t stream);
+
+// E4M3 cache rows cu_prefix[0] .. cu_prefix[batch]-1 of one layer ([H][cap][128]
+// codes, [H][cap] scales) expanded to bf16 value * scale, same layout.
+cudaError_t launch_cache_dequant_fp8(const void* codes_layer, const float* scales_layer,
+                                     const int32_t* cu_prefix, int batch, int num_heads,
+                                     int64_t capacity, void* out_layer, int32_t* status,
+                                     cudaStream_t stream);
 
 }  // namespace bca

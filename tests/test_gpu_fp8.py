@@ -68,6 +68,47 @@ def test_append_fp8_rejects_overflow():
     assert bca.read_status(st) == 5 and (cv == 0).all()
 
 
+# ---------------------------------------------------------------- expansion back to bf16
+
+def test_dequant_fp8_bit_exact_all_codes():
+    """Every code under scales from 0 through subnormal to 1e30: bf16(value * scale)
+    bit-exact against the oracle (NaN codes stay NaN); rows outside the prefix
+    range are not written."""
+    rng = np.random.default_rng(5)
+    L, H, cap, layer = 2, 3, 700, 1
+    codes = rng.integers(0, 256, size=(L, H, cap, 128), dtype=np.uint8)
+    codes[layer, 0, 10, :] = np.arange(128, dtype=np.uint8)
+    codes[layer, 0, 11, :] = np.arange(128, 256, dtype=np.uint8)
+    scales = (np.exp(rng.uniform(np.log(1e-30), np.log(1e30), size=(L, H, cap)))).astype(np.float32)
+    scales[layer, :, 10:12] = 1.0
+    scales[layer, 1, 20] = 0.0
+    scales[layer, 2, 21] = np.float32(1e-40)                     # subnormal scale
+    cu_p = np.array([7, 300, 300, 650], dtype=np.int32)          # starts past token 0
+    out = torch.full((H, cap, 128), 1.5, dtype=torch.bfloat16, device=DEV)
+    st = bca.new_status(DEV)
+    bca.prefix_cache_dequant_fp8(torch.from_numpy(codes).to(DEV), torch.from_numpy(scales).to(DEV),
+                                 torch.from_numpy(cu_p).to(DEV), layer, out=out, status=st)
+    assert bca.read_status(st) == 0
+    got = out.float().cpu().numpy()
+    exp = fp8.dequantize_rows(codes[layer], scales[layer])           # [H, cap, 128] float32
+    rows = slice(int(cu_p[0]), int(cu_p[-1]))
+    g, e = got[:, rows], exp[:, rows]
+    nan = np.isnan(e)
+    assert np.array_equal(np.isnan(g), nan)
+    assert np.array_equal(g[~nan].view(np.uint32), e[~nan].view(np.uint32))
+    assert (got[:, :cu_p[0]] == 1.5).all() and (got[:, cu_p[-1]:] == 1.5).all()
+
+
+def test_dequant_fp8_rejects_overflow():
+    codes = torch.zeros((1, 2, 8, 128), dtype=torch.uint8, device=DEV)
+    scales = torch.ones((1, 2, 8), dtype=torch.float32, device=DEV)
+    out = torch.full((2, 8, 128), 1.5, dtype=torch.bfloat16, device=DEV)
+    st = bca.new_status(DEV)
+    bca.prefix_cache_dequant_fp8(codes, scales, torch.tensor([0, 9], dtype=torch.int32, device=DEV),
+                                 0, out=out, status=st)
+    assert bca.read_status(st) == 5 and (out == 1.5).all()
+
+
 # ---------------------------------------------------------------- decode over the FP8 cache
 
 def _dequantized(x):
@@ -106,7 +147,7 @@ class Fp8DecodeCase:
         return cls(q[tr].contiguous(), k[tr].contiguous(), v[tr].contiguous(), k[pr].contiguous(),
                    v[pr].contiguous(), wl.cu_target(), wl.cu_prefix(), mode)
 
-    def run(self, status=None):
+    def run(self, status=None, workspace=None):
         c = self.caches
         ck = torch.from_numpy(c["k"]) if self.mode == "kv" else \
             torch.from_numpy(c["k"].view(np.int16)).view(torch.bfloat16)
@@ -115,7 +156,7 @@ class Fp8DecodeCase:
         return bca.prefix_decode_fp8(
             d(self.qt), d(ck), ti(c["v"]), ti(c["sk"]) if self.mode == "kv" else None, ti(c["sv"]),
             self.layer, ti(self.cu_p), d(self.kt), d(self.vt), ti(self.cu_q), self.max_q,
-            self.max_pre, SCALE, mode=self.mode, status=status)
+            self.max_pre, SCALE, mode=self.mode, workspace=workspace, status=status)
 
     def reference(self, quantised=True, rows=None, heads=None):
         kp, vp = self.kp, self.vp
@@ -161,6 +202,14 @@ def test_decode_fp8_full_size_edit(mode):
     out, lse = case.run()
     heads = np.array([3, 20])
     assert_close(out, lse, *case.reference(heads=heads), heads=heads, what=f"{wl.name} fp8 {mode}")
+
+
+def test_decode_fp8_workspace_checked():
+    case = _ragged(75, [200], [64], "kv")
+    ws = torch.empty(bca.prefix_decode_fp8_workspace_bytes("kv", 3, case.caches["v"].shape[2]) - 256,
+                     dtype=torch.uint8, device=DEV)
+    with pytest.raises(RuntimeError, match="status 4 "):
+        case.run(workspace=ws)
 
 
 def test_decode_fp8_v_only_closer_than_kv():
