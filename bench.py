@@ -11,6 +11,11 @@ metric: TFLOP/s counting only visible (q, k) pairs (4 * 128 * 32 flops each)
 of prefill + decode, divided by the time of the whole step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--cache bf16|fp8-v|fp8-kv]
+
+--cache fp8-v / fp8-kv runs the same step with the prefix cache in FP8 E4M3 (V, or
+K and V, quantised by the append and expanded by each decode) and adds the PSNR of
+the decode output against a bf16 cache.
 
 Under torchrun each rank runs its own independent request (weak scaling, no
 data-path collective); the per-step times are max-reduced over ranks.
@@ -141,7 +146,7 @@ class ClockSampler:
 class Problem:
     """The workload's tensors, resident on the device (plus pinned host copies for e2e)."""
 
-    def __init__(self, dev, with_host=True):
+    def __init__(self, dev, with_host=True, cache="bf16"):
         from prefix_kv_gb300 import flops
         from prefix_kv_gb300 import workloads as W
         wl = W.by_name(WORKLOAD)
@@ -169,9 +174,19 @@ class Problem:
         self.lse = torch.empty((self.H, self.S), dtype=torch.float32, device=dev)
         self.dout = torch.empty_like(d["q_tgt"])
         self.dlse = torch.empty((self.H, self.N), dtype=torch.float32, device=dev)
-        self.cache_k = torch.empty((1, self.H, self.P, 128), dtype=torch.bfloat16, device=dev)
-        self.cache_v = torch.empty_like(self.cache_k)
         import prefix_kv_gb300 as bca
+        self.cache = cache
+        self.fp8_mode = {"bf16": None, "fp8-v": "v", "fp8-kv": "kv"}[cache]
+        kdt = torch.uint8 if self.fp8_mode == "kv" else torch.bfloat16
+        vdt = torch.bfloat16 if self.fp8_mode is None else torch.uint8
+        self.cache_k = torch.empty((1, self.H, self.P, 128), dtype=kdt, device=dev)
+        self.cache_v = torch.empty((1, self.H, self.P, 128), dtype=vdt, device=dev)
+        if self.fp8_mode is not None:
+            self.scale_k = torch.empty((1, self.H, self.P), dtype=torch.float32, device=dev)
+            self.scale_v = torch.empty_like(self.scale_k)
+            self.dec_ws = torch.empty(
+                bca.prefix_decode_fp8_workspace_bytes(self.fp8_mode, self.H, self.P),
+                dtype=torch.uint8, device=dev)
         self.ws = torch.empty(bca.prefill_workspace_bytes(1, self.S, self.S), dtype=torch.uint8,
                               device=dev)
         self.status = bca.new_status(dev)
@@ -180,7 +195,15 @@ class Problem:
         self.pairs_decode = flops.decode_visible_pairs(wl.cu_target(), wl.cu_prefix())
         self.flops_prefill = flops.attention_flops(self.pairs_prefill, self.H)
         self.flops_decode = flops.attention_flops(self.pairs_decode, self.H)
-        self.append_bytes = 2 * 2 * self.P * self.H * 128 * 2   # K and V, read + write
+        rows = self.P * self.H
+        if self.fp8_mode is None:
+            self.append_bytes = 2 * 2 * rows * 128 * 2           # K and V, read + write
+        elif self.fp8_mode == "v":                               # K copied, V quantised
+            self.append_bytes = rows * (2 * 256 + 256 + 128 + 4)
+        else:                                                    # K and V quantised
+            self.append_bytes = rows * 2 * (256 + 128 + 4)
+        # kernel launches per step: schedule prep, prefill, append, [expansions], decode
+        self.launches = 4 + {None: 0, "v": 1, "kv": 2}[self.fp8_mode]
 
     def step(self, d, events=None):
         """The whole path through the binding; `events` = 4 CUDA events to split it."""
@@ -191,15 +214,46 @@ class Problem:
                     self.scale, out=self.out, lse=self.lse, workspace=self.ws, status=self.status)
         if events:
             events[1].record()
-        bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], self.cache_k, self.cache_v,
-                                0, status=self.status)
+        if self.fp8_mode is None:
+            bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], self.cache_k,
+                                    self.cache_v, 0, status=self.status)
+        else:
+            bca.prefix_cache_append_fp8(d["k"], d["v"], d["cu"], d["cu_pre"], self.cache_k,
+                                        self.cache_v, self.scale_k, self.scale_v, 0,
+                                        mode=self.fp8_mode, status=self.status)
         if events:
             events[2].record()
-        bca.prefix_decode(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"], d["k_tgt"],
-                          d["v_tgt"], d["cu_tgt"], self.N, self.P, self.scale, out=self.dout,
-                          lse=self.dlse, status=self.status)
+        if self.fp8_mode is None:
+            bca.prefix_decode(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"], d["k_tgt"],
+                              d["v_tgt"], d["cu_tgt"], self.N, self.P, self.scale, out=self.dout,
+                              lse=self.dlse, status=self.status)
+        else:
+            bca.prefix_decode_fp8(d["q_tgt"], self.cache_k, self.cache_v, self.scale_k,
+                                  self.scale_v, 0, d["cu_pre"], d["k_tgt"], d["v_tgt"],
+                                  d["cu_tgt"], self.N, self.P, self.scale, mode=self.fp8_mode,
+                                  out=self.dout, lse=self.dlse, workspace=self.dec_ws,
+                                  status=self.status)
         if events:
             events[3].record()
+
+
+def fp8_decode_psnr(prob: "Problem", dev) -> float:
+    """PSNR (dB, peak = max |reference|) of the decode output over the FP8 cache
+    against the same decode over a bf16 cache of the same prefix."""
+    import prefix_kv_gb300 as bca
+    d = prob.dev
+    ck = torch.empty((1, prob.H, prob.P, 128), dtype=torch.bfloat16, device=dev)
+    cv = torch.empty_like(ck)
+    bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], ck, cv, 0, status=prob.status)
+    ref, _ = bca.prefix_decode(d["q_tgt"], ck, cv, 0, d["cu_pre"], d["k_tgt"], d["v_tgt"],
+                               d["cu_tgt"], prob.N, prob.P, prob.scale, status=prob.status)
+    prob.step(d)
+    torch.cuda.synchronize()
+    ref = ref.float()
+    mse = (prob.dout.float() - ref).pow(2).mean().item()
+    peak = ref.abs().max().item()
+    del ck, cv
+    return round(10 * math.log10(peak * peak / mse), 2) if mse > 0 else float("inf")
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -265,6 +319,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8-v", "fp8-kv"],
+                    help="prefix cache format: bf16, or E4M3 with V / K and V quantised")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -290,7 +346,7 @@ def main():
         build()
 
     import prefix_kv_gb300 as bca
-    prob = Problem(dev, with_host=not args.no_e2e)
+    prob = Problem(dev, with_host=not args.no_e2e, cache=args.cache)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -333,6 +389,11 @@ def main():
     pre_tf = prob.flops_prefill / (s_pre / K * 1e-3) / 1e12
     dec_tf = prob.flops_decode / (s_dec / K * 1e-3) / 1e12
     app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9
+
+    # ---- FP8 cache: PSNR of the decode output against a bf16 cache (untimed) ---------
+    psnr = None
+    if prob.fp8_mode is not None:
+        psnr = fp8_decode_psnr(prob, dev)
 
     # ---- e2e through the public API with host buffers -------------------------------
     e2e = None
@@ -404,6 +465,9 @@ def main():
         "config": {"workload": WORKLOAD, "batch": 1, "seq_len": prob.S, "num_heads": prob.H,
                    "head_dim": 128, "prefix_len": prob.P, "target_len": prob.N,
                    "step": "schedule prep + prefill + cache append + prefix decode",
+                   "prefix_cache": {"bf16": "bf16", "fp8-v": "V in FP8 E4M3 (per token-head "
+                                    "fp32 scale), K bf16", "fp8-kv": "K and V in FP8 E4M3 "
+                                    "(per token-head fp32 scales)"}[args.cache],
                    "l2": "flushed (256 MiB write) between timed steps",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_bf16_peak": round(100 * value / peaks["bf16"], 2),
@@ -412,10 +476,11 @@ def main():
                       "append_frac_of_hbm": round(app_gbs / peaks["hbm"], 4),
                       "decode_ms": round(s_dec / K, 4), "decode_tflops": round(dec_tf, 2),
                       "decode_frac": round(dec_tf / peaks["bf16"], 4)},
+        "fp8_decode_psnr_db_vs_bf16_cache": psnr,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": 4 * K,
+        "gpu_launches": prob.launches * K,
         "clocks": clocks.summary(),
     }
     print(json.dumps(line), flush=True)
