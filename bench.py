@@ -146,7 +146,7 @@ class ClockSampler:
 class Problem:
     """The workload's tensors, resident on the device (plus pinned host copies for e2e)."""
 
-    def __init__(self, dev, with_host=True, cache="bf16"):
+    def __init__(self, dev, with_host=True, cache="bf16", prologue=False):
         from prefix_kv_gb300 import flops
         from prefix_kv_gb300 import workloads as W
         wl = W.by_name(WORKLOAD)
@@ -204,10 +204,38 @@ class Problem:
             self.append_bytes = rows * 2 * (256 + 128 + 4)
         # kernel launches per step: schedule prep, prefill, append, [expansions], decode
         self.launches = 4 + {None: 0, "v": 1, "kv": 2}[self.fp8_mode]
+        # optional Q/K prologue (RMS norm + three-axis RoPE; the prefill-side call also
+        # appends): coordinates and rotation table once per layout, outside the step
+        self.prologue = prologue
+        # named segments of the step, between consecutive CUDA events
+        self.segments = (["prologue", "prefill", "target_prologue", "decode"] if prologue
+                         else ["prefill", "append", "decode"])
+        if prologue:
+            if self.fp8_mode is not None:
+                raise SystemExit("--prologue appends a bf16 cache; combine it with --cache bf16")
+            d = self.dev
+            gw = torch.from_numpy(wl.grid_widths()).to(dev)
+            pos3 = bca.rope_positions(d["block_id"], d["cu"], gw, status=self.status)
+            self.table = bca.rope_table(pos3)
+            self.table_tgt = self.table[torch.from_numpy(wl.target_rows()).to(dev)].contiguous()
+            self.q_rot = torch.empty_like(d["q"])
+            self.k_rot = torch.empty_like(d["k"])
+            self.qt_rot = torch.empty_like(d["q_tgt"])
+            self.kt_rot = torch.empty_like(d["k_tgt"])
+            g = torch.Generator("cpu")
+            g.manual_seed(5)
+            self.gamma_q = (1 + 0.1 * torch.randn(128, generator=g)).to(dev)
+            self.gamma_k = (1 + 0.1 * torch.randn(128, generator=g)).to(dev)
+            self.launches += 1            # the target-side prologue (the append is fused)
+            rows = self.S * self.H
+            self.prologue_bytes = (rows * 4 * 256 + self.P * self.H * 3 * 256 + self.S * 512
+                                   + self.N * self.H * 4 * 256 + self.N * 512)
 
     def step(self, d, events=None):
         """The whole path through the binding; `events` = 4 CUDA events to split it."""
         import prefix_kv_gb300 as bca
+        if self.prologue:
+            return self.step_prologue(d, events)
         if events:
             events[0].record()
         bca.prefill(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"], self.S, self.S,
@@ -254,6 +282,38 @@ def fp8_decode_psnr(prob: "Problem", dev) -> float:
     peak = ref.abs().max().item()
     del ck, cv
     return round(10 * math.log10(peak * peak / mse), 2) if mse > 0 else float("inf")
+
+
+def _prologue_step(self, d, events=None):
+    """The step with the Q/K prologue: norm + RoPE + append, prefill on the rotated
+    Q/K; norm + RoPE of the target rows, decode over the cache.  Events split it
+    into (prologue + prefill, prologue, decode) at the same four marks."""
+    import prefix_kv_gb300 as bca
+    if events:
+        events[0].record()
+    bca.qk_norm_rope_append(d["q"], d["k"], self.table, d["cu"], v=d["v"], cu_prefix=d["cu_pre"],
+                            cache_k=self.cache_k, cache_v=self.cache_v, layer=0,
+                            gamma_q=self.gamma_q, gamma_k=self.gamma_k, q_out=self.q_rot,
+                            k_out=self.k_rot, status=self.status)
+    if events:
+        events[1].record()
+    bca.prefill(self.q_rot, self.k_rot, d["v"], d["block_id"], d["cu"], d["cu"], self.S, self.S,
+                self.scale, out=self.out, lse=self.lse, workspace=self.ws, status=self.status)
+    if events:
+        events[2].record()
+    bca.qk_norm_rope_append(d["q_tgt"], d["k_tgt"], self.table_tgt, d["cu_tgt"],
+                            gamma_q=self.gamma_q, gamma_k=self.gamma_k, q_out=self.qt_rot,
+                            k_out=self.kt_rot, status=self.status)
+    if events:
+        events[3].record()
+    bca.prefix_decode(self.qt_rot, self.cache_k, self.cache_v, 0, d["cu_pre"], self.kt_rot,
+                      d["v_tgt"], d["cu_tgt"], self.N, self.P, self.scale, out=self.dout,
+                      lse=self.dlse, status=self.status)
+    if events:
+        events[4].record()
+
+
+Problem.step_prologue = _prologue_step
 
 
 # ----------------------------------------------------------------------------- oracle timing
@@ -319,6 +379,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--prologue", action="store_true",
+                    help="add the fused Q/K RMS norm + three-axis RoPE (+ cache append) "
+                         "before prefill and decode")
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8-v", "fp8-kv"],
                     help="prefix cache format: bf16, or E4M3 with V / K and V quantised")
     args = ap.parse_args()
@@ -346,7 +409,7 @@ def main():
         build()
 
     import prefix_kv_gb300 as bca
-    prob = Problem(dev, with_host=not args.no_e2e, cache=args.cache)
+    prob = Problem(dev, with_host=not args.no_e2e, cache=args.cache, prologue=args.prologue)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -357,7 +420,9 @@ def main():
     if code != 0:
         raise SystemExit(f"device status {code} after warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    nseg = len(prob.segments)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nseg + 1)]
+           for _ in range(args.steps)]
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
@@ -372,23 +437,25 @@ def main():
     if code != 0:
         raise SystemExit(f"device status {code} after timed steps")
 
-    t_pre = [e[0].elapsed_time(e[1]) for e in evs]
-    t_app = [e[1].elapsed_time(e[2]) for e in evs]
-    t_dec = [e[2].elapsed_time(e[3]) for e in evs]
-    t_step = [e[0].elapsed_time(e[3]) for e in evs]
-    tot_ms = sum(t_step)
+    seg_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(nseg)]
+    tot_ms = sum(e[0].elapsed_time(e[nseg]) for e in evs)
     if dist is not None:
-        t = torch.tensor([tot_ms, sum(t_pre), sum(t_app), sum(t_dec)], device=dev)
+        t = torch.tensor([tot_ms] + seg_ms, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms, s_pre, s_app, s_dec = t.tolist()
-    else:
-        s_pre, s_app, s_dec = sum(t_pre), sum(t_app), sum(t_dec)
+        tot_ms, seg_ms = t[0].item(), t[1:].tolist()
+    seg = dict(zip(prob.segments, seg_ms))
+    s_pre, s_dec = seg["prefill"], seg["decode"]
     K = args.steps
     step_flops = prob.flops_prefill + prob.flops_decode
     value = world * K * step_flops / (tot_ms * 1e-3) / 1e12
     pre_tf = prob.flops_prefill / (s_pre / K * 1e-3) / 1e12
     dec_tf = prob.flops_decode / (s_dec / K * 1e-3) / 1e12
-    app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9
+    if prob.prologue:
+        s_app = seg["prologue"] + seg["target_prologue"]
+        app_gbs = prob.prologue_bytes / (s_app / K * 1e-3) / 1e9
+    else:
+        s_app = seg["append"]
+        app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9
 
     # ---- FP8 cache: PSNR of the decode output against a bf16 cache (untimed) ---------
     psnr = None
@@ -464,7 +531,9 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": WORKLOAD, "batch": 1, "seq_len": prob.S, "num_heads": prob.H,
                    "head_dim": 128, "prefix_len": prob.P, "target_len": prob.N,
-                   "step": "schedule prep + prefill + cache append + prefix decode",
+                   "step": ("Q/K RMS norm + 3-axis RoPE + cache append, schedule prep + "
+                            "prefill, target Q/K norm + RoPE, prefix decode") if prob.prologue
+                           else "schedule prep + prefill + cache append + prefix decode",
                    "prefix_cache": {"bf16": "bf16", "fp8-v": "V in FP8 E4M3 (per token-head "
                                     "fp32 scale), K bf16", "fp8-kv": "K and V in FP8 E4M3 "
                                     "(per token-head fp32 scales)"}[args.cache],
@@ -472,8 +541,10 @@ def main():
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "pct_of_bf16_peak": round(100 * value / peaks["bf16"], 2),
         "breakdown": {"prefill_ms": round(s_pre / K, 4), "prefill_tflops": round(pre_tf, 2),
-                      "append_ms": round(s_app / K, 4), "append_gbs": round(app_gbs, 1),
-                      "append_frac_of_hbm": round(app_gbs / peaks["hbm"], 4),
+                      ("prologue_ms" if prob.prologue else "append_ms"): round(s_app / K, 4),
+                      ("prologue_gbs" if prob.prologue else "append_gbs"): round(app_gbs, 1),
+                      ("prologue_frac_of_hbm" if prob.prologue else "append_frac_of_hbm"):
+                          round(app_gbs / peaks["hbm"], 4),
                       "decode_ms": round(s_dec / K, 4), "decode_tflops": round(dec_tf, 2),
                       "decode_frac": round(dec_tf / peaks["bf16"], 4)},
         "fp8_decode_psnr_db_vs_bf16_cache": psnr,

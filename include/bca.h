@@ -252,6 +252,56 @@ bca_status bca_prefix_decode_fp8(const void* q_tgt, const void* cache_k, const v
                                  void* workspace, size_t workspace_bytes, int32_t* status_dev,
                                  void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Q/K prologue: per-head RMS normalisation, three-axis RoPE and the append of
+ * the rotated prefix keys ("Qwen-Image 2.1: Block-Causal Attention, Prefix KV
+ * Cache, and Turbo", flozi.net: Q and K are RMS-normalised per head before
+ * RoPE; "Three-axis RoPE preserves image geometry": head dimensions split
+ * (16, 56, 56) across frame, height and width, base 10000; "Timestep-zero
+ * conditioning makes the prefix invariant": the cache holds post-RoPE K). */
+
+/* Coordinates of every packed token, pos3: device int32 [total][3] = (frame,
+ * height, width).  Per sequence a running coordinate c starts at 0; a text
+ * token (block id -1) takes (c, c, c) and advances c by one; an image block
+ * (one contiguous run of a non-negative id i) of n tokens with width
+ * w = grid_w[b * n_ids + i] (n a multiple of w, height n / w, tokens row-major)
+ * takes frame c and (row - height/2, column - width/2), then advances c by one.
+ * block_id: device int32 [total]; cu_seqlens: device int32 [batch+1]; grid_w:
+ * device int32 [batch][n_ids] (n_ids <= 4096, else BCA_ERR_UNSUPPORTED).  A
+ * sequence with an id >= n_ids or < -1, an id in two runs, or a block whose
+ * length is not a multiple of its width is reported as BCA_ERR_BLOCK_ID and
+ * its coordinates are not written. */
+bca_status bca_rope_positions(const int32_t* block_id, const int32_t* cu_seqlens, int32_t batch,
+                              int32_t total, const int32_t* grid_w, int32_t n_ids,
+                              int32_t* pos3, int32_t* status_dev, void* stream);
+
+/* Rotation table: table[t][j] = (cos, sin) of the angle of dimension pair j of
+ * token t, fp32 [total][64][2] (16-byte aligned).  Pair j < 8 is frame pair
+ * k = j, j < 36 height pair k = j - 8, else width pair k = j - 36; the angle is
+ * coordinate * 10000^(-2k/d) with d = 16, 56, 56; computed in double. */
+bca_status bca_rope_table(const int32_t* pos3, int32_t total, float* table, void* stream);
+
+/* For every (token, head) row of q and k (device bf16 [total][H][128]):
+ *   y = x / sqrt(mean(x^2) + eps) * gamma        (fp32; gamma = 1 when null)
+ *   pair (y[2j], y[2j+1]) -> (y0 cos - y1 sin, y0 sin + y1 cos) by rope_table row t
+ * written as bf16 to q_out / k_out (which may be q / k: in place is allowed).
+ * gamma_q, gamma_k: device fp32 [128] (16-byte aligned) or null.  When cu_prefix (device int32
+ * [batch+1]) is not null, the rotated keys and the values (v, device bf16
+ * [total][H][128]) of the first cu_prefix[b+1]-cu_prefix[b] tokens of each
+ * sequence are also written to cache tokens cu_prefix[b].. of layer `layer` of
+ * cache_k / cache_v (bf16 [num_layers][H][capacity][128]); the cache K row is
+ * bit-identical to the k_out row.  Validation and errors of the cache write are
+ * those of bca_prefix_cache_append (nothing is written when they fail); with a
+ * null cu_prefix, v and the cache arguments are not read. */
+bca_status bca_qk_norm_rope_append(const void* q, const void* k, const void* v,
+                                   const float* gamma_q, const float* gamma_k,
+                                   const float* rope_table, const int32_t* cu_seqlens,
+                                   const int32_t* cu_prefix, int32_t batch, int32_t num_heads,
+                                   int32_t head_dim, int32_t total, float eps, void* q_out,
+                                   void* k_out, void* cache_k, void* cache_v, int32_t layer,
+                                   int32_t num_layers, int64_t capacity, int32_t* status_dev,
+                                   void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -6,8 +6,10 @@ this package is its thin Python binding plus the seeded workload generator.
 from .api import (check_status, new_status, prefill, prefill_workspace_bytes,  # noqa: F401
                   prefix_cache_append, prefix_cache_append_fp8, prefix_decode, prefix_decode_fp8,
                   prefix_decode_fp8_workspace_bytes, prefix_cache_dequant_fp8,
-                  read_status, schedule_prep)
+                  qk_norm_rope_append, read_status, rope_positions, rope_table,
+                  schedule_prep)
 
 __all__ = ["prefill", "prefix_decode", "prefix_decode_fp8", "prefix_decode_fp8_workspace_bytes",
            "prefix_cache_dequant_fp8", "prefix_cache_append", "prefix_cache_append_fp8", "schedule_prep",
-           "prefill_workspace_bytes", "new_status", "read_status", "check_status"]
+           "prefill_workspace_bytes", "new_status", "read_status", "check_status",
+           "rope_positions", "rope_table", "qk_norm_rope_append"]

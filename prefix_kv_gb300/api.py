@@ -275,3 +275,71 @@ def prefix_decode_fp8(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: int, cu_
         _ptr(status), _stream(stream))
     _native.check(code, "bca_prefix_decode_fp8")
     return out, lse
+
+
+def rope_positions(block_id, cu_seqlens, grid_w, status=None, stream=None):
+    """(frame, height, width) RoPE coordinates, int32 ``[total, 3]``.
+
+    ``grid_w``: int32 ``[batch, n_ids]`` width in tokens of image block ``i`` of
+    sequence ``b`` (entries of absent ids are not read)."""
+    _need(block_id, "block_id", torch.int32, 1)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    _need(grid_w, "grid_w", torch.int32, 2)
+    total = block_id.numel()
+    batch = cu_seqlens.numel() - 1
+    if grid_w.shape[0] != batch:
+        raise ValueError("grid_w must have one row per sequence")
+    pos3 = torch.empty((total, 3), dtype=torch.int32, device=block_id.device)
+    code = _native.load().bca_rope_positions(_ptr(block_id), _ptr(cu_seqlens), batch, total,
+                                             _ptr(grid_w), grid_w.shape[1], _ptr(pos3),
+                                             _ptr(status), _stream(stream))
+    _native.check(code, "bca_rope_positions")
+    return pos3
+
+
+def rope_table(pos3, stream=None):
+    """fp32 ``[total, 64, 2]`` (cos, sin) of every token's 64 dimension pairs."""
+    _need(pos3, "pos3", torch.int32, 2)
+    total = pos3.shape[0]
+    table = torch.empty((total, 64, 2), dtype=torch.float32, device=pos3.device)
+    code = _native.load().bca_rope_table(_ptr(pos3), total, _ptr(table), _stream(stream))
+    _native.check(code, "bca_rope_table")
+    return table
+
+
+def qk_norm_rope_append(q, k, table, cu_seqlens, v=None, cu_prefix=None, cache_k=None,
+                        cache_v=None, layer: int = 0, gamma_q=None, gamma_k=None,
+                        eps: float = 1e-6, q_out=None, k_out=None, status=None, stream=None):
+    """RMS-normalise and rotate Q and K (``[total, H, 128]`` bf16); with ``cu_prefix``
+    also write the rotated prefix keys and the values into ``cache_{k,v}[layer]``.
+    Returns ``(q_out, k_out)``; pass ``q_out=q, k_out=k`` to work in place."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(table, "table", torch.float32, 3)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    total, H, D = q.shape
+    if k.shape != q.shape or tuple(table.shape) != (total, 64, 2):
+        raise ValueError("q, k and table shapes do not match")
+    for name, g in (("gamma_q", gamma_q), ("gamma_k", gamma_k)):
+        if g is not None:
+            _need(g, name, torch.float32, 1)
+    L, cap = 1, 0
+    if cu_prefix is not None:
+        _need(cu_prefix, "cu_prefix", torch.int32, 1)
+        _need(v, "v", torch.bfloat16, 3)
+        _need(cache_k, "cache_k", torch.bfloat16, 4)
+        _need(cache_v, "cache_v", torch.bfloat16, 4)
+        L, Hc, cap, Dc = cache_k.shape
+        if (Hc, Dc) != (H, D) or cache_v.shape != cache_k.shape or v.shape != q.shape:
+            raise ValueError("cache / v shapes do not match q")
+    if q_out is None:
+        q_out = torch.empty_like(q)
+    if k_out is None:
+        k_out = torch.empty_like(k)
+    batch = cu_seqlens.numel() - 1
+    code = _native.load().bca_qk_norm_rope_append(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(gamma_q), _ptr(gamma_k), _ptr(table), _ptr(cu_seqlens),
+        _ptr(cu_prefix), batch, H, D, total, float(eps), _ptr(q_out), _ptr(k_out),
+        _ptr(cache_k), _ptr(cache_v), layer, L, cap, _ptr(status), _stream(stream))
+    _native.check(code, "bca_qk_norm_rope_append")
+    return q_out, k_out

@@ -1,5 +1,5 @@
 // The exported C ABI: argument validation, workspace carving and launches.
-#include "common.cuh"
+#include "kernels.cuh"
 
 #include <cmath>
 
@@ -344,6 +344,59 @@ bca_status bca_prefix_cache_append_fp8(const void* k, const void* v, const int32
       static_cast<uint8_t*>(cache_v) + layer * rows * kHeadDim,
       quant_k ? scale_k + layer * rows : nullptr, scale_v + layer * rows, capacity, status_dev,
       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
+bca_status bca_rope_positions(const int32_t* block_id, const int32_t* cu_seqlens, int32_t batch,
+                              int32_t total, const int32_t* grid_w, int32_t n_ids,
+                              int32_t* pos3, int32_t* status_dev, void* stream) {
+  if (batch < 0 || total < 0 || n_ids < 0) return BCA_ERR_INVALID_ARG;
+  if (batch == 0 || total == 0) return BCA_OK;
+  if (!block_id || !cu_seqlens || !pos3 || (n_ids > 0 && !grid_w)) return BCA_ERR_INVALID_ARG;
+  if (n_ids > 4096 || batch > 65535) return BCA_ERR_UNSUPPORTED;
+  const cudaError_t e = launch_rope_positions(block_id, cu_seqlens, batch, grid_w, n_ids, pos3,
+                                              status_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
+bca_status bca_rope_table(const int32_t* pos3, int32_t total, float* table, void* stream) {
+  if (total < 0) return BCA_ERR_INVALID_ARG;
+  if (total == 0) return BCA_OK;
+  if (!pos3 || !table || (reinterpret_cast<uintptr_t>(table) & 15u)) return BCA_ERR_INVALID_ARG;
+  const cudaError_t e = launch_rope_table(pos3, total, table, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
+bca_status bca_qk_norm_rope_append(const void* q, const void* k, const void* v,
+                                   const float* gamma_q, const float* gamma_k,
+                                   const float* rope_table, const int32_t* cu_seqlens,
+                                   const int32_t* cu_prefix, int32_t batch, int32_t num_heads,
+                                   int32_t head_dim, int32_t total, float eps, void* q_out,
+                                   void* k_out, void* cache_k, void* cache_v, int32_t layer,
+                                   int32_t num_layers, int64_t capacity, int32_t* status_dev,
+                                   void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads <= 0 || total < 0 || !(eps >= 0.f) || !std::isfinite(eps))
+    return BCA_ERR_INVALID_ARG;
+  if (batch == 0 || total == 0) return BCA_OK;
+  if (!q || !k || !rope_table || !cu_seqlens || !q_out || !k_out) return BCA_ERR_INVALID_ARG;
+  const bool append = cu_prefix != nullptr;
+  if (append && (!v || layer < 0 || num_layers <= 0 || layer >= num_layers || capacity < 0 ||
+                 (capacity > 0 && (!cache_k || !cache_v))))
+    return BCA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_out) || !aligned16(k_out) ||
+      !aligned16(cache_k) || !aligned16(cache_v) || !aligned16(rope_table) ||
+      !aligned16(gamma_q) || !aligned16(gamma_k))
+    return BCA_ERR_INVALID_ARG;
+  const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
+  void* ck = append && capacity > 0 ? static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems
+                                    : nullptr;
+  void* cv = append && capacity > 0 ? static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems
+                                    : nullptr;
+  const cudaError_t e = launch_qk_norm_rope(q, k, v, gamma_q, gamma_k, rope_table, cu_seqlens,
+                                            cu_prefix, batch, num_heads, total, eps, q_out, k_out,
+                                            ck, cv, capacity, status_dev,
+                                            static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
 }
 

@@ -12,7 +12,7 @@
 // reads walk the packed tensor in order, writes land in 256-byte runs.
 // Validation (capacity, prefix <= sequence) is done by every thread before it
 // writes anything, so a failing call writes nothing.
-#include "common.cuh"
+#include "kernels.cuh"
 #include "ptx.cuh"
 
 namespace bca {

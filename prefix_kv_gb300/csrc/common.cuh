@@ -54,22 +54,4 @@ struct AttnLaunch {
 };
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream);  // returns bca_status
 
-cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_k,
-                                const int32_t* cu_prefix, int batch, int num_heads,
-                                void* cache_k_layer, void* cache_v_layer, int64_t capacity,
-                                int32_t* status, cudaStream_t stream);
-
-cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t* cu_k,
-                                    const int32_t* cu_prefix, int batch, int num_heads,
-                                    bool quant_k, void* cache_k_layer, void* cache_v_layer,
-                                    float* scale_k_layer, float* scale_v_layer, int64_t capacity,
-                                    int32_t* status, cudaStream_t stream);
-
-// E4M3 cache rows cu_prefix[0] .. cu_prefix[batch]-1 of one layer ([H][cap][128]
-// codes, [H][cap] scales) expanded to bf16 value * scale, same layout.
-cudaError_t launch_cache_dequant_fp8(const void* codes_layer, const float* scales_layer,
-                                     const int32_t* cu_prefix, int batch, int num_heads,
-                                     int64_t capacity, void* out_layer, int32_t* status,
-                                     cudaStream_t stream);
-
 }  // namespace bca

@@ -91,10 +91,34 @@ class Workload:
         rows = [np.arange(cu[b + 1] - n, cu[b + 1]) for b, n in enumerate(self.target_lens())]
         return np.concatenate(rows).astype(np.int64)
 
+    def grid_widths(self) -> np.ndarray:
+        """Width in latent tokens of every image block, int32 ``[batch, n_ids]``
+        (0 where a sequence has no such id): square images (4x4, 64x64, 128x128)
+        use the side; other spans the largest divisor of their length not above
+        its square root."""
+        n_ids = 1 + max([s.block for segs in self.seqs for s in segs] + [0])
+        out = np.zeros((self.batch, n_ids), dtype=np.int32)
+        for b, segs in enumerate(self.seqs):
+            for s in segs:
+                if s.is_image:
+                    out[b, s.block] = image_width(s.length)
+        return out
+
     def prefix_rows(self) -> np.ndarray:
         cu = self.cu_seqlens()
         rows = [np.arange(cu[b], cu[b] + p) for b, p in enumerate(self.prefix_lens())]
         return np.concatenate(rows).astype(np.int64) if rows else np.zeros(0, np.int64)
+
+
+def image_width(n: int) -> int:
+    """Largest divisor of ``n`` not above sqrt(n) (the side of a square image)."""
+    best = 1
+    d = 1
+    while d * d <= n:
+        if n % d == 0:
+            best = d
+        d += 1
+    return best
 
 
 # ---- tensors -----------------------------------------------------------------
