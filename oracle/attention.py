@@ -145,6 +145,48 @@ def prefill(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, softmax_scale: float,
     return out, lse
 
 
+def piece_mask(is_text: bool, q_len: int, kv_len: int) -> np.ndarray:
+    """Mask of one piece: a text piece is causal over itself, bottom-right aligned
+    (``ones(q_len, kv_len).tril(kv_len - q_len)``); an image piece sees every key."""
+    if is_text:
+        return np.tril(np.ones((q_len, kv_len), dtype=bool), kv_len - q_len)
+    return np.ones((q_len, kv_len), dtype=bool)
+
+
+def prefill_piecewise(q, k, v, block_id, cu_seqlens, softmax_scale: float):
+    """Block-causal prefill as separate exact attention calls, one per segment.
+
+    Qwen-Image 2.1 deployment notes, piecewise-attention paragraph, and flozi
+    "Two exact attention paths": the default diffusers processor runs one
+    attention call for every text or image segment of the prefix and one for
+    the target.  The queries of segment [a, e) of a sequence starting at s
+    attend over keys [s, e): a text segment with its causal triangle
+    (bottom-right aligned), an image segment (the target included) with no
+    mask.  Square sequences only (every query has its own key).  Returns
+    ``out [total, H, D]`` and ``lse [H, total]`` (float64).
+    """
+    bid = _i64(block_id)
+    cu = _i64(cu_seqlens)
+    total, H, D = q.shape
+    out = np.zeros((total, H, D))
+    lse = np.zeros((H, total))
+    for b in range(len(cu) - 1):
+        s, end = cu[b], cu[b + 1]
+        a = s
+        while a < end:
+            e = a + 1
+            while e < end and bid[e] == bid[a]:
+                e += 1
+            mask = piece_mask(bid[a] < 0, e - a, e - s)
+            for h in range(H):
+                o, l = masked_attention(_f64(q[a:e, h]), _f64(k[s:e, h]), _f64(v[s:e, h]), mask,
+                                        softmax_scale)
+                out[a:e, h] = o
+                lse[h, a:e] = l
+            a = e
+    return out, lse
+
+
 def prefix_decode(q_tgt, k_prefix, v_prefix, cu_prefix, k_tgt, v_tgt, cu_seqlens_q,
                   softmax_scale: float, rows=None, heads=None):
     """Cached-step attention: target queries over [prefix K/V; target K/V], no mask.

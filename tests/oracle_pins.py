@@ -336,11 +336,32 @@ def pin_cache_append_layout(orc):
     assert (ck[0] == -7).all() and (ck[1, :, 7:] == -7).all()
 
 
+def pin_piecewise_equals_block_causal(orc):
+    """The pages call both prefill paths exact: per-segment attention calls (text
+    causal over itself, images over everything before and themselves) equal the
+    one block-causal masked attention, on every valid layout up to length 6 and
+    on the tiny layout."""
+    H = 1
+    for n in range(1, 7):
+        for bid in _valid_layouts(n):
+            q, k, v = _rng_arrays(100 + n, (n, H, D), (n, H, D), (n, H, D))
+            cu = np.array([0, n])
+            o1, l1 = orc.prefill(q, k, v, bid, cu, cu, SCALE)
+            o2, l2 = orc.prefill_piecewise(q, k, v, bid, cu, SCALE)
+            assert np.allclose(o1, o2, rtol=0, atol=1e-12), bid
+            assert np.allclose(l1, l2, rtol=0, atol=1e-12), bid
+    bid, q, k, v = _tiny_inputs(13)
+    cu = np.array([0, 40])
+    o1, l1 = orc.prefill(q, k, v, bid, cu, cu, SCALE)
+    o2, l2 = orc.prefill_piecewise(q, k, v, bid, cu, SCALE)
+    assert np.allclose(o1, o2, rtol=0, atol=1e-12) and np.allclose(l1, l2, rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
     pin_worked_example_mask, pin_bottom_right, pin_tiny_layout, pin_adjacent_references,
     pin_brute_force_small, pin_zero_query_closed_form, pin_causal_text_equals_sdpa,
     pin_single_block_equals_full, pin_decode_equals_full, pin_large_scores_stable,
     pin_constant_values, pin_prefix_independent_of_target, pin_cached_equals_uncached,
     pin_short_q_rows_match_square, pin_varlen_matches_separate, pin_row_sampling,
-    pin_cache_append_layout,
+    pin_cache_append_layout, pin_piecewise_equals_block_causal,
 ]

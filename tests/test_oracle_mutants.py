@@ -32,7 +32,13 @@ def _vis_variant(causal_op="ge", text_matches_text=False, image_clause=True):
     return vis
 
 
+_real_piece_mask = orc.piece_mask
+
 MUTANTS = {
+    "piecewise_text_top_left": ("piece_mask",
+                                lambda is_text, q_len, kv_len:
+                                np.tril(np.ones((q_len, kv_len), dtype=bool))
+                                if is_text else _real_piece_mask(is_text, q_len, kv_len)),
     "top_left_alignment": ("query_positions",
                            lambda q_len, kv_len, rows=None:
                            np.arange(q_len) if rows is None else np.asarray(rows)),
