@@ -146,7 +146,7 @@ class ClockSampler:
 class Problem:
     """The workload's tensors, resident on the device (plus pinned host copies for e2e)."""
 
-    def __init__(self, dev, with_host=True, cache="bf16", prologue=False):
+    def __init__(self, dev, with_host=True, cache="bf16", prologue=False, piecewise=False):
         from prefix_kv_gb300 import flops
         from prefix_kv_gb300 import workloads as W
         wl = W.by_name(WORKLOAD)
@@ -207,10 +207,21 @@ class Problem:
         # optional Q/K prologue (RMS norm + three-axis RoPE; the prefill-side call also
         # appends): coordinates and rotation table once per layout, outside the step
         self.prologue = prologue
+        # the piecewise baseline: one prefill call per segment (two kernels + a copy each)
+        self.piecewise = piecewise
+        if piecewise:
+            self.bid_host = wl.block_id()
+            self.cu_host = wl.cu_seqlens()
+            self.pw_ws = torch.empty(bca.prefill_piecewise_workspace_bytes(
+                self.bid_host, self.cu_host, self.H), dtype=torch.uint8, device=dev)
+            n_pieces = int(np.count_nonzero(np.diff(self.bid_host))) + 1
+            self.launches += 2 * n_pieces - 2
         # named segments of the step, between consecutive CUDA events
         self.segments = (["prologue", "prefill", "target_prologue", "decode"] if prologue
                          else ["prefill", "append", "decode"])
         if prologue:
+            if piecewise:
+                raise SystemExit("--prologue runs the single-launch prefill; drop --piecewise")
             if self.fp8_mode is not None:
                 raise SystemExit("--prologue appends a bf16 cache; combine it with --cache bf16")
             d = self.dev
@@ -238,8 +249,14 @@ class Problem:
             return self.step_prologue(d, events)
         if events:
             events[0].record()
-        bca.prefill(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"], self.S, self.S,
-                    self.scale, out=self.out, lse=self.lse, workspace=self.ws, status=self.status)
+        if self.piecewise:
+            bca.prefill_piecewise(d["q"], d["k"], d["v"], d["block_id"], self.bid_host,
+                                  self.cu_host, self.scale, out=self.out, lse=self.lse,
+                                  workspace=self.pw_ws, status=self.status)
+        else:
+            bca.prefill(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"], self.S, self.S,
+                        self.scale, out=self.out, lse=self.lse, workspace=self.ws,
+                        status=self.status)
         if events:
             events[1].record()
         if self.fp8_mode is None:
@@ -379,6 +396,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--piecewise", action="store_true",
+                    help="baseline: prefill as one attention call per segment")
     ap.add_argument("--prologue", action="store_true",
                     help="add the fused Q/K RMS norm + three-axis RoPE (+ cache append) "
                          "before prefill and decode")
@@ -409,7 +428,8 @@ def main():
         build()
 
     import prefix_kv_gb300 as bca
-    prob = Problem(dev, with_host=not args.no_e2e, cache=args.cache, prologue=args.prologue)
+    prob = Problem(dev, with_host=not args.no_e2e, cache=args.cache, prologue=args.prologue,
+                   piecewise=args.piecewise)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -521,7 +541,7 @@ def main():
                 "frac": round(pre_tf / peaks["bf16"], 4),
                 "peak_source": f"{peaks['source']} bf16 dense burst",
                 "frac_of_sustained": round(pre_tf / peaks["bf16_sustained"], 4),
-                "traffic": profiled_traffic(),
+                "traffic": None if prob.piecewise else profiled_traffic(),
                 "traffic_source": ATTN_PROFILE,
                 "algorithmic": f"{prob.flops_prefill:.4e} flop per launch "
                                f"({prob.pairs_prefill} visible pairs/head x 32 heads x 512)"}
@@ -533,6 +553,8 @@ def main():
                    "head_dim": 128, "prefix_len": prob.P, "target_len": prob.N,
                    "step": ("Q/K RMS norm + 3-axis RoPE + cache append, schedule prep + "
                             "prefill, target Q/K norm + RoPE, prefix decode") if prob.prologue
+                           else ("piecewise prefill (schedule prep + attention + lse copy per "
+                                 "segment) + cache append + prefix decode") if prob.piecewise
                            else "schedule prep + prefill + cache append + prefix decode",
                    "prefix_cache": {"bf16": "bf16", "fp8-v": "V in FP8 E4M3 (per token-head "
                                     "fp32 scale), K bf16", "fp8-kv": "K and V in FP8 E4M3 "

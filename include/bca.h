@@ -146,6 +146,30 @@ bca_status bca_prefill_noalloc(const void* q, const void* k, const void* v,
                                int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
                                void* out, float* lse, int32_t* status_dev, void* stream);
 
+/* Block-causal prefill as one exact attention call per segment, a baseline
+ * for bca_prefill (Qwen-Image 2.1 deployment notes, piecewise-attention
+ * paragraph; flozi.net "Two exact attention paths": the default diffusers
+ * processor runs one call for every text or image segment of the prefix and
+ * one for the target).  Segment [a, e) of sequence b (a maximal run of one
+ * block id) is computed as its own problem: queries [a, e) over keys
+ * [cu[b], e), a text segment causal over itself (bottom-right aligned), an
+ * image segment unmasked; the results equal bca_prefill's.  Square sequences
+ * only (the same cu_seqlens for q and k).  block_id: device int32 [total];
+ * block_id_host / cu_seqlens_host: the same ids and offsets in host memory
+ * (the segment table is built on the host).  q, k, v, out, lse as in
+ * bca_prefill.  workspace: device memory of
+ * bca_prefill_piecewise_workspace_bytes (16-byte aligned), reused by the
+ * pieces in stream order.  Launches two kernels and one 2-D copy per segment. */
+size_t bca_prefill_piecewise_workspace_bytes(const int32_t* block_id_host,
+                                             const int32_t* cu_seqlens_host, int32_t batch,
+                                             int32_t num_heads);
+bca_status bca_prefill_piecewise(const void* q, const void* k, const void* v,
+                                 const int32_t* block_id, const int32_t* block_id_host,
+                                 const int32_t* cu_seqlens_host, int32_t batch, int32_t num_heads,
+                                 int32_t head_dim, int32_t total, float softmax_scale, void* out,
+                                 float* lse, void* workspace, size_t workspace_bytes,
+                                 int32_t* status_dev, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Prefix-cache "decode" (cached denoising steps): the target queries of every
  * sequence attend, with no mask, over [cached prefix K/V; their own K/V]

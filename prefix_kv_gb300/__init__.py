@@ -3,7 +3,8 @@
 The compute lives in ``lib/libbca_gb300.so`` (C ABI declared in ``include/bca.h``);
 this package is its thin Python binding plus the seeded workload generator.
 """
-from .api import (check_status, new_status, prefill, prefill_workspace_bytes,  # noqa: F401
+from .api import (check_status, new_status, prefill, prefill_piecewise,  # noqa: F401
+                  prefill_piecewise_workspace_bytes, prefill_workspace_bytes,
                   prefix_cache_append, prefix_cache_append_fp8, prefix_decode, prefix_decode_fp8,
                   prefix_decode_fp8_workspace_bytes, prefix_cache_dequant_fp8,
                   qk_norm_rope_append, read_status, rope_positions, rope_table,
@@ -12,4 +13,5 @@ from .api import (check_status, new_status, prefill, prefill_workspace_bytes,  #
 __all__ = ["prefill", "prefix_decode", "prefix_decode_fp8", "prefix_decode_fp8_workspace_bytes",
            "prefix_cache_dequant_fp8", "prefix_cache_append", "prefix_cache_append_fp8", "schedule_prep",
            "prefill_workspace_bytes", "new_status", "read_status", "check_status",
-           "rope_positions", "rope_table", "qk_norm_rope_append"]
+           "rope_positions", "rope_table", "qk_norm_rope_append", "prefill_piecewise",
+           "prefill_piecewise_workspace_bytes"]

@@ -38,6 +38,9 @@ SIGNATURES = {
     "bca_prefix_decode_fp8_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, c_i64]),
     "bca_prefix_cache_dequant_fp8": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32,
                                              c_i64, c_vp, c_vp, c_vp]),
+    "bca_prefill_piecewise_workspace_bytes": (c_size, [c_vp, c_vp, c_i32, c_i32]),
+    "bca_prefill_piecewise": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32,
+                                      c_i32, c_f32, c_vp, c_vp, c_vp, c_size, c_vp, c_vp]),
     "bca_rope_positions": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp]),
     "bca_rope_table": (c_i32, [c_vp, c_i32, c_vp, c_vp]),
     "bca_qk_norm_rope_append": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,

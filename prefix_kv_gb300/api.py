@@ -8,6 +8,8 @@ runs in the library's kernels; there is no CPU or PyTorch fallback.
 from __future__ import annotations
 
 import math
+
+import numpy as np
 from typing import Optional, Tuple
 
 import torch
@@ -343,3 +345,47 @@ def qk_norm_rope_append(q, k, table, cu_seqlens, v=None, cu_prefix=None, cache_k
         _ptr(cache_k), _ptr(cache_v), layer, L, cap, _ptr(status), _stream(stream))
     _native.check(code, "bca_qk_norm_rope_append")
     return q_out, k_out
+
+
+def _host_i32(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def prefill_piecewise_workspace_bytes(block_id_host, cu_seqlens_host, num_heads: int) -> int:
+    bid, cu = _host_i32(block_id_host), _host_i32(cu_seqlens_host)
+    return int(_native.load().bca_prefill_piecewise_workspace_bytes(
+        bid.ctypes.data, cu.ctypes.data, len(cu) - 1, num_heads))
+
+
+def prefill_piecewise(q, k, v, block_id, block_id_host, cu_seqlens_host,
+                      softmax_scale: Optional[float] = None, out=None, lse=None, workspace=None,
+                      status=None, stream=None):
+    """Block-causal prefill as one attention call per segment (the piecewise baseline);
+    same results as ``prefill`` for square sequences.  ``block_id_host`` and
+    ``cu_seqlens_host`` are host copies (NumPy or CPU tensors) of the ids and offsets."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 3)
+    _need(block_id, "block_id", torch.int32, 1)
+    bid, cu = _host_i32(block_id_host), _host_i32(cu_seqlens_host)
+    total, H, D = q.shape
+    if k.shape != q.shape or v.shape != q.shape or bid.shape[0] != total:
+        raise ValueError("shapes do not match")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, total), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    if workspace is None:
+        workspace = torch.empty(prefill_piecewise_workspace_bytes(bid, cu, H), dtype=torch.uint8,
+                                device=q.device)
+    code = _native.load().bca_prefill_piecewise(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(block_id), bid.ctypes.data, cu.ctypes.data, len(cu) - 1,
+        H, D, total, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        workspace.numel(), _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefill_piecewise")
+    return out, lse

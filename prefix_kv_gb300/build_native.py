@@ -23,7 +23,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I" + INCLUDE]
 UNITS = ["attn_fwd.cu", "sched_prep.cu", "cache_append.cu", "bca_api.cu", "prefill_noalloc.cu", "selftest.cu",
-         "qk_prologue.cu"]
+         "qk_prologue.cu", "prefill_piecewise.cu"]
 
 
 def _nvcc() -> str:
