@@ -326,6 +326,76 @@ bca_status bca_qk_norm_rope_append(const void* q, const void* k, const void* v,
                                    int32_t num_layers, int64_t capacity, int32_t* status_dev,
                                    void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Paged prefix cache (SenseNova-U1 / Prism-Infer notes, prefix KV reuse: the
+ * cache is a pool of pages that requests with a common prefix share).  A page
+ * holds 128 consecutive prefix tokens of one sequence for every head of a
+ * layer: one layer of the pool is a bf16 cache [H][num_pages * 128][128], and
+ * prefix token t of sequence b lives at token page_table[b * max_pages +
+ * t / 128] * 128 + t % 128 (cache layout [num_layers][H][num_pages*128][128]).
+ * cu_prefix (device int32 [batch+1]) gives only the prefix lengths here.  A
+ * page entry outside [0, num_pages), or a prefix needing more than max_pages
+ * pages, is reported as BCA_ERR_CAPACITY on the status word and nothing of
+ * that call (append) or that sequence (decode) is written.  num_pages <= 2^24. */
+
+/* bca_prefix_cache_append through a page table. */
+bca_status bca_prefix_cache_append_paged(const void* k, const void* v,
+                                         const int32_t* cu_seqlens_k, const int32_t* cu_prefix,
+                                         const int32_t* page_table, int32_t max_pages,
+                                         int32_t batch, int32_t num_heads, int32_t head_dim,
+                                         int32_t total_k, void* cache_k, void* cache_v,
+                                         int32_t layer, int32_t num_layers, int32_t num_pages,
+                                         int32_t* status_dev, void* stream);
+
+/* bca_prefix_decode with the prefix read through a page table. */
+bca_status bca_prefix_decode_paged(const void* q_tgt, const void* cache_k, const void* cache_v,
+                                   int32_t layer, int32_t num_layers, int32_t num_pages,
+                                   const int32_t* cu_prefix, const int32_t* page_table,
+                                   int32_t max_pages, const void* k_tgt, const void* v_tgt,
+                                   const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
+                                   int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
+                                   int32_t max_prefix, float softmax_scale, void* out, float* lse,
+                                   int32_t* status_dev, void* stream);
+
+/* Copy rows [0, n_rows) (n_rows <= 128) of page src_page to page dst_page, all
+ * heads, K and V, of one layer: the copy of a shared tail page's common rows
+ * into a page of its own. */
+bca_status bca_pool_copy_rows(void* cache_k, void* cache_v, int32_t layer, int32_t num_layers,
+                              int32_t num_heads, int32_t num_pages, int32_t src_page,
+                              int32_t dst_page, int32_t n_rows, void* stream);
+
+/* Host-side page pool (page ids only; thread-safe).  Rules kept (same notes):
+ * a page joins the hit index only when its owner publishes it after the K/V
+ * write completed; a page from bca_pool_alloc is unpublished, so a copied tail
+ * page does not inherit the old entry's hash; idle cached pages (published,
+ * no references) are lent to allocations, least recently released first, but
+ * a referenced page is never reclaimed; capacity counts physical pages. */
+typedef struct bca_page_pool bca_page_pool;
+/* A pool of num_pages pages, all free; null for num_pages <= 0. */
+bca_page_pool* bca_pool_create(int32_t num_pages);
+void bca_pool_destroy(bca_page_pool* pool);
+/* n pages with one reference each into pages_out: free pages first, then idle
+ * cached pages (which leave the index).  BCA_ERR_CAPACITY, and nothing taken,
+ * when fewer than n are free or idle. */
+bca_status bca_pool_alloc(bca_page_pool* pool, int32_t n, int32_t* pages_out);
+/* The longest run hashes[0..h) of published pages; each gains a reference and
+ * its id goes to pages_out[i].  Returns h. */
+int32_t bca_pool_match(bca_page_pool* pool, const uint64_t* hashes, int32_t n,
+                       int32_t* pages_out);
+/* Put a referenced, unpublished page into the index under `hash` (unique);
+ * BCA_ERR_INVALID_ARG otherwise. */
+bca_status bca_pool_publish(bca_page_pool* pool, int32_t page, uint64_t hash);
+/* Drop one reference per listed page (a page may be listed more than once).
+ * An unreferenced published page stays cached (idle); an unpublished one is
+ * freed.  BCA_ERR_INVALID_ARG, and nothing changed, for a bad id or a drop
+ * below zero. */
+bca_status bca_pool_release(bca_page_pool* pool, const int32_t* pages, int32_t n);
+/* Unique physical pages that are free, idle cached, and referenced. */
+void bca_pool_stats(bca_page_pool* pool, int32_t* free_pages, int32_t* idle_cached,
+                    int32_t* in_use);
+/* References held on a page (-1 for a bad id). */
+int32_t bca_pool_refs(bca_page_pool* pool, int32_t page);
+
 #ifdef __cplusplus
 }
 #endif

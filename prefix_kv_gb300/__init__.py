@@ -3,7 +3,8 @@
 The compute lives in ``lib/libbca_gb300.so`` (C ABI declared in ``include/bca.h``);
 this package is its thin Python binding plus the seeded workload generator.
 """
-from .api import (check_status, new_status, prefill, prefill_piecewise,  # noqa: F401
+from .api import (PagePool, check_status, new_status, pool_copy_rows,  # noqa: F401
+                  prefix_cache_append_paged, prefix_decode_paged, prefill, prefill_piecewise,
                   prefill_piecewise_workspace_bytes, prefill_workspace_bytes,
                   prefix_cache_append, prefix_cache_append_fp8, prefix_decode, prefix_decode_fp8,
                   prefix_decode_fp8_workspace_bytes, prefix_cache_dequant_fp8,
@@ -14,4 +15,5 @@ __all__ = ["prefill", "prefix_decode", "prefix_decode_fp8", "prefix_decode_fp8_w
            "prefix_cache_dequant_fp8", "prefix_cache_append", "prefix_cache_append_fp8", "schedule_prep",
            "prefill_workspace_bytes", "new_status", "read_status", "check_status",
            "rope_positions", "rope_table", "qk_norm_rope_append", "prefill_piecewise",
-           "prefill_piecewise_workspace_bytes"]
+           "prefill_piecewise_workspace_bytes", "PagePool", "prefix_cache_append_paged",
+           "prefix_decode_paged", "pool_copy_rows"]

@@ -41,6 +41,22 @@ SIGNATURES = {
     "bca_prefill_piecewise_workspace_bytes": (c_size, [c_vp, c_vp, c_i32, c_i32]),
     "bca_prefill_piecewise": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32,
                                       c_i32, c_f32, c_vp, c_vp, c_vp, c_size, c_vp, c_vp]),
+    "bca_prefix_cache_append_paged": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32,
+                                              c_i32, c_i32, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp,
+                                              c_vp]),
+    "bca_prefix_decode_paged": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32,
+                                        c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                        c_f32, c_vp, c_vp, c_vp, c_vp]),
+    "bca_pool_copy_rows": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
+                                   c_vp]),
+    "bca_pool_create": (c_vp, [c_i32]),
+    "bca_pool_destroy": (None, [c_vp]),
+    "bca_pool_alloc": (c_i32, [c_vp, c_i32, c_vp]),
+    "bca_pool_match": (c_i32, [c_vp, c_vp, c_i32, c_vp]),
+    "bca_pool_publish": (c_i32, [c_vp, c_i32, ctypes.c_uint64]),
+    "bca_pool_release": (c_i32, [c_vp, c_vp, c_i32]),
+    "bca_pool_stats": (None, [c_vp, c_vp, c_vp, c_vp]),
+    "bca_pool_refs": (c_i32, [c_vp, c_i32]),
     "bca_rope_positions": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp]),
     "bca_rope_table": (c_i32, [c_vp, c_i32, c_vp, c_vp]),
     "bca_qk_norm_rope_append": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,

@@ -7,6 +7,7 @@ runs in the library's kernels; there is no CPU or PyTorch fallback.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 
 import numpy as np
@@ -389,3 +390,119 @@ def prefill_piecewise(q, k, v, block_id, block_id_host, cu_seqlens_host,
         workspace.numel(), _ptr(status), _stream(stream))
     _native.check(code, "bca_prefill_piecewise")
     return out, lse
+
+
+# ---- paged prefix cache ---------------------------------------------------------------
+
+PAGE_TOKENS = 128
+
+
+class PagePool:
+    """Host-side page pool (``bca_pool_*``): page ids with references, a hash index
+    of published full pages, and reuse of idle cached pages.  The K/V data live in
+    cache tensors ``[L, H, num_pages * 128, 128]``."""
+
+    def __init__(self, num_pages: int):
+        self._lib = _native.load()
+        self.num_pages = num_pages
+        self._h = self._lib.bca_pool_create(num_pages)
+        if not self._h:
+            raise ValueError("num_pages must be positive")
+
+    def __del__(self):
+        h, self._h = getattr(self, "_h", None), None
+        if h:
+            self._lib.bca_pool_destroy(h)
+
+    def alloc(self, n: int) -> np.ndarray:
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        _native.check(self._lib.bca_pool_alloc(self._h, n, out.ctypes.data), "bca_pool_alloc")
+        return out[:n]
+
+    def match(self, hashes) -> np.ndarray:
+        hs = np.ascontiguousarray(np.asarray(hashes, dtype=np.uint64))
+        out = np.zeros(max(len(hs), 1), dtype=np.int32)
+        n = self._lib.bca_pool_match(self._h, hs.ctypes.data, len(hs), out.ctypes.data)
+        return out[:n]
+
+    def publish(self, page: int, h: int) -> None:
+        _native.check(self._lib.bca_pool_publish(self._h, int(page), int(h)), "bca_pool_publish")
+
+    def release(self, pages) -> None:
+        p = np.ascontiguousarray(np.asarray(pages, dtype=np.int32))
+        _native.check(self._lib.bca_pool_release(self._h, p.ctypes.data, len(p)),
+                      "bca_pool_release")
+
+    def stats(self) -> Tuple[int, int, int]:
+        """(free pages, idle cached pages, referenced pages)."""
+        a, b, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+        self._lib.bca_pool_stats(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c))
+        return a.value, b.value, c.value
+
+    def refs(self, page: int) -> int:
+        return int(self._lib.bca_pool_refs(self._h, int(page)))
+
+
+def _paged_shapes(cache_k, cache_v, page_table):
+    _need(cache_k, "cache_k", torch.bfloat16, 4)
+    _need(cache_v, "cache_v", torch.bfloat16, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    L, H, cap, D = cache_k.shape
+    if cache_v.shape != cache_k.shape or cap % PAGE_TOKENS:
+        raise ValueError("paged cache must be [L, H, num_pages * 128, 128]")
+    return L, H, cap // PAGE_TOKENS, D
+
+
+def prefix_cache_append_paged(k, v, cu_seqlens_k, cu_prefix, page_table, cache_k, cache_v,
+                              layer: int, status=None, stream=None) -> None:
+    """``prefix_cache_append`` into a paged cache through ``page_table [batch, max_pages]``."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _need(cu_prefix, "cu_prefix", torch.int32, 1)
+    L, H, n_pages, D = _paged_shapes(cache_k, cache_v, page_table)
+    total_k = k.shape[0]
+    batch = cu_seqlens_k.numel() - 1
+    code = _native.load().bca_prefix_cache_append_paged(
+        _ptr(k), _ptr(v), _ptr(cu_seqlens_k), _ptr(cu_prefix), _ptr(page_table),
+        page_table.shape[1], batch, H, D, total_k, _ptr(cache_k), _ptr(cache_v), layer, L,
+        n_pages, _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefix_cache_append_paged")
+
+
+def prefix_decode_paged(q_tgt, cache_k, cache_v, layer: int, cu_prefix, page_table, k_tgt, v_tgt,
+                        cu_seqlens_q, max_seqlen_q: int, max_prefix: int,
+                        softmax_scale: Optional[float] = None, out=None, lse=None, status=None,
+                        stream=None):
+    """``prefix_decode`` with the prefix read through ``page_table``."""
+    for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
+        _need(t, name, torch.bfloat16, 3)
+    _need(cu_prefix, "cu_prefix", torch.int32, 1)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    L, H, n_pages, D = _paged_shapes(cache_k, cache_v, page_table)
+    total_q = q_tgt.shape[0]
+    batch = cu_seqlens_q.numel() - 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q_tgt)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
+    code = _native.load().bca_prefix_decode_paged(
+        _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), layer, L, n_pages, _ptr(cu_prefix),
+        _ptr(page_table), page_table.shape[1], _ptr(k_tgt), _ptr(v_tgt), _ptr(cu_seqlens_q),
+        batch, H, D, total_q, max_seqlen_q, max_prefix, float(softmax_scale), _ptr(out),
+        _ptr(lse), _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefix_decode_paged")
+    return out, lse
+
+
+def pool_copy_rows(cache_k, cache_v, layer: int, src_page: int, dst_page: int, n_rows: int,
+                   stream=None) -> None:
+    """Copy rows ``[0, n_rows)`` of one page to another (all heads, K and V, one layer)."""
+    _need(cache_k, "cache_k", torch.bfloat16, 4)
+    L, H, cap, D = cache_k.shape
+    code = _native.load().bca_pool_copy_rows(_ptr(cache_k), _ptr(cache_v), layer, L, H,
+                                             cap // PAGE_TOKENS, src_page, dst_page, n_rows,
+                                             _stream(stream))
+    _native.check(code, "bca_pool_copy_rows")

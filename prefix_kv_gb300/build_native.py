@@ -23,7 +23,7 @@ ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-I" + INCLUDE]
 UNITS = ["attn_fwd.cu", "sched_prep.cu", "cache_append.cu", "bca_api.cu", "prefill_noalloc.cu", "selftest.cu",
-         "qk_prologue.cu", "prefill_piecewise.cu"]
+         "qk_prologue.cu", "prefill_piecewise.cu", "page_pool.cpp"]
 
 
 def _nvcc() -> str:
@@ -54,11 +54,11 @@ def build(force: bool = False, verbose: bool = False) -> str:
     nvcc = _nvcc()
 
     def compile_one(unit):
-        obj = os.path.join(BUILD, unit.replace(".cu", ".o"))
+        obj = os.path.join(BUILD, os.path.splitext(unit)[0] + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, "-c", os.path.join(CSRC, unit), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
-        r = subprocess.run(cmd, capture_output=True, text=True)
+        r = subprocess.run(cmd, capture_output=True, text=True, errors="replace")
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for {unit}:\n{r.stderr}")
         if verbose and r.stderr:
@@ -69,7 +69,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         objs = list(ex.map(compile_one, UNITS))
     tmp = LIB + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
-    r = subprocess.run(cmd, capture_output=True, text=True)
+    r = subprocess.run(cmd, capture_output=True, text=True, errors="replace")
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
     os.replace(tmp, LIB)

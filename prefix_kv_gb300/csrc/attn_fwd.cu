@@ -88,6 +88,8 @@ struct FwdParams {
   const int32_t* row_end;
   const PrefillTile* tiles;
   const int32_t* cu_prefix;
+  const int32_t* page_table;  // decode, paged cache: page of prefix tile j of sequence b
+  int max_pages;              //   at page_table[b * max_pages + j]; null: contiguous
   int decode_pairs_per_seq;   // decode: tile pairs per sequence (grid decoding)
   int decode_split_from;      // decode: first item split into single-tile items
   __nv_bfloat16* out;
@@ -183,12 +185,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     pre0 = p.cu_prefix[b];
     const int pre1 = p.cu_prefix[b + 1];
     n_pre = pre1 - pre0;
-    if (n_pre < 0 || pre0 < 0 || static_cast<int64_t>(pre1) > p.capacity) {
+    n_pre_tiles = (n_pre + kBlockN - 1) / kBlockN;
+    // contiguous: cache tokens [pre0, pre1) must lie in the cache; paged: every
+    // page of the prefix must lie in the pool (capacity = pages * 128)
+    bool bad = n_pre < 0;
+    if (p.page_table == nullptr) {
+      bad = bad || pre0 < 0 || static_cast<int64_t>(pre1) > p.capacity;
+    } else if (!bad) {
+      const int64_t n_pages = p.capacity / kBlockN;
+      for (int j = threadIdx.x; j < n_pre_tiles; j += blockDim.x) {
+        if (j >= p.max_pages) {
+          bad = true;
+          break;
+        }
+        const int pg = p.page_table[static_cast<int64_t>(b) * p.max_pages + j];
+        if (pg < 0 || pg >= n_pages) bad = true;
+      }
+    }
+    if (__syncthreads_or(bad)) {
       if (threadIdx.x == 0 && h == 0 && m_base == 0)
         report_status(p.status, n_pre < 0 ? BCA_ERR_SEQLENS : BCA_ERR_CAPACITY);
       return;
     }
-    n_pre_tiles = (n_pre + kBlockN - 1) / kBlockN;
     const int n_all = n_pre_tiles + (q_len + kBlockN - 1) / kBlockN;
     for (int i = 0; i < 2; ++i) nkt[i] = rows_valid[i] > 0 ? n_all : 0;
   }
@@ -284,7 +302,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
         } else if (j < n_pre_tiles) {
           const CUtensorMap* m = is_v ? &tm_v : &tm_k;
-          const int tok = pre0 + j * kBlockN;
+          const int tok = p.page_table != nullptr
+                              ? p.page_table[static_cast<int64_t>(b) * p.max_pages + j] * kBlockN
+                              : pre0 + j * kBlockN;
           tma_load_3d(m, &sm.kv_full[s], dst, 0, tok, h);
           tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, tok, h);
         } else {
@@ -640,6 +660,8 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   p.row_end = a.row_end;
   p.tiles = a.tiles;
   p.cu_prefix = a.cu_prefix;
+  p.page_table = a.page_table;
+  p.max_pages = a.max_pages;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.status = a.status;

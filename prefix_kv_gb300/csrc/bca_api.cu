@@ -44,8 +44,11 @@ bca_status decode_layer(const void* q_tgt, const void* k_layer, const void* v_la
                         const void* v_tgt, const int32_t* cu_seqlens_q, int32_t batch,
                         int32_t num_heads, int32_t total_q, int32_t max_seqlen_q,
                         float softmax_scale, void* out, float* lse, int32_t* status_dev,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, const int32_t* page_table = nullptr,
+                        int max_pages = 0) {
   AttnLaunch a{};
+  a.page_table = page_table;
+  a.max_pages = max_pages;
   a.q = q_tgt;
   // An empty cache (capacity 0) is never read, since every prefix must then be
   // empty; its tensor maps are pointed at q_tgt only to keep them valid.
@@ -218,6 +221,30 @@ bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void*
                       static_cast<cudaStream_t>(stream));
 }
 
+bca_status bca_prefix_decode_paged(const void* q_tgt, const void* cache_k, const void* cache_v,
+                                   int32_t layer, int32_t num_layers, int32_t num_pages,
+                                   const int32_t* cu_prefix, const int32_t* page_table,
+                                   int32_t max_pages, const void* k_tgt, const void* v_tgt,
+                                   const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
+                                   int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
+                                   int32_t max_prefix, float softmax_scale, void* out, float* lse,
+                                   int32_t* status_dev, void* stream) {
+  if (num_pages <= 0 || num_pages > (1 << 24) || max_pages < 0) return BCA_ERR_INVALID_ARG;
+  const int64_t capacity = static_cast<int64_t>(num_pages) * kBlockN;
+  bca_status st = check_decode_args(q_tgt, cache_k, cache_v, layer, num_layers, capacity,
+                                    cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads,
+                                    head_dim, total_q, max_seqlen_q, max_prefix, softmax_scale,
+                                    out, lse);
+  if (st != BCA_OK || batch == 0 || total_q == 0) return st;
+  if (!page_table) return BCA_ERR_INVALID_ARG;
+  const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
+  return decode_layer(q_tgt, static_cast<const __nv_bfloat16*>(cache_k) + layer * layer_elems,
+                      static_cast<const __nv_bfloat16*>(cache_v) + layer * layer_elems, capacity,
+                      cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads, total_q,
+                      max_seqlen_q, softmax_scale, out, lse, status_dev,
+                      static_cast<cudaStream_t>(stream), page_table, max_pages);
+}
+
 size_t bca_prefix_decode_fp8_workspace_bytes(int32_t mode, int32_t num_heads, int32_t head_dim,
                                              int64_t capacity) {
   if ((mode != BCA_FP8_V && mode != BCA_FP8_KV) || head_dim != kHeadDim || num_heads <= 0 ||
@@ -312,8 +339,53 @@ bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* 
   cudaError_t e = launch_cache_append(
       k, v, cu_seqlens_k, cu_prefix, batch, num_heads,
       static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems,
-      static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, capacity, status_dev,
-      static_cast<cudaStream_t>(stream));
+      static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, capacity, nullptr, 0,
+      status_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
+bca_status bca_prefix_cache_append_paged(const void* k, const void* v,
+                                         const int32_t* cu_seqlens_k, const int32_t* cu_prefix,
+                                         const int32_t* page_table, int32_t max_pages,
+                                         int32_t batch, int32_t num_heads, int32_t head_dim,
+                                         int32_t total_k, void* cache_k, void* cache_v,
+                                         int32_t layer, int32_t num_layers, int32_t num_pages,
+                                         int32_t* status_dev, void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads <= 0 || total_k < 0 || num_pages <= 0 || max_pages < 0 ||
+      layer < 0 || num_layers <= 0 || layer >= num_layers || num_pages > (1 << 24))
+    return BCA_ERR_INVALID_ARG;
+  if (batch == 0) return BCA_OK;
+  if (!k || !v || !cu_seqlens_k || !cu_prefix || !page_table || !cache_k || !cache_v)
+    return BCA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(cache_k) || !aligned16(cache_v))
+    return BCA_ERR_INVALID_ARG;
+  const int64_t capacity = static_cast<int64_t>(num_pages) * kBlockN;
+  const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
+  cudaError_t e = launch_cache_append(
+      k, v, cu_seqlens_k, cu_prefix, batch, num_heads,
+      static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems,
+      static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, capacity, page_table,
+      max_pages, status_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
+bca_status bca_pool_copy_rows(void* cache_k, void* cache_v, int32_t layer, int32_t num_layers,
+                              int32_t num_heads, int32_t num_pages, int32_t src_page,
+                              int32_t dst_page, int32_t n_rows, void* stream) {
+  if (!cache_k || !cache_v || layer < 0 || num_layers <= 0 || layer >= num_layers ||
+      num_heads <= 0 || num_pages <= 0 || num_pages > (1 << 24) || src_page < 0 ||
+      src_page >= num_pages || dst_page < 0 || dst_page >= num_pages || n_rows < 0 ||
+      n_rows > kBlockN)
+    return BCA_ERR_INVALID_ARG;
+  if (!aligned16(cache_k) || !aligned16(cache_v)) return BCA_ERR_INVALID_ARG;
+  if (n_rows == 0 || src_page == dst_page) return BCA_OK;
+  const int64_t capacity = static_cast<int64_t>(num_pages) * kBlockN;
+  const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
+  const cudaError_t e = launch_cache_copy_rows(
+      static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems,
+      static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, num_heads, capacity, src_page,
+      dst_page, n_rows, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
 }
 

@@ -22,11 +22,37 @@ constexpr int kAppendThreads = 256;
 constexpr int kMaxBatchSmem = 1024;
 constexpr int kUnroll = 4;
 
+// Cache token of prefix token t of sequence b: contiguous (cu_prefix[b] + t) or,
+// with a page table, page_table[b][t / 128] * 128 + t % 128.
+__device__ __forceinline__ int64_t cache_token(const int32_t* __restrict__ page_table,
+                                               int max_pages, const int32_t* cp, int b, int t) {
+  if (page_table == nullptr) return static_cast<int64_t>(cp[b]) + t;
+  return static_cast<int64_t>(page_table[static_cast<int64_t>(b) * max_pages + (t >> 7)]) * 128 +
+         (t & 127);
+}
+
+// Every page entry a prefix needs lies in [0, capacity / 128) (paged caches).
+__device__ int check_pages(const int32_t* __restrict__ page_table, int max_pages,
+                           const int32_t* cp, int batch, int64_t capacity) {
+  int bad = 0;
+  const int64_t n_pages = capacity / 128;
+  for (int b = 0; b < batch; ++b) {
+    const int n = (cp[b + 1] - cp[b] + 127) / 128;
+    if (n > max_pages) bad = BCA_ERR_CAPACITY;
+    for (int j = threadIdx.x; j < n && j < max_pages; j += blockDim.x) {
+      const int pg = page_table[static_cast<int64_t>(b) * max_pages + j];
+      if (pg < 0 || pg >= n_pages) bad = BCA_ERR_CAPACITY;
+    }
+  }
+  return bad;
+}
+
 __global__ void __launch_bounds__(kAppendThreads)
     cache_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                         const int32_t* __restrict__ cu_k, const int32_t* __restrict__ cu_prefix,
                         int batch, int num_heads, uint4* __restrict__ ck, uint4* __restrict__ cv,
-                        int64_t capacity, int32_t* status) {
+                        int64_t capacity, const int32_t* __restrict__ page_table, int max_pages,
+                        int32_t* status) {
   __shared__ int s_cp[kMaxBatchSmem + 1];
   __shared__ int s_ck[kMaxBatchSmem + 1];
   __shared__ int s_bad;
@@ -49,7 +75,11 @@ __global__ void __launch_bounds__(kAppendThreads)
     const int kl = ckk[i + 1] - ckk[i];
     if (pl < 0 || pl > kl || cp[i] < 0) s_bad = BCA_ERR_SEQLENS;
   }
-  if (threadIdx.x == 0 && static_cast<int64_t>(cp[batch]) > capacity) s_bad = BCA_ERR_CAPACITY;
+  if (page_table == nullptr) {
+    if (threadIdx.x == 0 && static_cast<int64_t>(cp[batch]) > capacity) s_bad = BCA_ERR_CAPACITY;
+  } else if (check_pages(page_table, max_pages, cp, batch, capacity) != 0) {
+    s_bad = BCA_ERR_CAPACITY;
+  }
   __syncthreads();
   if (s_bad != 0) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report_status(status, s_bad);
@@ -80,7 +110,8 @@ __global__ void __launch_bounds__(kAppendThreads)
         }
         const int64_t src_tok = static_cast<int64_t>(ckk[lo]) + (c - cp[lo]);
         const int64_t src = (src_tok * num_heads + hh) * 16 + x;
-        dst[u] = (static_cast<int64_t>(hh) * capacity + c) * 16 + x;
+        const int64_t ctok = cache_token(page_table, max_pages, cp, lo, c - cp[lo]);
+        dst[u] = (static_cast<int64_t>(hh) * capacity + ctok) * 16 + x;
         rk[u] = __ldcs(k + src);
         rv[u] = __ldcs(v + src);
       }
@@ -100,7 +131,8 @@ __global__ void __launch_bounds__(kAppendThreads)
 cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_k,
                                 const int32_t* cu_prefix, int batch, int num_heads,
                                 void* cache_k_layer, void* cache_v_layer, int64_t capacity,
-                                int32_t* status, cudaStream_t stream) {
+                                const int32_t* page_table, int max_pages, int32_t* status,
+                                cudaStream_t stream) {
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -108,7 +140,42 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_
   cache_append_kernel<<<grid, kAppendThreads, 0, stream>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
       num_heads, static_cast<uint4*>(cache_k_layer), static_cast<uint4*>(cache_v_layer), capacity,
-      status);
+      page_table, max_pages, status);
+  return cudaGetLastError();
+}
+
+namespace {
+
+// Rows [0, n_rows) of page src copied to page dst, every head, K and V.
+__global__ void __launch_bounds__(256)
+    cache_copy_rows_kernel(uint4* __restrict__ ck, uint4* __restrict__ cv, int num_heads,
+                           int64_t capacity, int src_page, int dst_page, int n_rows) {
+  const int64_t n = static_cast<int64_t>(num_heads) * n_rows * 16;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int x = static_cast<int>(i & 15);
+    const int64_t rh = i >> 4;
+    const int r = static_cast<int>(rh % n_rows);
+    const int hh = static_cast<int>(rh / n_rows);
+    const int64_t base = static_cast<int64_t>(hh) * capacity;
+    const int64_t s = (base + static_cast<int64_t>(src_page) * 128 + r) * 16 + x;
+    const int64_t d = (base + static_cast<int64_t>(dst_page) * 128 + r) * 16 + x;
+    ck[d] = ck[s];
+    cv[d] = cv[s];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_copy_rows(void* cache_k_layer, void* cache_v_layer, int num_heads,
+                                   int64_t capacity, int src_page, int dst_page, int n_rows,
+                                   cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(num_heads) * n_rows * 16;
+  const int blocks = static_cast<int>((n + 255) / 256 < 1216 ? (n + 255) / 256 : 1216);
+  if (blocks == 0) return cudaSuccess;
+  cache_copy_rows_kernel<<<blocks, 256, 0, stream>>>(static_cast<uint4*>(cache_k_layer),
+                                                     static_cast<uint4*>(cache_v_layer), num_heads,
+                                                     capacity, src_page, dst_page, n_rows);
   return cudaGetLastError();
 }
 

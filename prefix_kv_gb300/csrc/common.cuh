@@ -50,6 +50,8 @@ struct AttnLaunch {
   const int32_t* row_end;
   const PrefillTile* tiles;
   const int32_t* cu_prefix;
+  const int32_t* page_table;   // decode over a paged cache: [batch][max_pages], else null
+  int max_pages;
   int32_t* status;
 };
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream);  // returns bca_status

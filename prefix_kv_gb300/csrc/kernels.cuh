@@ -6,10 +6,16 @@
 
 namespace bca {
 
+// page_table (device int32 [batch][max_pages]) or null for the contiguous cache
 cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_k,
                                 const int32_t* cu_prefix, int batch, int num_heads,
                                 void* cache_k_layer, void* cache_v_layer, int64_t capacity,
-                                int32_t* status, cudaStream_t stream);
+                                const int32_t* page_table, int max_pages, int32_t* status,
+                                cudaStream_t stream);
+// Rows [0, n_rows) of page src_page copied to page dst_page (every head, K and V).
+cudaError_t launch_cache_copy_rows(void* cache_k_layer, void* cache_v_layer, int num_heads,
+                                   int64_t capacity, int src_page, int dst_page, int n_rows,
+                                   cudaStream_t stream);
 
 cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t* cu_k,
                                     const int32_t* cu_prefix, int batch, int num_heads,
