@@ -146,7 +146,8 @@ class ClockSampler:
 class Problem:
     """The workload's tensors, resident on the device (plus pinned host copies for e2e)."""
 
-    def __init__(self, dev, with_host=True, cache="bf16", prologue=False, piecewise=False):
+    def __init__(self, dev, with_host=True, cache="bf16", prologue=False, piecewise=False,
+                 paged=False):
         from prefix_kv_gb300 import flops
         from prefix_kv_gb300 import workloads as W
         wl = W.by_name(WORKLOAD)
@@ -207,6 +208,18 @@ class Problem:
         # optional Q/K prologue (RMS norm + three-axis RoPE; the prefill-side call also
         # appends): coordinates and rotation table once per layout, outside the step
         self.prologue = prologue
+        # paged cache: the prefix's 128-token pages in a shuffled order of a larger pool
+        self.paged = paged
+        if paged:
+            if self.fp8_mode is not None or prologue:
+                raise SystemExit("--paged combines with the bf16 cache and no prologue")
+            n_pages = (self.P + 127) // 128
+            pool_pages = n_pages + n_pages // 2
+            perm = np.random.default_rng(11).permutation(pool_pages)[:n_pages]
+            self.page_table = torch.from_numpy(perm.astype(np.int32)[None, :]).to(dev)
+            self.cache_k = torch.empty((1, self.H, pool_pages * 128, 128), dtype=torch.bfloat16,
+                                       device=dev)
+            self.cache_v = torch.empty_like(self.cache_k)
         # the piecewise baseline: one prefill call per segment (two kernels + a copy each)
         self.piecewise = piecewise
         if piecewise:
@@ -259,7 +272,10 @@ class Problem:
                         status=self.status)
         if events:
             events[1].record()
-        if self.fp8_mode is None:
+        if self.paged:
+            bca.prefix_cache_append_paged(d["k"], d["v"], d["cu"], d["cu_pre"], self.page_table,
+                                          self.cache_k, self.cache_v, 0, status=self.status)
+        elif self.fp8_mode is None:
             bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], self.cache_k,
                                     self.cache_v, 0, status=self.status)
         else:
@@ -268,7 +284,12 @@ class Problem:
                                         mode=self.fp8_mode, status=self.status)
         if events:
             events[2].record()
-        if self.fp8_mode is None:
+        if self.paged:
+            bca.prefix_decode_paged(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"],
+                                    self.page_table, d["k_tgt"], d["v_tgt"], d["cu_tgt"], self.N,
+                                    self.P, self.scale, out=self.dout, lse=self.dlse,
+                                    status=self.status)
+        elif self.fp8_mode is None:
             bca.prefix_decode(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"], d["k_tgt"],
                               d["v_tgt"], d["cu_tgt"], self.N, self.P, self.scale, out=self.dout,
                               lse=self.dlse, status=self.status)
@@ -396,6 +417,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--paged", action="store_true",
+                    help="prefix cache in 128-token pages of a shuffled page table")
     ap.add_argument("--piecewise", action="store_true",
                     help="baseline: prefill as one attention call per segment")
     ap.add_argument("--prologue", action="store_true",
@@ -429,7 +452,7 @@ def main():
 
     import prefix_kv_gb300 as bca
     prob = Problem(dev, with_host=not args.no_e2e, cache=args.cache, prologue=args.prologue,
-                   piecewise=args.piecewise)
+                   piecewise=args.piecewise, paged=args.paged)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -556,6 +579,8 @@ def main():
                            else ("piecewise prefill (schedule prep + attention + lse copy per "
                                  "segment) + cache append + prefix decode") if prob.piecewise
                            else "schedule prep + prefill + cache append + prefix decode",
+                   "prefix_cache_pages": ("128-token pages, shuffled page table" if prob.paged
+                                          else "contiguous"),
                    "prefix_cache": {"bf16": "bf16", "fp8-v": "V in FP8 E4M3 (per token-head "
                                     "fp32 scale), K bf16", "fp8-kv": "K and V in FP8 E4M3 "
                                     "(per token-head fp32 scales)"}[args.cache],
