@@ -32,18 +32,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
-// A waiting thread may be suspended up to this long per try (it resumes as
-// soon as the phase completes), so waiting warps do not spin on issue slots.
-constexpr uint32_t kTryWaitSuspendNs = 20000;
+// try_wait without a time hint: the hardware suspends the thread for its own
+// default interval per try.  A 20 us hint measured 1.8% slower on the
+// two-reference edit prefill (its waiters woke later), so none is given.
 
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kTryWaitSuspendNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
