@@ -141,6 +141,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------------------------- ranks
+
+def max_over_ranks(total_ms: float, seg_ms, dist, device):
+    """The slowest rank's total and per-segment times (every rank gets them);
+    unchanged when there is no process group."""
+    if dist is None:
+        return total_ms, list(seg_ms)
+    t = torch.tensor([total_ms] + list(seg_ms), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t[0].item(), t[1:].tolist()
+
+
+def whole_job_tflops(world: int, steps: int, step_flops: float, total_ms: float) -> float:
+    """Weak scaling: every rank runs its own step, so the job does world x steps
+    steps in the slowest rank's time."""
+    return world * steps * step_flops / (total_ms * 1e-3) / 1e12
+
+
 # ----------------------------------------------------------------------------- inputs
 
 class Problem:
@@ -482,15 +500,12 @@ def main():
 
     seg_ms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(nseg)]
     tot_ms = sum(e[0].elapsed_time(e[nseg]) for e in evs)
-    if dist is not None:
-        t = torch.tensor([tot_ms] + seg_ms, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        tot_ms, seg_ms = t[0].item(), t[1:].tolist()
+    tot_ms, seg_ms = max_over_ranks(tot_ms, seg_ms, dist, dev)
     seg = dict(zip(prob.segments, seg_ms))
     s_pre, s_dec = seg["prefill"], seg["decode"]
     K = args.steps
     step_flops = prob.flops_prefill + prob.flops_decode
-    value = world * K * step_flops / (tot_ms * 1e-3) / 1e12
+    value = whole_job_tflops(world, K, step_flops, tot_ms)
     pre_tf = prob.flops_prefill / (s_pre / K * 1e-3) / 1e12
     dec_tf = prob.flops_decode / (s_dec / K * 1e-3) / 1e12
     if prob.prologue:
@@ -538,12 +553,8 @@ def main():
             e2e_step()
         ev1.record()
         torch.cuda.synchronize()
-        e_ms = ev0.elapsed_time(ev1)
-        if dist is not None:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = t.item()
-        e2e = {"value": round(world * n_e2e * step_flops / (e_ms * 1e-3) / 1e12, 2),
+        e_ms, _ = max_over_ranks(ev0.elapsed_time(ev1), [], dist, dev)
+        e2e = {"value": round(whole_job_tflops(world, n_e2e, step_flops, e_ms), 2),
                "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_ms / n_e2e, 4), "steps": n_e2e}
 
