@@ -357,6 +357,39 @@ bca_status bca_prefix_decode_paged(const void* q_tgt, const void* cache_k, const
                                    int32_t max_prefix, float softmax_scale, void* out, float* lse,
                                    int32_t* status_dev, void* stream);
 
+/* bca_prefix_cache_append_fp8 into a paged cache: codes and scales of prefix
+ * token t of sequence b go to page token page_table[b * max_pages + t / 128] *
+ * 128 + t % 128 of layer `layer` (codes [L][H][num_pages*128][128], scales
+ * [L][H][num_pages*128]; in BCA_FP8_V mode cache_k is the bf16 paged cache). */
+bca_status bca_prefix_cache_append_fp8_paged(
+    const void* k, const void* v, const int32_t* cu_seqlens_k, const int32_t* cu_prefix,
+    const int32_t* page_table, int32_t max_pages, int32_t batch, int32_t num_heads,
+    int32_t head_dim, int32_t total_k, int32_t mode, void* cache_k, void* cache_v,
+    float* scale_k, float* scale_v, int32_t layer, int32_t num_layers, int32_t num_pages,
+    int32_t* status_dev, void* stream);
+
+/* Workspace bytes of bca_prefix_decode_fp8_paged: two bf16 buffers
+ * [H][prefix_rows][128] (256-byte rounded); 0 for invalid arguments. */
+size_t bca_prefix_decode_fp8_paged_workspace_bytes(int32_t num_heads, int32_t head_dim,
+                                                   int64_t prefix_rows);
+
+/* Prefix decode over a paged FP8 cache.  The prefixes are first gathered through
+ * the page table into the workspace, packed by cu_prefix (rows
+ * cu_prefix[b] .. cu_prefix[b+1]-1 of [H][prefix_rows][128]): E4M3 tensors are
+ * dequantised to bf16(fp32(value(code)) * scale), a bf16 K (BCA_FP8_V mode) is
+ * copied.  Then the contiguous bf16 decode runs on the gathered rows.
+ * prefix_rows >= cu_prefix[batch] bounds the gathered rows (a larger
+ * cu_prefix[batch] is BCA_ERR_CAPACITY on the status word).  Other arguments
+ * as in bca_prefix_decode_paged and bca_prefix_decode_fp8. */
+bca_status bca_prefix_decode_fp8_paged(
+    const void* q_tgt, const void* cache_k, const void* cache_v, int32_t mode,
+    const float* scale_k, const float* scale_v, int32_t layer, int32_t num_layers,
+    int32_t num_pages, const int32_t* cu_prefix, const int32_t* page_table, int32_t max_pages,
+    int64_t prefix_rows, const void* k_tgt, const void* v_tgt, const int32_t* cu_seqlens_q,
+    int32_t batch, int32_t num_heads, int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
+    int32_t max_prefix, float softmax_scale, void* out, float* lse, void* workspace,
+    size_t workspace_bytes, int32_t* status_dev, void* stream);
+
 /* Copy rows [0, n_rows) (n_rows <= 128) of page src_page to page dst_page, all
  * heads, K and V, of one layer: the copy of a shared tail page's common rows
  * into a page of its own. */

@@ -4,7 +4,8 @@ The compute lives in ``lib/libbca_gb300.so`` (C ABI declared in ``include/bca.h`
 this package is its thin Python binding plus the seeded workload generator.
 """
 from .api import (PagePool, check_status, new_status, pool_copy_rows,  # noqa: F401
-                  prefix_cache_append_paged, prefix_decode_paged, prefill, prefill_piecewise,
+                  prefix_cache_append_fp8_paged, prefix_cache_append_paged,
+                  prefix_decode_fp8_paged, prefix_decode_paged, prefill, prefill_piecewise,
                   prefill_piecewise_workspace_bytes, prefill_workspace_bytes,
                   prefix_cache_append, prefix_cache_append_fp8, prefix_decode, prefix_decode_fp8,
                   prefix_decode_fp8_workspace_bytes, prefix_cache_dequant_fp8,
@@ -16,4 +17,5 @@ __all__ = ["prefill", "prefix_decode", "prefix_decode_fp8", "prefix_decode_fp8_w
            "prefill_workspace_bytes", "new_status", "read_status", "check_status",
            "rope_positions", "rope_table", "qk_norm_rope_append", "prefill_piecewise",
            "prefill_piecewise_workspace_bytes", "PagePool", "prefix_cache_append_paged",
-           "prefix_decode_paged", "pool_copy_rows"]
+           "prefix_decode_paged", "pool_copy_rows", "prefix_cache_append_fp8_paged",
+           "prefix_decode_fp8_paged"]

@@ -47,6 +47,14 @@ SIGNATURES = {
     "bca_prefix_decode_paged": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32,
                                         c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
                                         c_f32, c_vp, c_vp, c_vp, c_vp]),
+    "bca_prefix_cache_append_fp8_paged": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
+                                                  c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp,
+                                                  c_vp, c_i32, c_i32, c_i32, c_vp, c_vp]),
+    "bca_prefix_decode_fp8_paged_workspace_bytes": (c_size, [c_i32, c_i32, c_i64]),
+    "bca_prefix_decode_fp8_paged": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_i32,
+                                            c_i32, c_vp, c_vp, c_i32, c_i64, c_vp, c_vp, c_vp,
+                                            c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_f32, c_vp,
+                                            c_vp, c_vp, c_size, c_vp, c_vp]),
     "bca_pool_copy_rows": (c_i32, [c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
                                    c_vp]),
     "bca_pool_create": (c_vp, [c_i32]),

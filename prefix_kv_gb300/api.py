@@ -506,3 +506,66 @@ def pool_copy_rows(cache_k, cache_v, layer: int, src_page: int, dst_page: int, n
                                              cap // PAGE_TOKENS, src_page, dst_page, n_rows,
                                              _stream(stream))
     _native.check(code, "bca_pool_copy_rows")
+
+
+def prefix_cache_append_fp8_paged(k, v, cu_seqlens_k, cu_prefix, page_table, cache_k, cache_v,
+                                  scale_k, scale_v, layer: int, mode: str = "v", status=None,
+                                  stream=None) -> None:
+    """``prefix_cache_append_fp8`` into a paged cache (``[L, H, num_pages * 128, 128]``
+    codes, ``[L, H, num_pages * 128]`` scales) through ``page_table``."""
+    _need(k, "k", torch.bfloat16, 3)
+    _need(v, "v", torch.bfloat16, 3)
+    _need(page_table, "page_table", torch.int32, 2)
+    m = FP8_MODES[mode]
+    _need(cache_k, "cache_k", torch.uint8 if mode == "kv" else torch.bfloat16, 4)
+    _need(cache_v, "cache_v", torch.uint8, 4)
+    _need(scale_v, "scale_v", torch.float32, 3)
+    if mode == "kv":
+        _need(scale_k, "scale_k", torch.float32, 3)
+    L, H, cap, D = cache_v.shape
+    if cap % PAGE_TOKENS or tuple(cache_k.shape) != tuple(cache_v.shape) or \
+            tuple(scale_v.shape) != (L, H, cap):
+        raise ValueError("paged FP8 cache shapes do not match")
+    batch = cu_seqlens_k.numel() - 1
+    code = _native.load().bca_prefix_cache_append_fp8_paged(
+        _ptr(k), _ptr(v), _ptr(cu_seqlens_k), _ptr(cu_prefix), _ptr(page_table),
+        page_table.shape[1], batch, H, D, k.shape[0], m, _ptr(cache_k), _ptr(cache_v),
+        _ptr(scale_k) if mode == "kv" else None, _ptr(scale_v), layer, L, cap // PAGE_TOKENS,
+        _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefix_cache_append_fp8_paged")
+
+
+def prefix_decode_fp8_paged(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: int, cu_prefix,
+                            page_table, prefix_rows: int, k_tgt, v_tgt, cu_seqlens_q,
+                            max_seqlen_q: int, max_prefix: int,
+                            softmax_scale: Optional[float] = None, mode: str = "v", out=None,
+                            lse=None, workspace=None, status=None, stream=None):
+    """Decode over a paged FP8 cache: gather (+ dequantise) the prefixes into a
+    workspace packed by ``cu_prefix`` (``prefix_rows >= cu_prefix[-1]``), then
+    the contiguous decode."""
+    for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
+        _need(t, name, torch.bfloat16, 3)
+    m = FP8_MODES[mode]
+    _need(cache_v, "cache_v", torch.uint8, 4)
+    _need(page_table, "page_table", torch.int32, 2)
+    L, H, cap, D = cache_v.shape
+    total_q = q_tgt.shape[0]
+    batch = cu_seqlens_q.numel() - 1
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q_tgt)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
+    lib = _native.load()
+    if workspace is None:
+        workspace = torch.empty(lib.bca_prefix_decode_fp8_paged_workspace_bytes(H, D, prefix_rows),
+                                dtype=torch.uint8, device=q_tgt.device)
+    code = lib.bca_prefix_decode_fp8_paged(
+        _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), m, _ptr(scale_k) if mode == "kv" else None,
+        _ptr(scale_v), layer, L, cap // PAGE_TOKENS, _ptr(cu_prefix), _ptr(page_table),
+        page_table.shape[1], prefix_rows, _ptr(k_tgt), _ptr(v_tgt), _ptr(cu_seqlens_q), batch, H,
+        D, total_q, max_seqlen_q, max_prefix, float(softmax_scale), _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+    _native.check(code, "bca_prefix_decode_fp8_paged")
+    return out, lse

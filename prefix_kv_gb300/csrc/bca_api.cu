@@ -101,6 +101,37 @@ size_t bf16_layer_bytes(int32_t num_heads, int64_t capacity) {
   return (b + 255) & ~static_cast<size_t>(255);
 }
 
+// Shared by the contiguous and paged FP8 appends (page_table null: contiguous).
+bca_status append_fp8_impl(const void* k, const void* v, const int32_t* cu_seqlens_k,
+                           const int32_t* cu_prefix, const int32_t* page_table, int max_pages,
+                           int32_t batch, int32_t num_heads, int32_t head_dim, int32_t total_k,
+                           int32_t mode, void* cache_k, void* cache_v, float* scale_k,
+                           float* scale_v, int32_t layer, int32_t num_layers, int64_t capacity,
+                           int32_t* status_dev, void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (mode != BCA_FP8_V && mode != BCA_FP8_KV) return BCA_ERR_INVALID_ARG;
+  if (batch < 0 || num_heads <= 0 || total_k < 0 || capacity < 0 || layer < 0 ||
+      num_layers <= 0 || layer >= num_layers)
+    return BCA_ERR_INVALID_ARG;
+  if (batch == 0) return BCA_OK;
+  if (!k || !v || !cu_seqlens_k || !cu_prefix) return BCA_ERR_INVALID_ARG;
+  const bool quant_k = mode == BCA_FP8_KV;
+  if (capacity > 0 && (!cache_k || !cache_v || !scale_v || (quant_k && !scale_k)))
+    return BCA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(cache_k) || !aligned16(cache_v) ||
+      (reinterpret_cast<uintptr_t>(scale_v) & 3u) || (reinterpret_cast<uintptr_t>(scale_k) & 3u))
+    return BCA_ERR_INVALID_ARG;
+  const size_t rows = static_cast<size_t>(num_heads) * capacity;   // per layer
+  const size_t k_bytes = quant_k ? 1 : 2;
+  cudaError_t e = launch_cache_append_fp8(
+      k, v, cu_seqlens_k, cu_prefix, batch, num_heads, quant_k,
+      static_cast<uint8_t*>(cache_k) + layer * rows * kHeadDim * k_bytes,
+      static_cast<uint8_t*>(cache_v) + layer * rows * kHeadDim,
+      quant_k ? scale_k + layer * rows : nullptr, scale_v + layer * rows, capacity, page_table,
+      max_pages, status_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -395,28 +426,73 @@ bca_status bca_prefix_cache_append_fp8(const void* k, const void* v, const int32
                                        void* cache_k, void* cache_v, float* scale_k,
                                        float* scale_v, int32_t layer, int32_t num_layers,
                                        int64_t capacity, int32_t* status_dev, void* stream) {
-  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  return append_fp8_impl(k, v, cu_seqlens_k, cu_prefix, nullptr, 0, batch, num_heads, head_dim,
+                         total_k, mode, cache_k, cache_v, scale_k, scale_v, layer, num_layers,
+                         capacity, status_dev, stream);
+}
+
+bca_status bca_prefix_cache_append_fp8_paged(
+    const void* k, const void* v, const int32_t* cu_seqlens_k, const int32_t* cu_prefix,
+    const int32_t* page_table, int32_t max_pages, int32_t batch, int32_t num_heads,
+    int32_t head_dim, int32_t total_k, int32_t mode, void* cache_k, void* cache_v,
+    float* scale_k, float* scale_v, int32_t layer, int32_t num_layers, int32_t num_pages,
+    int32_t* status_dev, void* stream) {
+  if (num_pages <= 0 || num_pages > (1 << 24) || max_pages < 0 || !page_table)
+    return BCA_ERR_INVALID_ARG;
+  return append_fp8_impl(k, v, cu_seqlens_k, cu_prefix, page_table, max_pages, batch, num_heads,
+                         head_dim, total_k, mode, cache_k, cache_v, scale_k, scale_v, layer,
+                         num_layers, static_cast<int64_t>(num_pages) * kBlockN, status_dev,
+                         stream);
+}
+
+size_t bca_prefix_decode_fp8_paged_workspace_bytes(int32_t num_heads, int32_t head_dim,
+                                                   int64_t prefix_rows) {
+  if (head_dim != kHeadDim || num_heads <= 0 || prefix_rows < 0) return 0;
+  return 2 * bf16_layer_bytes(num_heads, prefix_rows);
+}
+
+bca_status bca_prefix_decode_fp8_paged(
+    const void* q_tgt, const void* cache_k, const void* cache_v, int32_t mode,
+    const float* scale_k, const float* scale_v, int32_t layer, int32_t num_layers,
+    int32_t num_pages, const int32_t* cu_prefix, const int32_t* page_table, int32_t max_pages,
+    int64_t prefix_rows, const void* k_tgt, const void* v_tgt, const int32_t* cu_seqlens_q,
+    int32_t batch, int32_t num_heads, int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
+    int32_t max_prefix, float softmax_scale, void* out, float* lse, void* workspace,
+    size_t workspace_bytes, int32_t* status_dev, void* stream) {
   if (mode != BCA_FP8_V && mode != BCA_FP8_KV) return BCA_ERR_INVALID_ARG;
-  if (batch < 0 || num_heads <= 0 || total_k < 0 || capacity < 0 || layer < 0 ||
-      num_layers <= 0 || layer >= num_layers)
+  if (num_pages <= 0 || num_pages > (1 << 24) || max_pages < 0 || prefix_rows < 0)
     return BCA_ERR_INVALID_ARG;
-  if (batch == 0) return BCA_OK;
-  if (!k || !v || !cu_seqlens_k || !cu_prefix) return BCA_ERR_INVALID_ARG;
-  const bool quant_k = mode == BCA_FP8_KV;
-  if (capacity > 0 && (!cache_k || !cache_v || !scale_v || (quant_k && !scale_k)))
+  const int64_t capacity = static_cast<int64_t>(num_pages) * kBlockN;
+  bca_status st = check_decode_args(q_tgt, cache_k, cache_v, layer, num_layers, capacity,
+                                    cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads,
+                                    head_dim, total_q, max_seqlen_q, max_prefix, softmax_scale,
+                                    out, lse);
+  if (st != BCA_OK || batch == 0 || total_q == 0) return st;
+  const bool k8 = mode == BCA_FP8_KV;
+  if (!page_table || !scale_v || (k8 && !scale_k)) return BCA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(scale_v) & 3u) || (reinterpret_cast<uintptr_t>(scale_k) & 3u))
     return BCA_ERR_INVALID_ARG;
-  if (!aligned16(k) || !aligned16(v) || !aligned16(cache_k) || !aligned16(cache_v) ||
-      (reinterpret_cast<uintptr_t>(scale_v) & 3u) || (reinterpret_cast<uintptr_t>(scale_k) & 3u))
-    return BCA_ERR_INVALID_ARG;
-  const size_t rows = static_cast<size_t>(num_heads) * capacity;   // per layer
-  const size_t k_bytes = quant_k ? 1 : 2;
-  cudaError_t e = launch_cache_append_fp8(
-      k, v, cu_seqlens_k, cu_prefix, batch, num_heads, quant_k,
-      static_cast<uint8_t*>(cache_k) + layer * rows * kHeadDim * k_bytes,
-      static_cast<uint8_t*>(cache_v) + layer * rows * kHeadDim,
-      quant_k ? scale_k + layer * rows : nullptr, scale_v + layer * rows, capacity, status_dev,
-      static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
+  const size_t need = bca_prefix_decode_fp8_paged_workspace_bytes(num_heads, head_dim,
+                                                                   prefix_rows);
+  if (workspace == nullptr || workspace_bytes < need || !aligned16(workspace))
+    return BCA_ERR_WORKSPACE;
+  auto s = static_cast<cudaStream_t>(stream);
+  const size_t rows = static_cast<size_t>(num_heads) * capacity;   // (head, token) rows per layer
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* k_out = ws;
+  void* v_out = ws + bf16_layer_bytes(num_heads, prefix_rows);
+  const void* k_src = static_cast<const uint8_t*>(cache_k) + layer * rows * kHeadDim * (k8 ? 1 : 2);
+  const void* v_src = static_cast<const uint8_t*>(cache_v) + layer * rows * kHeadDim;
+  if (launch_cache_gather(k8, k_src, k8 ? scale_k + layer * rows : nullptr, cu_prefix,
+                          page_table, max_pages, batch, num_heads, capacity, k_out, prefix_rows,
+                          status_dev, s) != cudaSuccess ||
+      launch_cache_gather(true, v_src, scale_v + layer * rows, cu_prefix, page_table, max_pages,
+                          batch, num_heads, capacity, v_out, prefix_rows, status_dev, s) !=
+          cudaSuccess)
+    return BCA_ERR_CUDA;
+  return decode_layer(q_tgt, k_out, v_out, prefix_rows, cu_prefix, k_tgt, v_tgt, cu_seqlens_q,
+                      batch, num_heads, total_q, max_seqlen_q, softmax_scale, out, lse,
+                      status_dev, s);
 }
 
 bca_status bca_rope_positions(const int32_t* block_id, const int32_t* cu_seqlens, int32_t batch,

@@ -226,6 +226,7 @@ __global__ void __launch_bounds__(256)
                             const int32_t* __restrict__ cu_k, const int32_t* __restrict__ cu_prefix,
                             int batch, int num_heads, void* __restrict__ ck, uint2* __restrict__ cv,
                             float* __restrict__ sk, float* __restrict__ sv, int64_t capacity,
+                            const int32_t* __restrict__ page_table, int max_pages,
                             int32_t* status) {
   __shared__ int s_bad;
   if (threadIdx.x == 0) s_bad = 0;
@@ -235,8 +236,12 @@ __global__ void __launch_bounds__(256)
     const int kl = cu_k[i + 1] - cu_k[i];
     if (pl < 0 || pl > kl || cu_prefix[i] < 0) s_bad = BCA_ERR_SEQLENS;
   }
-  if (threadIdx.x == 0 && static_cast<int64_t>(cu_prefix[batch]) > capacity)
+  if (page_table == nullptr) {
+    if (threadIdx.x == 0 && static_cast<int64_t>(cu_prefix[batch]) > capacity)
+      s_bad = BCA_ERR_CAPACITY;
+  } else if (check_pages(page_table, max_pages, cu_prefix, batch, capacity) != 0) {
     s_bad = BCA_ERR_CAPACITY;
+  }
   __syncthreads();
   if (s_bad != 0) {
     if (blockIdx.x == 0 && threadIdx.x == 0) report_status(status, s_bad);
@@ -261,7 +266,8 @@ __global__ void __launch_bounds__(256)
     }
     const int64_t src_tok = static_cast<int64_t>(cu_k[lo]) + (c - cu_prefix[lo]);
     const int64_t src = (src_tok * num_heads + hh) * 16 + lane16;
-    const int64_t dst_row = static_cast<int64_t>(hh) * capacity + c;
+    const int64_t dst_row = static_cast<int64_t>(hh) * capacity +
+                            cache_token(page_table, max_pages, cu_prefix, lo, c - cu_prefix[lo]);
     float scale_v, scale_k;
     const uint2 qv = quantize8(__ldcs(v + src), &scale_v);
     if (live) {
@@ -287,7 +293,8 @@ cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t*
                                     const int32_t* cu_prefix, int batch, int num_heads,
                                     bool quant_k, void* cache_k_layer, void* cache_v_layer,
                                     float* scale_k_layer, float* scale_v_layer, int64_t capacity,
-                                    int32_t* status, cudaStream_t stream) {
+                                    const int32_t* page_table, int max_pages, int32_t* status,
+                                    cudaStream_t stream) {
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -296,12 +303,12 @@ cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t*
     cache_append_fp8_kernel<true><<<grid, 256, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
         num_heads, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
-        scale_v_layer, capacity, status);
+        scale_v_layer, capacity, page_table, max_pages, status);
   } else {
     cache_append_fp8_kernel<false><<<grid, 256, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
         num_heads, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
-        scale_v_layer, capacity, status);
+        scale_v_layer, capacity, page_table, max_pages, status);
   }
   return cudaGetLastError();
 }
@@ -365,6 +372,98 @@ cudaError_t launch_cache_dequant_fp8(const void* codes_layer, const float* scale
   cache_dequant_fp8_kernel<<<sms * 8, 256, 0, stream>>>(
       static_cast<const uint4*>(codes_layer), scales_layer, cu_prefix, batch, num_heads, capacity,
       static_cast<uint4*>(out_layer), status);
+  return cudaGetLastError();
+}
+
+}  // namespace bca
+
+// ---------------------------------------------------------------------------
+// Gather of a paged cache layer into a packed bf16 buffer (SenseNova-U1 /
+// Prism-Infer notes, prefix KV reuse: a prefix hit gathers and dequantises the
+// paged K/V in one batch).  Prefix token t of sequence b is read from cache
+// token page_table[b][t / 128] * 128 + t % 128 of the [H][capacity][128]
+// layer and written to row cu_prefix[b] + t of out [H][out_rows][128]: E4M3
+// codes (kFp8) become bf16(fp32(value(code)) * scale), bf16 rows are copied.
+namespace bca {
+namespace {
+
+template <bool kFp8>
+__global__ void __launch_bounds__(256)
+    cache_gather_kernel(const void* __restrict__ src, const float* __restrict__ scales,
+                        const int32_t* __restrict__ cu_prefix, const int32_t* __restrict__ page_table,
+                        int max_pages, int batch, int num_heads, int64_t capacity,
+                        uint4* __restrict__ out, int64_t out_rows, int32_t* status) {
+  __shared__ int s_bad;
+  if (threadIdx.x == 0) s_bad = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < batch; i += blockDim.x)
+    if (cu_prefix[i + 1] < cu_prefix[i] || cu_prefix[i] < 0) s_bad = BCA_ERR_SEQLENS;
+  if (threadIdx.x == 0 && static_cast<int64_t>(cu_prefix[batch]) > out_rows)
+    s_bad = BCA_ERR_CAPACITY;
+  if (check_pages(page_table, max_pages, cu_prefix, batch, capacity) != 0) s_bad = BCA_ERR_CAPACITY;
+  __syncthreads();
+  if (s_bad != 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report_status(status, s_bad);
+    return;
+  }
+  const int p0 = cu_prefix[0];
+  const int64_t tokens = cu_prefix[batch] - p0;
+  const int64_t chunks = tokens * num_heads * 8;         // 16-value chunks (32 bf16 bytes out)
+  for (int64_t ch = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; ch < chunks;
+       ch += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row_in = ch >> 3;
+    const int hh = static_cast<int>(row_in / tokens);
+    const int c = static_cast<int>(row_in - hh * tokens) + p0;   // packed prefix row
+    int lo = 0, hi = batch - 1;                                   // its sequence
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu_prefix[mid] <= c) lo = mid; else hi = mid - 1;
+    }
+    const int64_t src_row =
+        static_cast<int64_t>(hh) * capacity + cache_token(page_table, max_pages, cu_prefix, lo,
+                                                          c - cu_prefix[lo]);
+    const int64_t dst_row = static_cast<int64_t>(hh) * out_rows + c;
+    const int x = static_cast<int>(ch & 7);
+    if constexpr (kFp8) {
+      const uint4 raw = __ldcs(static_cast<const uint4*>(src) + src_row * 8 + x);
+      const float sc = __ldg(scales + src_row);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(w[q] >> (16 * hb)));
+          o[2 * q + hb] = pack_bf16x2(f.x * sc, f.y * sc);
+        }
+      }
+      out[dst_row * 16 + 2 * x] = make_uint4(o[0], o[1], o[2], o[3]);
+      out[dst_row * 16 + 2 * x + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+    } else {
+      const uint4* s4 = static_cast<const uint4*>(src);
+      out[dst_row * 16 + 2 * x] = __ldcs(s4 + src_row * 16 + 2 * x);
+      out[dst_row * 16 + 2 * x + 1] = __ldcs(s4 + src_row * 16 + 2 * x + 1);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_cache_gather(bool fp8, const void* src_layer, const float* scales_layer,
+                                const int32_t* cu_prefix, const int32_t* page_table, int max_pages,
+                                int batch, int num_heads, int64_t capacity, void* out,
+                                int64_t out_rows, int32_t* status, cudaStream_t stream) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (fp8)
+    cache_gather_kernel<true><<<sms * 8, 256, 0, stream>>>(
+        src_layer, scales_layer, cu_prefix, page_table, max_pages, batch, num_heads, capacity,
+        static_cast<uint4*>(out), out_rows, status);
+  else
+    cache_gather_kernel<false><<<sms * 8, 256, 0, stream>>>(
+        src_layer, scales_layer, cu_prefix, page_table, max_pages, batch, num_heads, capacity,
+        static_cast<uint4*>(out), out_rows, status);
   return cudaGetLastError();
 }
 

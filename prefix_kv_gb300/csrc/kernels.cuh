@@ -21,7 +21,14 @@ cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t*
                                     const int32_t* cu_prefix, int batch, int num_heads,
                                     bool quant_k, void* cache_k_layer, void* cache_v_layer,
                                     float* scale_k_layer, float* scale_v_layer, int64_t capacity,
-                                    int32_t* status, cudaStream_t stream);
+                                    const int32_t* page_table, int max_pages, int32_t* status,
+                                    cudaStream_t stream);
+// Paged layer rows (E4M3 with scales, or bf16) gathered into packed bf16 rows
+// cu_prefix[b] + t of out [H][out_rows][128].
+cudaError_t launch_cache_gather(bool fp8, const void* src_layer, const float* scales_layer,
+                                const int32_t* cu_prefix, const int32_t* page_table, int max_pages,
+                                int batch, int num_heads, int64_t capacity, void* out,
+                                int64_t out_rows, int32_t* status, cudaStream_t stream);
 
 // E4M3 cache rows cu_prefix[0] .. cu_prefix[batch]-1 of one layer ([H][cap][128]
 // codes, [H][cap] scales) expanded to bf16 value * scale, same layout.

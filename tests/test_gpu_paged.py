@@ -160,3 +160,82 @@ def test_two_requests_share_pages_through_the_pool():
     ref = oracle.prefix_decode(qt, kB, vB, [0, 300], kt, vt, [0, 64], SCALE)
     assert_close(out, lse, *ref, what="shared pages")
     assert pool.refs(pages_a[0]) == 2 and pool.stats()[2] == 4
+
+
+# ---------------------------------------------------------------- FP8 E4M3 pages
+
+from oracle import fp8 as ofp8
+import oracle as _oracle
+
+
+@pytest.mark.parametrize("mode", ["v", "kv"])
+def test_fp8_paged_append_and_decode(mode):
+    H, n_pages = 3, 12
+    pre, tgt = [300, 129, 5], [40, 200, 64]
+    kp, vp, qt, kt, vt, cp, cq = _case(95, pre, tgt, H)
+    pt, _ = _page_table(pre, n_pages, 6)
+    cap = n_pages * 128
+    kdt = torch.uint8 if mode == "kv" else torch.bfloat16
+    fill_k = 0x7F if mode == "kv" else float("nan")
+    ck = torch.full((1, H, cap, 128), fill_k, dtype=kdt, device=DEV)
+    cv = torch.full((1, H, cap, 128), 0x7F, dtype=torch.uint8, device=DEV)
+    sk = torch.full((1, H, cap), float("nan"), dtype=torch.float32, device=DEV)
+    sv = torch.full_like(sk, float("nan"))
+    st = bca.new_status(DEV)
+    bca.prefix_cache_append_fp8_paged(kp.to(DEV), vp.to(DEV), _ti(cp), _ti(cp), _ti(pt), ck, cv,
+                                      sk if mode == "kv" else None, sv, 0, mode=mode, status=st)
+    assert bca.read_status(st) == 0
+    # expected codes / scales: the oracle's quantisation, placed through the page table
+    vc, vs = ofp8.quantize_rows(vp)
+    kc, ks = ofp8.quantize_rows(kp)
+    got_cv, got_sv = cv.cpu().numpy(), sv.cpu().numpy()
+    got_ck, got_sk = ck.cpu(), sk.cpu().numpy()
+    for b in range(len(pre)):
+        for t in range(pre[b]):
+            r, slot = int(cp[b]) + t, pg.page_slot(pt, b, t)
+            assert np.array_equal(got_cv[0, :, slot], vc[r])
+            assert np.array_equal(got_sv[0, :, slot].view(np.uint32), vs[r].view(np.uint32))
+            if mode == "kv":
+                assert np.array_equal(got_ck.numpy()[0, :, slot], kc[r])
+                assert np.array_equal(got_sk[0, :, slot].view(np.uint32), ks[r].view(np.uint32))
+            else:
+                assert torch.equal(got_ck[0, :, slot].view(torch.int16), kp[r].view(torch.int16))
+    rows = int(cp[-1])
+    out, lse = bca.prefix_decode_fp8_paged(qt.to(DEV), ck, cv, sk if mode == "kv" else None, sv,
+                                           0, _ti(cp), _ti(pt), rows, kt.to(DEV), vt.to(DEV),
+                                           _ti(cq), max(tgt), max(pre), SCALE, mode=mode,
+                                           status=st)
+    assert bca.read_status(st) == 0
+    vh = torch.from_numpy(ofp8.dequantize_rows(vc, vs)).to(torch.bfloat16)
+    kh = torch.from_numpy(ofp8.dequantize_rows(kc, ks)).to(torch.bfloat16) if mode == "kv" else kp
+    ref = _oracle.prefix_decode(qt, kh, vh, cp, kt, vt, cq, SCALE)
+    assert_close(out, lse, *ref, what=f"fp8 paged {mode}")
+
+
+def test_fp8_paged_decode_equals_contiguous():
+    H, n_pages, mode = 2, 6, "kv"
+    pre, tgt = [333, 50], [128, 77]
+    kp, vp, qt, kt, vt, cp, cq = _case(96, pre, tgt, H)
+    pt, _ = _page_table(pre, n_pages, 8)
+    d = lambda t: t.to(DEV)
+    # paged
+    ck = torch.zeros((1, H, n_pages * 128, 128), dtype=torch.uint8, device=DEV)
+    cv = torch.zeros_like(ck)
+    sk = torch.zeros((1, H, n_pages * 128), dtype=torch.float32, device=DEV)
+    sv = torch.zeros_like(sk)
+    bca.prefix_cache_append_fp8_paged(d(kp), d(vp), _ti(cp), _ti(cp), _ti(pt), ck, cv, sk, sv, 0,
+                                      mode=mode)
+    out_p, lse_p = bca.prefix_decode_fp8_paged(d(qt), ck, cv, sk, sv, 0, _ti(cp), _ti(pt),
+                                               int(cp[-1]), d(kt), d(vt), _ti(cq), max(tgt),
+                                               max(pre), SCALE, mode=mode)
+    # contiguous
+    cap = int(cp[-1])
+    ck2 = torch.zeros((1, H, cap, 128), dtype=torch.uint8, device=DEV)
+    cv2 = torch.zeros_like(ck2)
+    sk2 = torch.zeros((1, H, cap), dtype=torch.float32, device=DEV)
+    sv2 = torch.zeros_like(sk2)
+    bca.prefix_cache_append_fp8(d(kp), d(vp), _ti(cp), _ti(cp), ck2, cv2, sk2, sv2, 0, mode=mode)
+    out_c, lse_c = bca.prefix_decode_fp8(d(qt), ck2, cv2, sk2, sv2, 0, _ti(cp), d(kt), d(vt),
+                                         _ti(cq), max(tgt), max(pre), SCALE, mode=mode)
+    assert torch.equal(out_p.view(torch.int16), out_c.view(torch.int16))
+    assert torch.equal(lse_p, lse_c)
