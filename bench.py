@@ -165,17 +165,22 @@ class Problem:
     """The workload's tensors, resident on the device (plus pinned host copies for e2e)."""
 
     def __init__(self, dev, with_host=True, cache="bf16", prologue=False, piecewise=False,
-                 paged=False):
+                 paged=False, workload=WORKLOAD):
         from prefix_kv_gb300 import flops
         from prefix_kv_gb300 import workloads as W
-        wl = W.by_name(WORKLOAD)
+        wl = W.by_name(workload)
         self.wl = wl
         q, k, v = W.make_qkv(wl)
         tr = torch.from_numpy(wl.target_rows())
         self.H = wl.num_heads
-        self.S = wl.seq_lens[0]
-        self.N = wl.target_lens()[0]
-        self.P = wl.prefix_lens()[0]
+        # packed totals, per-sequence maxima, and the first sequence (the CPU sample's)
+        self.batch = wl.batch
+        self.decode = wl.decode
+        self.S, self.max_s = wl.total, max(wl.seq_lens)
+        self.N = sum(wl.target_lens()) if wl.decode else 0
+        self.P = sum(wl.prefix_lens()) if wl.decode else 0
+        self.max_n, self.max_p = max(wl.target_lens()), max(wl.prefix_lens())
+        self.S0, self.N0, self.P0 = wl.seq_lens[0], wl.target_lens()[0], wl.prefix_lens()[0]
         self.scale = 1.0 / math.sqrt(128)
         self.host = {
             "q": q, "k": k, "v": v,
@@ -206,12 +211,14 @@ class Problem:
             self.dec_ws = torch.empty(
                 bca.prefix_decode_fp8_workspace_bytes(self.fp8_mode, self.H, self.P),
                 dtype=torch.uint8, device=dev)
-        self.ws = torch.empty(bca.prefill_workspace_bytes(1, self.S, self.S), dtype=torch.uint8,
+        self.ws = torch.empty(bca.prefill_workspace_bytes(self.batch, self.S, self.max_s),
+                              dtype=torch.uint8,
                               device=dev)
         self.status = bca.new_status(dev)
         cu = wl.cu_seqlens()
         self.pairs_prefill = flops.prefill_visible_pairs(wl.block_id(), cu, cu)
-        self.pairs_decode = flops.decode_visible_pairs(wl.cu_target(), wl.cu_prefix())
+        self.pairs_decode = (flops.decode_visible_pairs(wl.cu_target(), wl.cu_prefix())
+                             if wl.decode else 0)
         self.flops_prefill = flops.attention_flops(self.pairs_prefill, self.H)
         self.flops_decode = flops.attention_flops(self.pairs_decode, self.H)
         rows = self.P * self.H
@@ -222,7 +229,8 @@ class Problem:
         else:                                                    # K and V quantised
             self.append_bytes = rows * 2 * (256 + 128 + 4)
         # kernel launches per step: schedule prep, prefill, append, [expansions], decode
-        self.launches = 4 + {None: 0, "v": 1, "kv": 2}[self.fp8_mode]
+        self.launches = (4 + {None: 0, "v": 1, "kv": 2}[self.fp8_mode] if wl.decode
+                         else 2)          # prefill only: schedule prep + attention
         # optional Q/K prologue (RMS norm + three-axis RoPE; the prefill-side call also
         # appends): coordinates and rotation table once per layout, outside the step
         self.prologue = prologue
@@ -231,10 +239,16 @@ class Problem:
         if paged:
             if self.fp8_mode is not None or prologue:
                 raise SystemExit("--paged combines with the bf16 cache and no prologue")
-            n_pages = (self.P + 127) // 128
+            need = [(p_ + 127) // 128 for p_ in wl.prefix_lens()]
+            n_pages = sum(need)
             pool_pages = n_pages + n_pages // 2
-            perm = np.random.default_rng(11).permutation(pool_pages)[:n_pages]
-            self.page_table = torch.from_numpy(perm.astype(np.int32)[None, :]).to(dev)
+            perm = np.random.default_rng(11).permutation(pool_pages)[:n_pages].astype(np.int32)
+            table = np.full((self.batch, max(need)), -1, dtype=np.int32)
+            at = 0
+            for b_, n_ in enumerate(need):
+                table[b_, :n_] = perm[at:at + n_]
+                at += n_
+            self.page_table = torch.from_numpy(table).to(dev)
             self.cache_k = torch.empty((1, self.H, pool_pages * 128, 128), dtype=torch.bfloat16,
                                        device=dev)
             self.cache_v = torch.empty_like(self.cache_k)
@@ -245,11 +259,14 @@ class Problem:
             self.cu_host = wl.cu_seqlens()
             self.pw_ws = torch.empty(bca.prefill_piecewise_workspace_bytes(
                 self.bid_host, self.cu_host, self.H), dtype=torch.uint8, device=dev)
-            n_pieces = int(np.count_nonzero(np.diff(self.bid_host))) + 1
+            n_pieces = sum(int(np.count_nonzero(np.diff(self.bid_host[a:e]))) + 1
+                           for a, e in zip(self.cu_host[:-1], self.cu_host[1:]) if e > a)
             self.launches += 2 * n_pieces - 2
         # named segments of the step, between consecutive CUDA events
         self.segments = (["prologue", "prefill", "target_prologue", "decode"] if prologue
                          else ["prefill", "append", "decode"])
+        if prologue and not self.decode:
+            raise SystemExit("--prologue needs a workload with a decode step")
         if prologue:
             if piecewise:
                 raise SystemExit("--prologue runs the single-launch prefill; drop --piecewise")
@@ -285,11 +302,16 @@ class Problem:
                                   self.cu_host, self.scale, out=self.out, lse=self.lse,
                                   workspace=self.pw_ws, status=self.status)
         else:
-            bca.prefill(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"], self.S, self.S,
-                        self.scale, out=self.out, lse=self.lse, workspace=self.ws,
+            bca.prefill(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"], self.max_s,
+                        self.max_s, self.scale, out=self.out, lse=self.lse, workspace=self.ws,
                         status=self.status)
         if events:
             events[1].record()
+        if not self.decode:            # prefill-only workload: no cache, no cached step
+            if events:
+                events[2].record()
+                events[3].record()
+            return
         if self.paged:
             bca.prefix_cache_append_paged(d["k"], d["v"], d["cu"], d["cu_pre"], self.page_table,
                                           self.cache_k, self.cache_v, 0, status=self.status)
@@ -304,17 +326,17 @@ class Problem:
             events[2].record()
         if self.paged:
             bca.prefix_decode_paged(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"],
-                                    self.page_table, d["k_tgt"], d["v_tgt"], d["cu_tgt"], self.N,
-                                    self.P, self.scale, out=self.dout, lse=self.dlse,
+                                    self.page_table, d["k_tgt"], d["v_tgt"], d["cu_tgt"],
+                                    self.max_n, self.max_p, self.scale, out=self.dout, lse=self.dlse,
                                     status=self.status)
         elif self.fp8_mode is None:
             bca.prefix_decode(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"], d["k_tgt"],
-                              d["v_tgt"], d["cu_tgt"], self.N, self.P, self.scale, out=self.dout,
+                              d["v_tgt"], d["cu_tgt"], self.max_n, self.max_p, self.scale, out=self.dout,
                               lse=self.dlse, status=self.status)
         else:
             bca.prefix_decode_fp8(d["q_tgt"], self.cache_k, self.cache_v, self.scale_k,
                                   self.scale_v, 0, d["cu_pre"], d["k_tgt"], d["v_tgt"],
-                                  d["cu_tgt"], self.N, self.P, self.scale, mode=self.fp8_mode,
+                                  d["cu_tgt"], self.max_n, self.max_p, self.scale, mode=self.fp8_mode,
                                   out=self.dout, lse=self.dlse, workspace=self.dec_ws,
                                   status=self.status)
         if events:
@@ -330,7 +352,8 @@ def fp8_decode_psnr(prob: "Problem", dev) -> float:
     cv = torch.empty_like(ck)
     bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], ck, cv, 0, status=prob.status)
     ref, _ = bca.prefix_decode(d["q_tgt"], ck, cv, 0, d["cu_pre"], d["k_tgt"], d["v_tgt"],
-                               d["cu_tgt"], prob.N, prob.P, prob.scale, status=prob.status)
+                               d["cu_tgt"], prob.max_n, prob.max_p, prob.scale,
+                               status=prob.status)
     prob.step(d)
     torch.cuda.synchronize()
     ref = ref.float()
@@ -353,7 +376,8 @@ def _prologue_step(self, d, events=None):
                             k_out=self.k_rot, status=self.status)
     if events:
         events[1].record()
-    bca.prefill(self.q_rot, self.k_rot, d["v"], d["block_id"], d["cu"], d["cu"], self.S, self.S,
+    bca.prefill(self.q_rot, self.k_rot, d["v"], d["block_id"], d["cu"], d["cu"], self.max_s,
+                self.max_s,
                 self.scale, out=self.out, lse=self.lse, workspace=self.ws, status=self.status)
     if events:
         events[2].record()
@@ -363,7 +387,7 @@ def _prologue_step(self, d, events=None):
     if events:
         events[3].record()
     bca.prefix_decode(self.qt_rot, self.cache_k, self.cache_v, 0, d["cu_pre"], self.kt_rot,
-                      d["v_tgt"], d["cu_tgt"], self.N, self.P, self.scale, out=self.dout,
+                      d["v_tgt"], d["cu_tgt"], self.max_n, self.max_p, self.scale, out=self.dout,
                       lse=self.dlse, status=self.status)
     if events:
         events[4].record()
@@ -380,10 +404,10 @@ def oracle_sample(prob: "Problem", step_idx: int, target_s: float = 3.0):
     wl, h = prob.wl, step_idx % prob.H
     host = prob.host
     cu = wl.cu_seqlens()
-    S = prob.S
+    S = prob.S0                        # rows of the first sequence
     # prefill: blocks of query rows of one head, until about target_s / 2
     from prefix_kv_gb300 import flops
-    e_rows = flops.row_ends(wl.block_id(), S)
+    e_rows = flops.row_ends(wl.block_id()[:S], S)
     t0 = time.perf_counter()
     rows_done, pairs, n = 0, 0, 512
     start = (step_idx * 1543) % S
@@ -394,22 +418,26 @@ def oracle_sample(prob: "Problem", step_idx: int, target_s: float = 3.0):
                        rows=rows, heads=np.array([h]))
         pairs += int(e_rows[rows].sum())
         rows_done += len(rows)
-    t1 = time.perf_counter()
+    t_prefill = time.perf_counter() - t0
     # decode: query rows of the same head
     drows_done, dpairs = 0, 0
-    while time.perf_counter() - t1 < target_s / 2 and drows_done < prob.N:
-        rows = np.arange(drows_done, min(prob.N, drows_done + n))
-        P = prob.P
-        oracle.prefix_decode(host["q_tgt"], host["k"][:P], host["v"][:P], wl.cu_prefix(),
+    n_dec = prob.N0 if wl.decode else 0
+    if "k_pre" not in host and n_dec:
+        pr = torch.from_numpy(wl.prefix_rows())
+        host = dict(host, k_pre=host["k"][pr].contiguous(), v_pre=host["v"][pr].contiguous())
+    t1 = time.perf_counter()
+    while time.perf_counter() - t1 < target_s / 2 and drows_done < n_dec:
+        rows = np.arange(drows_done, min(n_dec, drows_done + n))
+        oracle.prefix_decode(host["q_tgt"], host["k_pre"], host["v_pre"], wl.cu_prefix(),
                              host["k_tgt"], host["v_tgt"], wl.cu_target(), prob.scale,
                              rows=rows, heads=np.array([h]))
-        dpairs += len(rows) * (P + prob.N)
+        dpairs += len(rows) * (prob.P0 + prob.N0)
         drows_done += len(rows)
-    t2 = time.perf_counter()
+    t_decode = time.perf_counter() - t1
     fl = 4.0 * 128 * (pairs + dpairs)
-    desc = (f"head {h}: {rows_done} prefill rows + {drows_done} decode rows of {WORKLOAD} "
+    desc = (f"head {h}: {rows_done} prefill rows + {drows_done} decode rows of {wl.name} "
             f"(float64 NumPy oracle with explicit mask)")
-    return fl, t2 - t0, desc
+    return fl, t_prefill + t_decode, desc
 
 
 def cpu_threads():
@@ -435,6 +463,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="another config's workload (tiny_mixed_s40, t2i_1024_s4352, "
+                         "cfg_edit_4ref_varlen, neo_mixed_32seq); the default is the headline")
     ap.add_argument("--paged", action="store_true",
                     help="prefix cache in 128-token pages of a shuffled page table")
     ap.add_argument("--piecewise", action="store_true",
@@ -470,7 +501,7 @@ def main():
 
     import prefix_kv_gb300 as bca
     prob = Problem(dev, with_host=not args.no_e2e, cache=args.cache, prologue=args.prologue,
-                   piecewise=args.piecewise, paged=args.paged)
+                   piecewise=args.piecewise, paged=args.paged, workload=args.workload)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -507,13 +538,13 @@ def main():
     step_flops = prob.flops_prefill + prob.flops_decode
     value = whole_job_tflops(world, K, step_flops, tot_ms)
     pre_tf = prob.flops_prefill / (s_pre / K * 1e-3) / 1e12
-    dec_tf = prob.flops_decode / (s_dec / K * 1e-3) / 1e12
+    dec_tf = prob.flops_decode / (s_dec / K * 1e-3) / 1e12 if prob.decode else 0.0
     if prob.prologue:
         s_app = seg["prologue"] + seg["target_prologue"]
         app_gbs = prob.prologue_bytes / (s_app / K * 1e-3) / 1e9
     else:
         s_app = seg["append"]
-        app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9
+        app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9 if prob.decode else 0.0
 
     # ---- FP8 cache: PSNR of the decode output against a bf16 cache (untimed) ---------
     psnr = None
@@ -583,8 +614,13 @@ def main():
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(tot_ms / K, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": 1, "seq_len": prob.S, "num_heads": prob.H,
-                   "head_dim": 128, "prefix_len": prob.P, "target_len": prob.N,
+        "config": {"workload": prob.wl.name, "batch": prob.batch,
+                   "seq_len": prob.wl.seq_lens if prob.batch > 1 else prob.S,
+                   "num_heads": prob.H, "head_dim": 128,
+                   "prefix_len": (prob.wl.prefix_lens() if prob.batch > 1 else prob.P)
+                   if prob.decode else 0,
+                   "target_len": (prob.wl.target_lens() if prob.batch > 1 else prob.N)
+                   if prob.decode else 0,
                    "step": ("Q/K RMS norm + 3-axis RoPE + cache append, schedule prep + "
                             "prefill, target Q/K norm + RoPE, prefix decode") if prob.prologue
                            else ("piecewise prefill (schedule prep + attention + lse copy per "
@@ -627,13 +663,15 @@ def run_reference(args, rank, world, peaks):
     class HostProblem:
         pass
     hp = HostProblem()
-    wl = W.by_name(WORKLOAD)
+    wl = W.by_name(args.workload)
     q, k, v = W.make_qkv(wl)
     tr = torch.from_numpy(wl.target_rows())
-    hp.wl, hp.H, hp.S = wl, wl.num_heads, wl.seq_lens[0]
-    hp.N, hp.P, hp.scale = wl.target_lens()[0], wl.prefix_lens()[0], 1.0 / math.sqrt(128)
+    pr = torch.from_numpy(wl.prefix_rows())
+    hp.wl, hp.H, hp.S0 = wl, wl.num_heads, wl.seq_lens[0]
+    hp.N0, hp.P0, hp.scale = wl.target_lens()[0], wl.prefix_lens()[0], 1.0 / math.sqrt(128)
     hp.host = {"q": q, "k": k, "v": v, "q_tgt": q[tr].contiguous(), "k_tgt": k[tr].contiguous(),
-               "v_tgt": v[tr].contiguous()}
+               "v_tgt": v[tr].contiguous(), "k_pre": k[pr].contiguous(),
+               "v_pre": v[pr].contiguous()}
     for i in range(args.warmup):
         oracle_sample(hp, i, target_s=1.0)
     fl_tot, s_tot, desc = 0.0, 0.0, ""
@@ -647,8 +685,9 @@ def run_reference(args, rank, world, peaks):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(1e3 * s_tot / args.steps, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": 1, "seq_len": hp.S, "num_heads": hp.H,
-                   "head_dim": 128, "prefix_len": hp.P, "target_len": hp.N,
+        "config": {"workload": wl.name, "batch": wl.batch, "seq_len": wl.seq_lens,
+                   "num_heads": hp.H, "head_dim": 128, "prefix_len": wl.prefix_lens(),
+                   "target_len": wl.target_lens(),
                    "step": "bounded sample of prefill + prefix decode rows (oracle)"},
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": cpu_threads(),
                          "kind": "oracle", "sample": "each step: " + desc},
