@@ -28,6 +28,19 @@
  *   prefix invariant", "The prefix cache is a compute-for-memory trade" and
  *   "Two exact attention paths"; SenseNova-U1 inference-infra notes,
  *   "NEO-Unify 多模态 Prefill 的注意力" (per-M-block K-range extension).
+ *
+ * Beyond the prefill / decode / append path, the same library carries:
+ *   - an FP8 E4M3 prefix cache with one fp32 scale per (token, head)
+ *     (deployment notes, prefix-cache section): bca_prefix_cache_append_fp8,
+ *     bca_prefix_cache_dequant_fp8, bca_prefix_decode_fp8;
+ *   - the Q/K prologue, per-head RMS norm and three-axis RoPE fused with the
+ *     cache append (flozi.net, "Three-axis RoPE preserves image geometry"):
+ *     bca_rope_positions, bca_rope_table, bca_qk_norm_rope_append;
+ *   - the piecewise prefill baseline (one call per segment):
+ *     bca_prefill_piecewise;
+ *   - a paged prefix cache with a host page pool (SenseNova-U1 / Prism-Infer
+ *     notes, prefix KV reuse): bca_prefix_cache_append_paged,
+ *     bca_prefix_decode_paged, their FP8 forms, bca_pool_copy_rows, bca_pool_*.
  */
 #ifndef BCA_GB300_H
 #define BCA_GB300_H
@@ -45,9 +58,12 @@ enum {
   BCA_OK = 0,
   BCA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, negative size, bad scale      */
   BCA_ERR_UNSUPPORTED = 2,   /* head_dim != 128, more than 1024 image runs in a sequence */
-  BCA_ERR_BLOCK_ID = 3,      /* id < -1, or one image id split over separate runs      */
-  BCA_ERR_WORKSPACE = 4,     /* workspace NULL or smaller than bca_prefill_workspace_bytes */
-  BCA_ERR_CAPACITY = 5,      /* cache overflow: cu_prefix[batch] > capacity            */
+  BCA_ERR_BLOCK_ID = 3,      /* id < -1, one image id split over separate runs, or (RoPE
+                                coordinates) an id / image width that does not fit   */
+  BCA_ERR_WORKSPACE = 4,     /* workspace NULL, misaligned or smaller than its
+                                *_workspace_bytes                                     */
+  BCA_ERR_CAPACITY = 5,      /* cache overflow: cu_prefix[batch] > capacity, or a page
+                                id outside the pool                                   */
   BCA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, ...)    */
   BCA_ERR_TIMEOUT = 7,       /* a bounded device wait ran out; outputs are undefined   */
   BCA_ERR_SEQLENS = 8        /* cu_seqlens not monotone, q_len > kv_len, or a length

@@ -23,7 +23,10 @@
 // boundary tiles evaluate `key < e(r)`.  Decode reads the cached prefix tiles
 // through one tensor map and the target tiles through another, and masks only
 // the ragged end of each ("Two exact attention paths": cached steps need no
-// block-causal mask).
+// block-causal mask).  Prefix tile j of sequence b starts at cache token
+// cu_prefix[b] + 128 j, or with a page table at page_table[b][j] * 128 (a
+// 128-token page is one tile).  The last softmax warpgroup to read S(j) hands
+// the ring stages of V(j-1) and K(j) back to the producer.
 //
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax + epilogue of Q0 (thread t owns TMEM lane t = query row t)
@@ -96,18 +99,6 @@ struct FwdParams {
   float* lse;
   int32_t* status;
 };
-
-// K-major operand (Q, K): 128 rows x 128 bf16 stored as two 128-byte-swizzled
-// halves of 16 KB (columns 0-63, 64-127).  K-step kk covers columns 16kk..16kk+15.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t base, int kk) {
-  return smem_desc_sw128(base + (kk >> 2) * kHalfBytes + (kk & 3) * 32, 16, 1024);
-}
-// MN-major operand (V as the B of O += P V): rows = keys (the K dimension),
-// 64-column halves along N (head dim) are 16 KB apart (LBO), 8-key groups are
-// 1024 B apart (SBO).  K-step kk covers keys 16kk..16kk+15.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t base, int kk) {
-  return smem_desc_sw128(base + kk * 2048, kHalfBytes, 1024);
-}
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitLimitNs));
@@ -328,7 +319,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_qk = idesc_bf16_f32(kBlockM, kBlockN, 0, 0);
       constexpr uint32_t idesc_pv = idesc_bf16_f32(kBlockM, kHeadDim, 0, 1);
-      // descriptor start fields are in 16-byte units; a stage is kTileBytes / 16 apart
+      // Operand layouts.  K-major (Q as A, K as B of S = Q K^T): 128 rows x 128
+      // bf16 as two 128-byte-swizzled halves of 16 KB (columns 0-63, 64-127);
+      // K-step kk starts at half kk / 4, byte 32 * (kk % 4).  MN-major (V as B
+      // of O += P V): rows are keys, the 64-column halves along the head dim are
+      // 16 KB apart (LBO), 8-key groups 1024 B apart (SBO); K-step kk starts at
+      // key 16 kk (2048 B).  Descriptor start fields are in 16-byte units; a
+      // ring stage is kTileBytes / 16 apart.
       const uint64_t desc_q[2] = {smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024),
                                   smem_desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
       const uint64_t desc_k0 = smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024);

@@ -11,7 +11,11 @@
 // both sides, so one 16-thread group moves one row with 16-byte vectors;
 // reads walk the packed tensor in order, writes land in 256-byte runs.
 // Validation (capacity, prefix <= sequence) is done by every thread before it
-// writes anything, so a failing call writes nothing.
+// writes anything, so a failing call writes nothing.  With a page table the
+// prefix token t of sequence b goes to cache token page_table[b][t/128]*128 +
+// t%128 instead (one 128-token page per tile), every page id checked first.
+// Further down: the row copy of a shared tail page, the FP8 E4M3 append, its
+// expansion back to bf16, and the gather of paged layers for decode.
 #include "kernels.cuh"
 #include "ptx.cuh"
 
