@@ -95,3 +95,119 @@ def test_decode_and_append_host_validation(lib):
     assert app(16, 16, 16, 16, 1, 2, 128, 8, 16, 16, 2, 2, 64, None, None) == 1
     assert app(16, 16, 16, 16, 1, 2, 128, 8, None, 16, 0, 1, 64, None, None) == 1
     assert app(16, 16, 16, 16, 0, 2, 128, 8, 16, 16, 0, 1, 64, None, None) == 0
+
+
+def test_fp8_entry_points_host_validation(lib):
+    app = lib.bca_prefix_cache_append_fp8
+    #          k   v  ck  cp  B  H  D    tk mode ck  cv  sk  sv  layer L cap st  s
+    assert app(16, 16, 16, 16, 1, 2, 128, 8, 0, 16, 16, 16, 16, 0, 1, 64, None, None) == 1
+    assert app(16, 16, 16, 16, 1, 2, 64, 8, 1, 16, 16, 16, 16, 0, 1, 64, None, None) == 2
+    assert app(16, 16, 16, 16, 1, 2, 128, 8, 1, 16, 16, 16, None, 0, 1, 64, None, None) == 1
+    assert app(16, 16, 16, 16, 1, 2, 128, 8, 2, 16, 16, None, 16, 0, 1, 64, None, None) == 1
+    assert app(16, 16, 16, 16, 1, 2, 128, 8, 1, 16, 16, 16, 18, 0, 1, 64, None, None) == 1
+    assert app(16, 16, 16, 16, 0, 2, 128, 8, 1, 16, 16, 16, 16, 0, 1, 64, None, None) == 0
+    deq = lib.bca_prefix_cache_dequant_fp8
+    #          codes sc  cp  B  H  D    layer L cap out st  s
+    assert deq(16, 16, 16, 1, 2, 64, 0, 1, 64, 16, None, None) == 2
+    assert deq(16, 16, 16, 1, 2, 128, 1, 1, 64, 16, None, None) == 1
+    assert deq(16, 16, 16, 1, 2, 128, 0, 1, 64, None, None, None) == 1
+    assert deq(24, 16, 16, 1, 2, 128, 0, 1, 64, 16, None, None) == 1
+    assert deq(16, 16, 16, 1, 2, 128, 0, 1, 0, 16, None, None) == 0
+    wsb = lib.bca_prefix_decode_fp8_workspace_bytes
+    assert wsb(1, 2, 128, 64) == 2 * 64 * 128 * 2
+    assert wsb(2, 2, 128, 64) == 2 * 2 * 64 * 128 * 2
+    assert wsb(0, 2, 128, 64) == 0 and wsb(1, 2, 64, 64) == 0
+    dec = lib.bca_prefix_decode_fp8
+    # q ck cv mode sk sv layer L cap cup tk tv cq B H D tq mq mp scale out lse ws wsb st s
+    args = [16, 16, 16, 1, 16, 16, 0, 1, 64, 16, 16, 16, 16, 1, 2, 128, 8, 8, 8, 0.1, 16, 16,
+            16, 1 << 20, None, None]
+    bad_mode = list(args); bad_mode[3] = 0
+    assert dec(*bad_mode) == 1
+    no_ws = list(args); no_ws[22] = None
+    assert dec(*no_ws) == 4
+    small_ws = list(args); small_ws[23] = 100
+    assert dec(*small_ws) == 4
+
+
+def test_prologue_entry_points_host_validation(lib):
+    pos = lib.bca_rope_positions
+    #          bid cu  B  total gw  n_ids pos st  s
+    assert pos(16, 16, 1, 8, 16, 5000, 16, None, None) == 2
+    assert pos(16, 16, -1, 8, 16, 1, 16, None, None) == 1
+    assert pos(16, 16, 1, 8, None, 1, 16, None, None) == 1
+    assert pos(16, 16, 0, 8, 16, 1, 16, None, None) == 0
+    tab = lib.bca_rope_table
+    assert tab(16, -1, 16, None) == 1
+    assert tab(16, 4, 24, None) == 1                  # table misaligned
+    assert tab(16, 0, 16, None) == 0
+    qk = lib.bca_qk_norm_rope_append
+    # q k v gq gk table cu cp B H D total eps qo ko ck cv layer L cap st s
+    base = [16, 16, 16, 16, 16, 16, 16, None, 1, 2, 128, 8, 1e-6, 16, 16, None, None, 0, 1, 0,
+            None, None]
+    d64 = list(base); d64[10] = 64
+    assert qk(*d64) == 2
+    neg_eps = list(base); neg_eps[12] = -1.0
+    assert qk(*neg_eps) == 1
+    nan_eps = list(base); nan_eps[12] = float("nan")
+    assert qk(*nan_eps) == 1
+    bad_gamma = list(base); bad_gamma[3] = 20
+    assert qk(*bad_gamma) == 1
+    app_no_v = list(base); app_no_v[7] = 16; app_no_v[2] = None; app_no_v[15] = 16
+    app_no_v[16] = 16; app_no_v[19] = 64
+    assert qk(*app_no_v) == 1
+    empty = list(base); empty[11] = 0
+    assert qk(*empty) == 0
+
+
+def test_piecewise_host_validation(lib):
+    bid = (ctypes.c_int32 * 8)(-1, -1, 0, 0, 0, -1, 1, 1)
+    cu = (ctypes.c_int32 * 2)(0, 8)
+    need = lib.bca_prefill_piecewise_workspace_bytes(bid, cu, 1, 2)
+    assert need > 0
+    assert lib.bca_prefill_piecewise_workspace_bytes(None, cu, 1, 2) == 0
+    pw = lib.bca_prefill_piecewise
+    # q k v bid bid_h cu_h B H D total scale out lse ws wsb st s
+    args = [16, 16, 16, 16, bid, cu, 1, 2, 128, 8, 0.1, 16, 16, 16, need, None, None]
+    d64 = list(args); d64[8] = 64
+    assert pw(*d64) == 2
+    short = list(args); short[9] = 9                    # cu_seqlens does not end at total
+    assert pw(*short) == 8
+    small = list(args); small[14] = need - 1
+    assert pw(*small) == 4
+    empty = list(args); empty[6] = 0
+    assert pw(*empty) == 0
+
+
+def test_paged_entry_points_host_validation(lib):
+    app = lib.bca_prefix_cache_append_paged
+    # k v ck cp pt maxp B H D tk ck cv layer L npages st s
+    assert app(16, 16, 16, 16, 16, 2, 1, 2, 128, 8, 16, 16, 0, 1, 0, None, None) == 1
+    assert app(16, 16, 16, 16, None, 2, 1, 2, 128, 8, 16, 16, 0, 1, 4, None, None) == 1
+    assert app(16, 16, 16, 16, 16, 2, 1, 2, 64, 8, 16, 16, 0, 1, 4, None, None) == 2
+    dec = lib.bca_prefix_decode_paged
+    # q ck cv layer L npages cp pt maxp tk tv cq B H D tq mq mp scale out lse st s
+    args = [16, 16, 16, 0, 1, 4, 16, 16, 2, 16, 16, 16, 1, 2, 128, 8, 8, 8, 0.1, 16, 16, None,
+            None]
+    no_pages = list(args); no_pages[5] = 0
+    assert dec(*no_pages) == 1
+    no_table = list(args); no_table[7] = None
+    assert dec(*no_table) == 1
+    cp = lib.bca_pool_copy_rows
+    # ck cv layer L H npages src dst rows s
+    assert cp(16, 16, 0, 1, 2, 4, 1, 1, 10, None) == 0   # same page: nothing to do
+    assert cp(16, 16, 0, 1, 2, 4, 1, 2, 129, None) == 1
+    assert cp(16, 16, 0, 1, 2, 4, 4, 2, 10, None) == 1
+    assert cp(16, 16, 0, 1, 2, 4, 1, 2, 0, None) == 0
+    a8 = lib.bca_prefix_cache_append_fp8_paged
+    # k v ck cp pt maxp B H D tk mode ck cv sk sv layer L npages st s
+    assert a8(16, 16, 16, 16, 16, 2, 1, 2, 128, 8, 1, 16, 16, 16, 16, 0, 1, 0, None, None) == 1
+    assert a8(16, 16, 16, 16, 16, 2, 1, 2, 128, 8, 3, 16, 16, 16, 16, 0, 1, 4, None, None) == 1
+    d8 = lib.bca_prefix_decode_fp8_paged
+    # q ck cv mode sk sv layer L npages cp pt maxp rows tk tv cq B H D tq mq mp scale out lse ws wsb st s
+    args8 = [16, 16, 16, 1, 16, 16, 0, 1, 4, 16, 16, 2, 256, 16, 16, 16, 1, 2, 128, 8, 8, 8, 0.1,
+             16, 16, 16, 1 << 20, None, None]
+    m0 = list(args8); m0[3] = 0
+    assert d8(*m0) == 1
+    small = list(args8); small[26] = 10
+    assert d8(*small) == 4
+    assert lib.bca_prefix_decode_fp8_paged_workspace_bytes(2, 128, 256) == 2 * 2 * 256 * 128 * 2
