@@ -161,6 +161,17 @@ def whole_job_tflops(world: int, steps: int, step_flops: float, total_ms: float)
 
 # ----------------------------------------------------------------------------- inputs
 
+def decode_grids(num_heads, max_q, batch, sms):
+    """Grids one decode call launches: tile pairs (head x pair x sequence) fill
+    whole waves of the SMs; a last wave at most half full becomes a second grid
+    of key-split single tiles (two CTAs per pair)."""
+    pairs = (-(-max_q // 128) + 1) // 2
+    items = num_heads * pairs * batch
+    tail = items % sms
+    split_from = items - tail if 0 < tail and 2 * tail <= sms else items
+    return int(split_from > 0) + int(items > split_from)
+
+
 class Problem:
     """The workload's tensors, resident on the device (plus pinned host copies for e2e)."""
 
@@ -229,7 +240,10 @@ class Problem:
         else:                                                    # K and V quantised
             self.append_bytes = rows * 2 * (256 + 128 + 4)
         # kernel launches per step: schedule prep, prefill, append, [expansions], decode
-        self.launches = (4 + {None: 0, "v": 1, "kv": 2}[self.fp8_mode] if wl.decode
+        # (one grid of tile pairs and, for a short last wave, one of key-split tiles)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.launches = (3 + {None: 0, "v": 1, "kv": 2}[self.fp8_mode] +
+                         decode_grids(self.H, self.max_n, self.batch, sms) if wl.decode
                          else 2)          # prefill only: schedule prep + attention
         # optional Q/K prologue (RMS norm + three-axis RoPE; the prefill-side call also
         # appends): coordinates and rotation table once per layout, outside the step

@@ -10,6 +10,12 @@
 // softmax warpgroup turns S into P the tensor core runs the other tile's MMAs.
 // Because S_i(j+1) is issued after PV_i(j), the commit that signals S_i(j+1)
 // also covers PV_i(j): the softmax may rescale O_i right after seeing S_i(j+1).
+// Decode items that would fill less than half of a last wave run in a second
+// grid as single query tiles whose key range is split in two: warpgroup i runs
+// the same loop over its part with its own K/V tiles (the stages are handed
+// back by MMA commits), and warpgroup 0 merges the two partial rows, each
+// against its own reference max, at the end.  Such an item takes about half a
+// pair's time, where a single tile on one warpgroup would take 0.7.
 // The reference max is taken exactly on the first K tile; afterwards P is
 // formed against it directly and the max is only recomputed (with O and l
 // rescaled) for a tile whose row sum would exceed 2^16.  O and l share the
@@ -74,8 +80,11 @@ struct FwdSmem {
   uint64_t fix_req;     // MMA thread saw a tail V tile land: fix-up warp may zero it
   uint64_t v_fixed;     // fix-up warp zeroed the tail rows of that V tile
   uint64_t drain;
+  uint64_t merge;       // key split: warpgroup 1 published its row maxima and sums
   uint32_t tmem_base;
   int abort;
+  int fix_stage;        // the V tile to fix: its ring stage and first row past the segment
+  int fix_from;
 };
 constexpr size_t kSmemBytes = sizeof(FwdSmem) + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -104,44 +113,18 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitLimitNs));
 }
 
-template <bool kDecode>
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
-                    const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v,
-                    const __grid_constant__ CUtensorMap tm_k2,
-                    const __grid_constant__ CUtensorMap tm_v2, const FwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-
+// One work item: head h, sequence b and its query tiles m_base .. m_base + n_qt - 1
+// (kSplit: the single tile m_base for both softmax warpgroups, each over part
+// of the key range; their partial results are merged at the end).
+template <bool kDecode, bool kSplit>
+__device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                                          const CUtensorMap& tm_v, const CUtensorMap& tm_k2,
+                                          const CUtensorMap& tm_v2, const FwdParams& p, FwdSmem& sm,
+                                          const int h, const int b, const int m_base,
+                                          const int n_qt) {
+  static_assert(kDecode || !kSplit, "key split is a decode item");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // Work item: head h, sequence b and its query tiles m_base .. m_base + n_qt - 1.
-  // Prefill: a 3-D grid of (head, tile pair, sequence), costliest pairs first.
-  // Decode: a 1-D list of equal-cost tile pairs; the pairs of a last, partly
-  // filled wave are split into single-tile items so that wave ends sooner.
-  int h, b, m_base, n_qt;
-  if constexpr (!kDecode) {
-    h = blockIdx.x;
-    m_base = 2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y));
-    b = blockIdx.z;
-    n_qt = 2;
-  } else {
-    const int L = blockIdx.x;
-    int item = L, sub = 0;
-    n_qt = 2;
-    if (L >= p.decode_split_from) {
-      item = p.decode_split_from + (L - p.decode_split_from) / 2;
-      sub = (L - p.decode_split_from) & 1;
-      n_qt = 1;
-    }
-    h = item % p.num_heads;
-    const int rest = item / p.num_heads;
-    m_base = 2 * (rest % p.decode_pairs_per_seq) + sub;
-    b = rest / p.decode_pairs_per_seq;
-  }
-
   // Another CTA already gave up waiting: do not start new work.
   if (p.status != nullptr && *reinterpret_cast<volatile int32_t*>(p.status) == BCA_ERR_TIMEOUT)
     return;
@@ -151,8 +134,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int q_len = p.cu_q[b + 1] - q_seq0;
   int rows_valid[2], nkt[2];
   int k_min[2] = {0, 0}, k_hi[2] = {0, 0};
-  for (int i = 0; i < 2; ++i)
-    rows_valid[i] = i < n_qt ? min(kBlockM, max(0, q_len - (m_base + i) * kBlockM)) : 0;
+  for (int i = 0; i < 2; ++i) {
+    const int m = m_base + (kSplit ? 0 : i);   // a key-split item's warpgroups share one tile
+    rows_valid[i] = i < n_qt ? min(kBlockM, max(0, q_len - m * kBlockM)) : 0;
+  }
   if (rows_valid[0] <= 0) return;
 
   int kv_seq0 = 0;     // prefill: first key of the sequence
@@ -199,14 +184,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       return;
     }
     const int n_all = n_pre_tiles + (q_len + kBlockN - 1) / kBlockN;
-    for (int i = 0; i < 2; ++i) nkt[i] = rows_valid[i] > 0 ? n_all : 0;
+    if constexpr (kSplit) {
+      // warpgroup 1: key tiles [n_all - n_all / 2, n_all); warpgroup 0: the
+      // rest (as many or one more; all of a single tile)
+      nkt[1] = n_all / 2;
+      nkt[0] = n_all - nkt[1];
+    } else {
+      for (int i = 0; i < 2; ++i) nkt[i] = rows_valid[i] > 0 ? n_all : 0;
+    }
   }
   // Row ends never decrease along a sequence, so a present Q1 needs at least as
   // many key tiles as Q0; keep that invariant explicitly (extra tiles would be
   // fully masked), since ring stages are released by Q1's softmax (below).
-  if (nkt[1] > 0 && nkt[1] < nkt[0]) nkt[1] = nkt[0];
+  if (!kSplit && nkt[1] > 0 && nkt[1] < nkt[0]) nkt[1] = nkt[0];
   const int nk = max(nkt[0], nkt[1]);
   const int k_hi_all = max(k_hi[0], k_hi[1]);
+  const int koff1 = kSplit ? nkt[0] : 0;                  // first key tile of warpgroup 1
+  const int n_kv_tiles = kSplit ? nkt[0] + nkt[1] : nk;   // distinct K/V tiles of the item
   // valid keys left in K/V tile j's segment (>= 128: the tile is full)
   auto seg_left_of = [&](int j) {
     if constexpr (!kDecode) {
@@ -231,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&sm.fix_req, 1);
     mbar_init(&sm.v_fixed, 1);
     mbar_init(&sm.drain, 1);
+    mbar_init(&sm.merge, kSoftmaxThreads);
     sm.abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -266,21 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t armed = 0;   // bit s: stage s has been loaded at least once
       uint32_t parity = 0;  // bit s: parity of the last load into stage s
-      const int n_q = rows_valid[1] > 0 ? 2 : 1;
+      const int n_q = !kSplit && rows_valid[1] > 0 ? 2 : 1;
       mbar_arrive_expect_tx(&sm.q_full, n_q * kTileBytes);
       for (int i = 0; i < n_q; ++i) {
         const int row0 = q_seq0 + (m_base + i) * kBlockM;
         tma_load_3d(&tm_q, &sm.q_full, sm.q[i], 0, h, row0);
         tma_load_3d(&tm_q, &sm.q_full, sm.q[i] + kHalfBytes, 64, h, row0);
       }
-      for (int i = 0; i < 2 * nk; ++i) {
-        const int j = i >> 1;
-        const bool is_v = i & 1;
-        const int s = stage_of(i);
-        const int r = i / kStages;
+      // Load number idx (ring stage idx % kStages) of K or V tile g.
+      auto load = [&](int idx, bool is_v, int g) {
+        const int s = stage_of(idx);
+        const int r = idx / kStages;
         if (r > 0 && !mbar_wait(&sm.kv_empty[s], (r - 1) & 1, abort_flag, kWaitLimitNs)) {
           give_up();
-          break;
+          return false;
         }
         mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
         armed |= 1u << s;
@@ -288,21 +282,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* dst = sm.kv[s];
         if constexpr (!kDecode) {
           const CUtensorMap* m = is_v ? &tm_v : &tm_k;
-          const int tok = kv_seq0 + j * kBlockN;
+          const int tok = kv_seq0 + g * kBlockN;
           tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
           tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
-        } else if (j < n_pre_tiles) {
+        } else if (g < n_pre_tiles) {
           const CUtensorMap* m = is_v ? &tm_v : &tm_k;
           const int tok = p.page_table != nullptr
-                              ? p.page_table[static_cast<int64_t>(b) * p.max_pages + j] * kBlockN
-                              : pre0 + j * kBlockN;
+                              ? p.page_table[static_cast<int64_t>(b) * p.max_pages + g] * kBlockN
+                              : pre0 + g * kBlockN;
           tma_load_3d(m, &sm.kv_full[s], dst, 0, tok, h);
           tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, tok, h);
         } else {
           const CUtensorMap* m = is_v ? &tm_v2 : &tm_k2;
-          const int tok = q_seq0 + (j - n_pre_tiles) * kBlockN;
+          const int tok = q_seq0 + (g - n_pre_tiles) * kBlockN;
           tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
           tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
+        }
+        return true;
+      };
+      if constexpr (!kSplit) {
+        // K_j, V_j shared by both query tiles: loads 2j and 2j + 1
+        for (int i = 0; i < 2 * nk; ++i)
+          if (!load(i, i & 1, i >> 1)) break;
+      } else {
+        // Each warpgroup has its own tiles; loads follow the MMA thread's order of
+        // use: K_0(0), K_1(0), then per step j: V_0(j), K_0(j+1), V_1(j), K_1(j+1).
+        int idx = 0;
+        bool go = true;
+        for (int j = 0; j <= nk && go; ++j) {
+          for (int i = 0; i < 2 && go; ++i) {
+            const int g0 = i == 0 ? 0 : koff1;
+            if (j >= 1 && j - 1 < nkt[i]) go = load(idx++, true, g0 + j - 1);
+            if (go && j < nkt[i]) go = load(idx++, false, g0 + j);
+          }
         }
       }
       // If anything went wrong, let every load in flight land before the CTA exits.
@@ -326,8 +338,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // 16 KB apart (LBO), 8-key groups 1024 B apart (SBO); K-step kk starts at
       // key 16 kk (2048 B).  Descriptor start fields are in 16-byte units; a
       // ring stage is kTileBytes / 16 apart.
+      // (a key-split item has its one query tile in q[0], used by both S MMAs)
       const uint64_t desc_q[2] = {smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024),
-                                  smem_desc_sw128(smem_u32(sm.q[1]), 16, 1024)};
+                                  smem_desc_sw128(smem_u32(sm.q[kSplit ? 0 : 1]), 16, 1024)};
       const uint64_t desc_k0 = smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024);
       const uint64_t desc_v0 = smem_desc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);
       auto issue_s = [&](int i, int stage) {  // S_i = Q_i K^T
@@ -351,38 +364,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j == nkt[i] - 1) umma_commit(&sm.o_final[i]);
       };
 
-      bool ok = mbar_wait(&sm.q_full, 0, abort_flag, kWaitLimitNs);
-      if (ok && nk > 0) {
-        ok = mbar_wait(&sm.kv_full[stage_of(0)], phase_of(0), abort_flag, kWaitLimitNs);
-        if (ok) {
-          for (int i = 0; i < 2; ++i)
-            if (nkt[i] > 0) issue_s(i, stage_of(0));
-        }
-      }
+      // V tile g in stage s has landed; if its segment ends inside it, have the
+      // fix-up warp zero the rows past the end before any PV reads it.
       int tails = 0;
-      for (int j = 0; j < nk && ok; ++j) {
-        const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
-        ok = mbar_wait(&sm.kv_full[vs], phase_of(2 * j + 1), abort_flag, kWaitLimitNs);
-        if (ok && seg_left_of(j) < kBlockN) {  // the fix-up warp zeroes V rows past the segment
-          mbar_arrive(&sm.fix_req);
-          ok = mbar_wait(&sm.v_fixed, tails & 1, abort_flag, kWaitLimitNs);
-          ++tails;
-        }
-        bool k_next_ready = false;
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (j < nkt[i]) {
-            ok = mbar_wait(&sm.p_full[i], j & 1, abort_flag, kWaitLimitNs);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(i, vs, j);
+      auto fix_tail = [&](int g, int s) {
+        const int left = seg_left_of(g);
+        if (left >= kBlockN) return true;
+        sm.fix_stage = s;
+        sm.fix_from = left;
+        mbar_arrive(&sm.fix_req);
+        return mbar_wait(&sm.v_fixed, (tails++) & 1, abort_flag, kWaitLimitNs);
+      };
+      auto landed = [&](int idx) {
+        return mbar_wait(&sm.kv_full[stage_of(idx)], phase_of(idx), abort_flag, kWaitLimitNs);
+      };
+
+      bool ok = mbar_wait(&sm.q_full, 0, abort_flag, kWaitLimitNs);
+      if constexpr (!kSplit) {
+        if (ok && nk > 0) {
+          ok = landed(0);
+          if (ok) {
+            for (int i = 0; i < 2; ++i)
+              if (nkt[i] > 0) issue_s(i, stage_of(0));
           }
-          if (j + 1 < nkt[i]) {
-            if (!k_next_ready) {
-              ok = mbar_wait(&sm.kv_full[ks], phase_of(2 * j + 2), abort_flag, kWaitLimitNs);
+        }
+        for (int j = 0; j < nk && ok; ++j) {
+          const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
+          ok = landed(2 * j + 1) && fix_tail(j, vs);
+          bool k_next_ready = false;
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (j < nkt[i]) {
+              ok = mbar_wait(&sm.p_full[i], j & 1, abort_flag, kWaitLimitNs);
               if (!ok) break;
-              k_next_ready = true;
+              tc_fence_after();
+              issue_pv(i, vs, j);
             }
-            issue_s(i, ks);
+            if (j + 1 < nkt[i]) {
+              if (!k_next_ready) {
+                ok = landed(2 * j + 2);
+                if (!ok) break;
+                k_next_ready = true;
+              }
+              issue_s(i, ks);
+            }
+          }
+        }
+      } else {
+        // Key split: every operand is used once, in the producer's load order, and
+        // its stage is handed back by a commit as soon as its MMA completes.
+        int c = 0;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (nkt[i] == 0) continue;
+          ok = landed(c);
+          if (ok) {
+            issue_s(i, stage_of(c));
+            umma_commit(&sm.kv_empty[stage_of(c)]);
+            ++c;
+          }
+        }
+        for (int j = 0; j < nk && ok; ++j) {
+          for (int i = 0; i < 2 && ok; ++i) {
+            if (j < nkt[i]) {
+              const int vs = stage_of(c);
+              ok = landed(c) && fix_tail((i == 0 ? 0 : koff1) + j, vs) &&
+                   mbar_wait(&sm.p_full[i], j & 1, abort_flag, kWaitLimitNs);
+              if (!ok) break;
+              tc_fence_after();
+              issue_pv(i, vs, j);
+              umma_commit(&sm.kv_empty[vs]);
+              ++c;
+            }
+            if (j + 1 < nkt[i]) {
+              ok = landed(c);
+              if (!ok) break;
+              issue_s(i, stage_of(c));
+              umma_commit(&sm.kv_empty[stage_of(c)]);
+              ++c;
+            }
           }
         }
       }
@@ -396,19 +454,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ====================== V tail fix-up ======================
     // Keys past the end of a tile's segment may hold anything (another
     // sequence, unused cache capacity): zero those V rows so 0 * V stays 0.
-    // The request comes from the MMA thread after its own wait on the tile's
-    // kv_full phase, so this warp never polls a ring barrier phases behind.
-    int tails = 0;
-    for (int j = 0; j < nk; ++j) {
-      const int seg_left = seg_left_of(j);
-      if (seg_left >= kBlockN) continue;
-      const int vi = 2 * j + 1;
-      if (!warp_wait(&sm.fix_req, tails & 1, abort_flag)) {
+    // The MMA thread names the stage and the first row to clear, after its own
+    // wait on the tile's kv_full phase, so this warp never polls a ring barrier.
+    int n_tails = 0;
+    for (int g = 0; g < n_kv_tiles; ++g) n_tails += seg_left_of(g) < kBlockN ? 1 : 0;
+    for (int t = 0; t < n_tails; ++t) {
+      if (!warp_wait(&sm.fix_req, t & 1, abort_flag)) {
         if (lane == 0) give_up();
         break;
       }
-      ++tails;
-      uint8_t* vb = sm.kv[stage_of(vi)];
+      uint8_t* vb = sm.kv[*reinterpret_cast<volatile int*>(&sm.fix_stage)];
+      const int seg_left = *reinterpret_cast<volatile int*>(&sm.fix_from);
       const int nrows = kBlockN - seg_left;
       for (int idx = lane; idx < nrows * 16; idx += 32) {
         const int row = seg_left + (idx >> 4);
@@ -428,12 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int wq = warp & 3;                // TMEM lane group
     const int row = wq * 32 + lane;         // == TMEM lane == row within the tile
     const int n_tiles = nkt[qi];
-    const int row0 = q_seq0 + (m_base + qi) * kBlockM;
+    const int koff = qi == 1 ? koff1 : 0;   // global index of this warpgroup's first key tile
+    const int row0 = q_seq0 + (m_base + (kSplit ? 0 : qi)) * kBlockM;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_addr = lane_addr + kColS + qi * 128;
     const uint32_t o_addr = lane_addr + kColO + qi * 128;
     const bool row_valid = row < rows_valid[qi];
-    const bool releaser = qi == 1 || nkt[1] == 0;
+    const bool releaser = !kSplit && (qi == 1 || nkt[1] == 0);
     int e_row = 0;
     if constexpr (!kDecode) e_row = row_valid ? p.row_end[row0 + row] : k_hi[qi];
     const float sl2 = p.scale_log2;
@@ -463,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         lim = e_row - j * kBlockN;
         need_mask = (j + 1) * kBlockN > k_min[qi];
       } else {
-        lim = j < n_pre_tiles ? n_pre - j * kBlockN : q_len - (j - n_pre_tiles) * kBlockN;
+        const int g = koff + j;
+        lim = g < n_pre_tiles ? n_pre - g * kBlockN : q_len - (g - n_pre_tiles) * kBlockN;
         need_mask = lim < kBlockN;
       }
       if (need_mask) {
@@ -541,33 +599,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sm.p_full[qi]);
     }
 
-    if (ok && n_tiles > 0) ok = warp_wait(&sm.o_final[qi], 0, abort_flag);
-    if (!ok) {
-      if (lane == 0) give_up();
-    } else if (n_tiles > 0) {
-      tc_fence_after();
-      const float inv_l = 1.f / l_run;
-      __nv_bfloat16* orow =
-          p.out + (static_cast<size_t>(row0 + row) * p.num_heads + h) * kHeadDim;
+    if constexpr (kSplit) {
+      // Key split: warpgroup 1 hands its row maxima and sums to warpgroup 0, which
+      // brings both partial rows to the larger max before adding O and l.  With a
+      // single key tile warpgroup 1 has none, and there is nothing to merge.
+      float* const ml = reinterpret_cast<float*>(sm.q[1]);   // q[1] holds no query here
+      const bool use1 = nkt[1] > 0;
+      if (qi == 1) {
+        if (!ok) {
+          if (lane == 0) give_up();
+        } else if (use1) {
+          ml[2 * row] = m_ref;
+          ml[2 * row + 1] = l_run;
+          mbar_arrive(&sm.merge);
+        }
+      } else {
+        ok = ok && warp_wait(&sm.o_final[0], 0, abort_flag);
+        if (use1)
+          ok = ok && warp_wait(&sm.merge, 0, abort_flag) && warp_wait(&sm.o_final[1], 0, abort_flag);
+        if (!ok) {
+          if (lane == 0) give_up();
+        } else {
+          tc_fence_after();
+          float m_fin = m_ref, l_fin = l_run, a0 = 1.f, a1 = 0.f;
+          if (use1) {
+            const float m1 = ml[2 * row], l1 = ml[2 * row + 1];
+            m_fin = fmaxf(m_ref, m1);
+            a0 = ex2_approx(m_ref - m_fin);
+            a1 = ex2_approx(m1 - m_fin);
+            l_fin = l_run * a0 + l1 * a1;
+          }
+          const float inv_l = 1.f / l_fin;
+          const float c0 = a0 * inv_l, c1 = a1 * inv_l;
+          __nv_bfloat16* orow =
+              p.out + (static_cast<size_t>(row0 + row) * p.num_heads + h) * kHeadDim;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(o_addr + c * 32, r);
-        uint32_t w[16];
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r0[16], r1[16];
+            tmem_ld16(o_addr + c * 16, r0);
+            if (use1) {
+              tmem_ld16(o_addr + 128 + c * 16, r1);
+            } else {
 #pragma unroll
-        for (int x = 0; x < 16; ++x)
-          w[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
-                             __uint_as_float(r[2 * x + 1]) * inv_l);
-        if (row_valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+              for (int x = 0; x < 16; ++x) r1[x] = 0;
+            }
+            uint32_t w[8];
 #pragma unroll
-          for (int x = 0; x < 4; ++x)
-            dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+            for (int x = 0; x < 8; ++x)
+              w[x] = pack_bf16x2(
+                  __uint_as_float(r0[2 * x]) * c0 + __uint_as_float(r1[2 * x]) * c1,
+                  __uint_as_float(r0[2 * x + 1]) * c0 + __uint_as_float(r1[2 * x + 1]) * c1);
+            if (row_valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
+              dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+              dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+          }
+          if (row_valid) {
+            p.lse[static_cast<size_t>(h) * p.total_q + row0 + row] =
+                (m_fin + log2f(l_fin)) * 0.69314718055994530942f;
+          }
         }
       }
-      if (row_valid) {
-        p.lse[static_cast<size_t>(h) * p.total_q + row0 + row] =
-            (m_ref + log2f(l_run)) * 0.69314718055994530942f;
+    } else {
+      if (ok && n_tiles > 0) ok = warp_wait(&sm.o_final[qi], 0, abort_flag);
+      if (!ok) {
+        if (lane == 0) give_up();
+      } else if (n_tiles > 0) {
+        tc_fence_after();
+        const float inv_l = 1.f / l_run;
+        __nv_bfloat16* orow =
+            p.out + (static_cast<size_t>(row0 + row) * p.num_heads + h) * kHeadDim;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c * 32, r);
+          uint32_t w[16];
+#pragma unroll
+          for (int x = 0; x < 16; ++x)
+            w[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
+                               __uint_as_float(r[2 * x + 1]) * inv_l);
+          if (row_valid) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+              dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+          }
+        }
+        if (row_valid) {
+          p.lse[static_cast<size_t>(h) * p.total_q + row0 + row] =
+              (m_ref + log2f(l_run)) * 0.69314718055994530942f;
+        }
       }
     }
   }
@@ -578,6 +700,44 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Prefill: a 3-D grid of (head, tile pair, sequence), costliest pairs first.
+// Decode: a 1-D list of equal-cost tile pairs; the pairs of a last, partly
+// filled wave become single-tile items (kSplit: two CTAs per pair, each with its
+// key range split between the two softmax warpgroups), launched as a second
+// grid that may start as soon as every pair CTA has started.
+template <bool kDecode, bool kSplit>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v,
+                    const __grid_constant__ CUtensorMap tm_k2,
+                    const __grid_constant__ CUtensorMap tm_v2, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  if constexpr (!kDecode) {
+    attn_item<false, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, blockIdx.x, blockIdx.z,
+                            2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y)),
+                            2);
+  } else if constexpr (!kSplit) {
+    grid_launch_dependents();
+    const int L = blockIdx.x;
+    const int rest = L / p.num_heads;
+    attn_item<true, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, L % p.num_heads,
+                           rest / p.decode_pairs_per_seq, 2 * (rest % p.decode_pairs_per_seq), 2);
+  } else {
+    const int item = p.decode_split_from + static_cast<int>(blockIdx.x) / 2;
+    const int sub = blockIdx.x & 1;
+    const int rest = item / p.num_heads;
+    attn_item<true, true>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, item % p.num_heads,
+                          rest / p.decode_pairs_per_seq,
+                          2 * (rest % p.decode_pairs_per_seq) + sub, 2);
+    // This grid may run beside the pair grid launched before it: do not
+    // complete before that grid has, so work queued after both sees its output.
+    grid_dependency_wait();
   }
 }
 
@@ -663,50 +823,70 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   p.lse = a.lse;
   p.status = a.status;
 
-  dim3 grid(a.num_heads, (a.tiles_per_seq + 1) / 2, a.batch);
-  if (decode) {
-    // Equal-cost pair items; when the last wave would be at most half full,
-    // its pairs become single-tile items (two CTAs each, ~0.7x the time).
-    static int sms = 0;
-    if (sms == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 1;
-    }
-    const int pps = (a.tiles_per_seq + 1) / 2;
-    const int64_t items = static_cast<int64_t>(a.num_heads) * pps * a.batch;
-    const int64_t tail = items % sms;
-    const int64_t split_from = (tail > 0 && 2 * tail <= sms) ? items - tail : items;
-    const int64_t ctas = split_from + 2 * (items - split_from);
-    if (ctas > 0x7fffffff) return BCA_ERR_UNSUPPORTED;
-    p.decode_pairs_per_seq = pps;
-    p.decode_split_from = static_cast<int>(split_from);
-    grid = dim3(static_cast<unsigned>(ctas), 1, 1);
-  }
-  cudaError_t err;
   if (!decode) {
     static bool attr_set = false;
     if (!attr_set) {
-      err = cudaFuncSetAttribute(attn_fwd_kernel<false>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-      if (err != cudaSuccess) return BCA_ERR_CUDA;
+      if (cudaFuncSetAttribute(attn_fwd_kernel<false, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes)) != cudaSuccess)
+        return BCA_ERR_CUDA;
       attr_set = true;
     }
-    attn_fwd_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
-  } else {
-    static bool attr_set = false;
-    if (!attr_set) {
-      err = cudaFuncSetAttribute(attn_fwd_kernel<true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kSmemBytes));
-      if (err != cudaSuccess) return BCA_ERR_CUDA;
-      attr_set = true;
-    }
-    attn_fwd_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+    const dim3 grid(a.num_heads, (a.tiles_per_seq + 1) / 2, a.batch);
+    attn_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+    const cudaError_t err = cudaGetLastError();
+    return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
   }
-  err = cudaGetLastError();
+  // Decode: equal-cost pair items; when the last wave would be at most half
+  // full, its pairs become key-split single-tile items (two CTAs each, about
+  // half a pair's time) in a second grid.
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
+  const int pps = (a.tiles_per_seq + 1) / 2;
+  const int64_t items = static_cast<int64_t>(a.num_heads) * pps * a.batch;
+  const int64_t tail = items % sms;
+  const int64_t split_from = (tail > 0 && 2 * tail <= sms) ? items - tail : items;
+  const int64_t n_split = 2 * (items - split_from);
+  if (split_from > 0x7fffffff || n_split > 0x7fffffff) return BCA_ERR_UNSUPPORTED;
+  p.decode_pairs_per_seq = pps;
+  p.decode_split_from = static_cast<int>(split_from);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attn_fwd_kernel<true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_kernel<true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess)
+      return BCA_ERR_CUDA;
+    attr_set = true;
+  }
+  if (split_from > 0) {
+    const dim3 grid(static_cast<unsigned>(split_from), 1, 1);
+    attn_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+    if (cudaGetLastError() != cudaSuccess) return BCA_ERR_CUDA;
+  }
+  if (n_split > 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(n_split), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = split_from > 0 ? 1 : 0;
+    if (cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true, true>, tq, tk, tv, tk2, tv2, p) !=
+        cudaSuccess)
+      return BCA_ERR_CUDA;
+  }
+  const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
 }
 

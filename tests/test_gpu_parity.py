@@ -207,6 +207,7 @@ def test_decode_tiny():
     (61, [24, 0, 300, 129], [16, 200, 1, 256]),
     (62, [1000], [130]),
     (63, [128, 256], [128, 384]),
+    (64, [0, 5, 0], [100, 3, 128]),   # a single key tile: nothing to split
 ])
 def test_decode_ragged(seed, pre, tgt):
     H = 3
