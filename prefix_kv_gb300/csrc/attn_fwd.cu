@@ -102,6 +102,7 @@ struct FwdParams {
   const int32_t* cu_prefix;
   const int32_t* page_table;  // decode, paged cache: page of prefix tile j of sequence b
   int max_pages;              //   at page_table[b * max_pages + j]; null: contiguous
+  int head_groups;            // prefill: grid z = sequence * head_groups + group
   int decode_pairs_per_seq;   // decode: tile pairs per sequence (grid decoding)
   int decode_split_from;      // decode: first item split into single-tile items
   __nv_bfloat16* out;
@@ -703,8 +704,11 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   }
 }
 
-// Prefill: a 3-D grid of (head, tile pair, sequence), costliest pairs first.
-// Decode: a 1-D list of equal-cost tile pairs; the pairs of a last, partly
+// Prefill: a 3-D grid of (head in group, tile pair, sequence x head group): the
+// pairs of a group of heads, costliest first, then the next group, so that the
+// CTAs in flight share the K/V of a few heads in L2.
+// Decode: a 1-D list of equal-cost tile pairs, the pairs of one head next to
+// each other (they stream the same K/V tiles); the pairs of a last, partly
 // filled wave become single-tile items (kSplit: two CTAs per pair, each with its
 // key range split between the two softmax warpgroups), launched as a second
 // grid that may start as soon as every pair CTA has started.
@@ -719,22 +723,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   if constexpr (!kDecode) {
-    attn_item<false, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, blockIdx.x, blockIdx.z,
+    const int h = blockIdx.x + (blockIdx.z % p.head_groups) * gridDim.x;   // groups are full
+    attn_item<false, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, h, blockIdx.z / p.head_groups,
                             2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y)),
                             2);
   } else if constexpr (!kSplit) {
     grid_launch_dependents();
     const int L = blockIdx.x;
-    const int rest = L / p.num_heads;
-    attn_item<true, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, L % p.num_heads,
-                           rest / p.decode_pairs_per_seq, 2 * (rest % p.decode_pairs_per_seq), 2);
+    const int rest = L / p.decode_pairs_per_seq;
+    attn_item<true, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, rest % p.num_heads,
+                           rest / p.num_heads, 2 * (L % p.decode_pairs_per_seq), 2);
   } else {
     const int item = p.decode_split_from + static_cast<int>(blockIdx.x) / 2;
     const int sub = blockIdx.x & 1;
-    const int rest = item / p.num_heads;
-    attn_item<true, true>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, item % p.num_heads,
-                          rest / p.decode_pairs_per_seq,
-                          2 * (rest % p.decode_pairs_per_seq) + sub, 2);
+    const int rest = item / p.decode_pairs_per_seq;
+    attn_item<true, true>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, rest % p.num_heads,
+                          rest / p.num_heads, 2 * (item % p.decode_pairs_per_seq) + sub, 2);
     // This grid may run beside the pair grid launched before it: do not
     // complete before that grid has, so work queued after both sees its output.
     grid_dependency_wait();
@@ -832,7 +836,23 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
         return BCA_ERR_CUDA;
       attr_set = true;
     }
-    const dim3 grid(a.num_heads, (a.tiles_per_seq + 1) / 2, a.batch);
+    // Groups of 8 heads (about 50 MB of K/V at 12.5k keys, well inside L2), else
+    // of the largest divisor of the head count down to 4, else one group: every
+    // group is full, so the kernel needs no bound check (which measured slower).
+    int per_group = a.num_heads;
+    for (int d = 8; d >= 4; --d) {
+      if (a.num_heads > d && a.num_heads % d == 0) {
+        per_group = d;
+        break;
+      }
+    }
+    int groups = a.num_heads / per_group;
+    if (static_cast<int64_t>(a.batch) * groups > 65535) {
+      per_group = a.num_heads;
+      groups = 1;
+    }
+    p.head_groups = groups;
+    const dim3 grid(per_group, (a.tiles_per_seq + 1) / 2, a.batch * groups);
     attn_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;

@@ -125,6 +125,14 @@ def test_prefill_ragged_varlen(seed, kv, ql):
     assert_close(out, lse, *case.reference(), what=f"ragged{seed}")
 
 
+@pytest.mark.parametrize("heads", [12, 16, 20])
+def test_prefill_head_groups(heads):
+    # the grid runs the heads in groups (6 x 2, 8 x 2, 5 x 4 here): every head's rows
+    case = ragged_case(30 + heads, [700, 260], heads=heads)
+    out, lse = case.run()
+    assert_close(out, lse, *case.reference(), what=f"heads{heads}")
+
+
 def test_prefill_adjacent_spans_and_many_runs():
     case = ragged_case(21, [1200, 333], max_spans=40, max_span=40)
     out, lse = case.run()
