@@ -198,6 +198,9 @@ bca_status bca_prefill_piecewise(const void* q, const void* k, const void* v,
  * is cache tokens cu_prefix[b] .. cu_prefix[b+1]-1 of layer `layer`;
  * cu_prefix: device int32 [batch+1]; out/lse as in bca_prefill.
  * max_prefix bounds cu_prefix[b+1]-cu_prefix[b].
+ * Launches one or two kernels on `stream`: the query-tile pairs, and, when
+ * they would leave a last wave at most half full, that wave's pairs as
+ * key-split single tiles in a second grid that may start as the first drains.
  */
 bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void* cache_v,
                              int32_t layer, int32_t num_layers, int64_t capacity,

@@ -234,7 +234,8 @@ def test_decode_ragged(seed, pre, tgt):
     assert_close(out, lse, *case.reference(), what=f"decode{seed}")
 
 
-@pytest.mark.parametrize("wl,heads", [(W.t2i_1024(), [1, 30]), (W.edit_two_ref(), [2, 17])],
+# heads 28-31 hold the last 56 tile pairs, which run as the key-split tail grid
+@pytest.mark.parametrize("wl,heads", [(W.t2i_1024(), [1, 30]), (W.edit_two_ref(), [2, 17, 31])],
                          ids=lambda x: getattr(x, "name", ""))
 def test_decode_full_size(wl, heads):
     case = DecodeCase.from_workload(wl)
