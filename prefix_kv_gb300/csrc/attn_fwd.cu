@@ -485,7 +485,10 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     const int wq = warp & 3;                // TMEM lane group
     const int row = wq * 32 + lane;         // == TMEM lane == row within the tile
     const int n_tiles = nkt[qi];
-    const int koff = qi == 1 ? koff1 : 0;   // global index of this warpgroup's first key tile
+    // decode: this warpgroup's key tiles, counted from its first one (koff1 for
+    // warpgroup 1 of a key-split item): prefix tiles before tgt0, keys left in the prefix
+    const int tgt0 = n_pre_tiles - (qi == 1 ? koff1 : 0);
+    const int pre_left0 = n_pre - (qi == 1 ? koff1 : 0) * kBlockN;
     const int row0 = q_seq0 + (m_base + (kSplit ? 0 : qi)) * kBlockM;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_addr = lane_addr + kColS + qi * 128;
@@ -521,8 +524,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
         lim = e_row - j * kBlockN;
         need_mask = (j + 1) * kBlockN > k_min[qi];
       } else {
-        const int g = koff + j;
-        lim = g < n_pre_tiles ? n_pre - g * kBlockN : q_len - (g - n_pre_tiles) * kBlockN;
+        lim = j < tgt0 ? pre_left0 - j * kBlockN : q_len - (j - tgt0) * kBlockN;
         need_mask = lim < kBlockN;
       }
       if (need_mask) {
