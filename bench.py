@@ -454,6 +454,47 @@ def oracle_sample(prob: "Problem", step_idx: int, target_s: float = 3.0):
     return fl, t_prefill + t_decode, desc
 
 
+class HostProblem:
+    """The workload's host tensors only (the CPU legs never touch a GPU)."""
+
+    def __init__(self, workload):
+        from prefix_kv_gb300 import workloads as W
+        wl = W.by_name(workload)
+        q, k, v = W.make_qkv(wl)
+        tr = torch.from_numpy(wl.target_rows())
+        pr = torch.from_numpy(wl.prefix_rows())
+        self.wl, self.H, self.S0 = wl, wl.num_heads, wl.seq_lens[0]
+        self.N0, self.P0 = wl.target_lens()[0], wl.prefix_lens()[0]
+        self.scale = 1.0 / math.sqrt(128)
+        self.host = {"q": q, "k": k, "v": v, "q_tgt": q[tr].contiguous(),
+                     "k_tgt": k[tr].contiguous(), "v_tgt": v[tr].contiguous(),
+                     "k_pre": k[pr].contiguous(), "v_pre": v[pr].contiguous()}
+
+
+def host_problem(workload):
+    return HostProblem(workload)
+
+
+def oracle_one_thread(workload, seconds):
+    """The same oracle sample on one host thread: bench.py runs itself with the BLAS and
+    OpenMP thread counts set to 1 (they cannot change once NumPy is loaded)."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS",
+                "NUMEXPR_NUM_THREADS", "VECLIB_MAXIMUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample",
+                            str(seconds), "--workload", workload], env=env,
+                           capture_output=True, text=True, timeout=30 * seconds + 120)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+        return {"value": round(d["flops"] / d["seconds"] / 1e12, 6), "unit": UNIT,
+                "cores": d["threads"], "seconds": round(d["seconds"], 2),
+                "sample": d["sample"]}
+    except (subprocess.SubprocessError, ValueError, KeyError, IndexError) as e:
+        return {"unavailable": f"{type(e).__name__}: {e}"[:200]}
+
+
 def cpu_threads():
     try:
         import threadpoolctl
@@ -463,7 +504,11 @@ def cpu_threads():
             return int(n[0])
     except Exception:
         pass
-    return os.cpu_count() or 1
+    # without threadpoolctl: the thread-count variables BLAS and OpenMP honour, if set
+    limits = [int(os.environ[v]) for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS",
+                                           "MKL_NUM_THREADS")
+              if os.environ.get(v, "").isdigit() and int(os.environ[v]) > 0]
+    return min(limits) if limits else (os.cpu_count() or 1)
 
 
 # ----------------------------------------------------------------------------- main
@@ -489,7 +534,16 @@ def main():
                          "before prefill and decode")
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8-v", "fp8-kv"],
                     help="prefix cache format: bf16, or E4M3 with V / K and V quantised")
+    ap.add_argument("--oracle-sample", type=float, default=None, metavar="SECONDS",
+                    help="internal: time one oracle sample on the host, print it as JSON "
+                         "and exit (how the one-thread CPU baseline is taken)")
     args = ap.parse_args()
+
+    if args.oracle_sample is not None:
+        fl, secs, desc = oracle_sample(host_problem(args.workload), 0, target_s=args.oracle_sample)
+        print(json.dumps({"flops": fl, "seconds": secs, "threads": cpu_threads(),
+                          "sample": desc}), flush=True)
+        return
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -637,7 +691,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         fl, secs, desc = oracle_sample(prob, 0, target_s=args.cpu_seconds)
         cpu = {"value": round(fl / secs / 1e12, 6), "unit": UNIT, "cores": cpu_threads(),
-               "kind": "oracle", "sample": desc, "seconds": round(secs, 2)}
+               "kind": "oracle", "sample": desc, "seconds": round(secs, 2),
+               "one_thread": oracle_one_thread(prob.wl.name, args.cpu_seconds / 2)}
 
     if rank != 0:
         if dist is not None:
@@ -700,21 +755,8 @@ def run_reference(args, rank, world, peaks):
     """The oracle as it stands on the host cores, each step a bounded sample."""
     if rank != 0:
         return
-    # the host-side problem only: this leg never touches a GPU
-    from prefix_kv_gb300 import workloads as W
-
-    class HostProblem:
-        pass
-    hp = HostProblem()
-    wl = W.by_name(args.workload)
-    q, k, v = W.make_qkv(wl)
-    tr = torch.from_numpy(wl.target_rows())
-    pr = torch.from_numpy(wl.prefix_rows())
-    hp.wl, hp.H, hp.S0 = wl, wl.num_heads, wl.seq_lens[0]
-    hp.N0, hp.P0, hp.scale = wl.target_lens()[0], wl.prefix_lens()[0], 1.0 / math.sqrt(128)
-    hp.host = {"q": q, "k": k, "v": v, "q_tgt": q[tr].contiguous(), "k_tgt": k[tr].contiguous(),
-               "v_tgt": v[tr].contiguous(), "k_pre": k[pr].contiguous(),
-               "v_pre": v[pr].contiguous()}
+    hp = host_problem(args.workload)   # this leg never touches a GPU
+    wl = hp.wl
     for i in range(args.warmup):
         oracle_sample(hp, i, target_s=1.0)
     fl_tot, s_tot, desc = 0.0, 0.0, ""
