@@ -234,6 +234,30 @@ def test_decode_ragged(seed, pre, tgt):
     assert_close(out, lse, *case.reference(), what=f"decode{seed}")
 
 
+def test_decode_pair_grid_and_tail_ragged():
+    # 8 heads x 5 sequences x 4 pairs = 160 items on a 152-SM GB300: 152 run in the pair
+    # grid and 8 as 16 key-split tail CTAs; ragged lengths leave some pairs half or wholly
+    # empty, and one sequence has no prefix
+    H = 8
+    pre, tgt = [900, 0, 333, 1500, 128], [1000, 700, 1024, 5, 257]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    items = H * 4 * len(tgt)
+    if not (items > sms and 0 < items % sms <= sms // 2):
+        pytest.skip(f"{sms} SMs: this shape does not give both decode grids")
+    kp = W.randn_bf16((sum(pre), H, 128), 81)
+    vp = W.randn_bf16((sum(pre), H, 128), 82)
+    qt = W.randn_bf16((sum(tgt), H, 128), 83)
+    kt = W.randn_bf16((sum(tgt), H, 128), 84)
+    vt = W.randn_bf16((sum(tgt), H, 128), 85)
+    cu_p = np.concatenate([[0], np.cumsum(pre)])
+    cu_q = np.concatenate([[0], np.cumsum(tgt)])
+    case = DecodeCase(qt, kt, vt, kp, vp, cu_q, cu_p, layers=1, layer=0, cache_fill=float("nan"))
+    st = _status()
+    out, lse = case.run(status=st)
+    assert bca.read_status(st) == 0
+    assert_close(out, lse, *case.reference(), what="pairs+tail")
+
+
 # heads 28-31 hold the last 56 tile pairs, which run as the key-split tail grid
 @pytest.mark.parametrize("wl,heads", [(W.t2i_1024(), [1, 30]), (W.edit_two_ref(), [2, 17, 31])],
                          ids=lambda x: getattr(x, "name", ""))
