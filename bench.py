@@ -176,6 +176,7 @@ class Problem:
     """The workload's tensors, resident on the device (plus pinned host copies for e2e)."""
 
     def __init__(self, dev, with_host=True, cache="bf16", prologue=False, piecewise=False,
+                 separate_append=False,
                  paged=False, workload=WORKLOAD):
         from prefix_kv_gb300 import flops
         from prefix_kv_gb300 import workloads as W
@@ -276,6 +277,12 @@ class Problem:
             n_pieces = sum(int(np.count_nonzero(np.diff(self.bid_host[a:e]))) + 1
                            for a, e in zip(self.cu_host[:-1], self.cu_host[1:]) if e > a)
             self.launches += 2 * n_pieces - 2
+        # the bf16 contiguous cache is written by the prefill launch itself
+        # (bca_prefill_append) unless the two separate calls are asked for
+        self.fused = (self.decode and self.fp8_mode is None and not paged and not piecewise
+                      and not prologue and not separate_append)
+        if self.fused:
+            self.launches -= 1
         # named segments of the step, between consecutive CUDA events
         self.segments = (["prologue", "prefill", "target_prologue", "decode"] if prologue
                          else ["prefill", "append", "decode"])
@@ -315,6 +322,11 @@ class Problem:
             bca.prefill_piecewise(d["q"], d["k"], d["v"], d["block_id"], self.bid_host,
                                   self.cu_host, self.scale, out=self.out, lse=self.lse,
                                   workspace=self.pw_ws, status=self.status)
+        elif self.fused:
+            bca.prefill_append(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"],
+                               self.max_s, self.max_s, d["cu_pre"], self.cache_k, self.cache_v,
+                               0, self.scale, out=self.out, lse=self.lse, workspace=self.ws,
+                               status=self.status)
         else:
             bca.prefill(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"], self.max_s,
                         self.max_s, self.scale, out=self.out, lse=self.lse, workspace=self.ws,
@@ -326,7 +338,9 @@ class Problem:
                 events[2].record()
                 events[3].record()
             return
-        if self.paged:
+        if self.fused:
+            pass                       # written by the prefill launch
+        elif self.paged:
             bca.prefix_cache_append_paged(d["k"], d["v"], d["cu"], d["cu_pre"], self.page_table,
                                           self.cache_k, self.cache_v, 0, status=self.status)
         elif self.fp8_mode is None:
@@ -355,6 +369,26 @@ class Problem:
                                   status=self.status)
         if events:
             events[3].record()
+
+
+def time_standalone_append(prob: "Problem", flush, n: int = 10) -> float:
+    """Median ms of bca_prefix_cache_append on the step's inputs.  L2 is emptied before each
+    launch by reading a buffer larger than it: a read leaves clean lines, where a write
+    would leave dirty ones whose write-back competes with the copy being timed."""
+    import prefix_kv_gb300 as bca
+    d = prob.dev
+    ts = []
+    for i in range(n + 2):
+        flush.max()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], prob.cache_k, prob.cache_v,
+                                0, status=prob.status)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= 2:
+            ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
 
 
 def fp8_decode_psnr(prob: "Problem", dev) -> float:
@@ -534,6 +568,9 @@ def main():
                          "before prefill and decode")
     ap.add_argument("--cache", default="bf16", choices=["bf16", "fp8-v", "fp8-kv"],
                     help="prefix cache format: bf16, or E4M3 with V / K and V quantised")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="time the cache append as its own launch instead of fused into the "
+                         "prefill (bf16 contiguous cache)")
     ap.add_argument("--oracle-sample", type=float, default=None, metavar="SECONDS",
                     help="internal: time one oracle sample on the host, print it as JSON "
                          "and exit (how the one-thread CPU baseline is taken)")
@@ -569,7 +606,8 @@ def main():
 
     import prefix_kv_gb300 as bca
     prob = Problem(dev, with_host=not args.no_e2e, cache=args.cache, prologue=args.prologue,
-                   piecewise=args.piecewise, paged=args.paged, workload=args.workload)
+                   piecewise=args.piecewise, paged=args.paged, workload=args.workload,
+                   separate_append=args.separate_append)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
@@ -610,6 +648,11 @@ def main():
     if prob.prologue:
         s_app = seg["prologue"] + seg["target_prologue"]
         app_gbs = prob.prologue_bytes / (s_app / K * 1e-3) / 1e9
+    elif prob.fused:
+        # the step writes the cache inside the prefill launch; the standalone append
+        # kernel is timed on its own (L2 flushed before each launch) for its HBM row
+        s_app = K * time_standalone_append(prob, flush)
+        app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9
     else:
         s_app = seg["append"]
         app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9 if prob.decode else 0.0
@@ -723,6 +766,8 @@ def main():
                             "prefill, target Q/K norm + RoPE, prefix decode") if prob.prologue
                            else ("piecewise prefill (schedule prep + attention + lse copy per "
                                  "segment) + cache append + prefix decode") if prob.piecewise
+                           else ("schedule prep + prefill with the cache append in the same "
+                                 "launch + prefix decode") if prob.fused
                            else "schedule prep + prefill + cache append + prefix decode",
                    "prefix_cache_pages": ("128-token pages, shuffled page table" if prob.paged
                                           else "contiguous"),
@@ -738,7 +783,12 @@ def main():
                       ("prologue_frac_of_hbm" if prob.prologue else "append_frac_of_hbm"):
                           round(app_gbs / peaks["hbm"], 4),
                       "decode_ms": round(s_dec / K, 4), "decode_tflops": round(dec_tf, 2),
-                      "decode_frac": round(dec_tf / peaks["bf16"], 4)},
+                      "decode_frac": round(dec_tf / peaks["bf16"], 4),
+                      **({"append_in_step": "inside the prefill launch (bca_prefill_append); "
+                                            "append_* time the standalone kernel on the same "
+                                            "inputs, median of 10 launches, L2 emptied by a "
+                                            "256 MiB read before each"}
+                         if prob.fused else {})},
         "fp8_decode_psnr_db_vs_bf16_cache": psnr,
         "roofline": roofline,
         "cpu_baseline": cpu,

@@ -30,6 +30,8 @@
  *   "NEO-Unify 多模态 Prefill 的注意力" (per-M-block K-range extension).
  *
  * Beyond the prefill / decode / append path, the same library carries:
+ *   - the prefill with the cache append fused in (one launch fewer):
+ *     bca_prefill_append;
  *   - an FP8 E4M3 prefix cache with one fp32 scale per (token, head)
  *     (deployment notes, prefix-cache section): bca_prefix_cache_append_fp8,
  *     bca_prefix_cache_dequant_fp8, bca_prefix_decode_fp8;
@@ -138,6 +140,29 @@ bca_status bca_prefill(const void* q, const void* k, const void* v, const int32_
                        int32_t max_seqlen_k, float softmax_scale, void* out, float* lse,
                        void* workspace, size_t workspace_bytes, int32_t* status_dev,
                        void* stream);
+
+/* Prefill with the prefix cache append fused in: bca_prefill, and the cache
+ * rows bca_prefix_cache_append would write (same arguments and layout:
+ * cu_prefix device int32 [batch+1], cache_k/v device bf16
+ * [num_layers][H][capacity][128], layer `layer`), written from the key and
+ * value tiles the attention already reads (flozi.net "Timestep-zero
+ * conditioning makes the prefix invariant": the first step clones the
+ * post-RoPE prefix K/V into the cache).  One launch fewer than the two calls.
+ * Errors as in the two calls: nothing is written to the cache when a prefix is
+ * longer than its keys or a sequence with a prefix has no query rows
+ * (BCA_ERR_SEQLENS), or cu_prefix[batch] > capacity (BCA_ERR_CAPACITY); a
+ * sequence that fails block-id validation gets neither output nor cache rows.
+ * With batch == 0 or total_q == 0 nothing is launched and nothing is written.
+ */
+bca_status bca_prefill_append(const void* q, const void* k, const void* v,
+                              const int32_t* block_id, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_k, int32_t batch, int32_t num_heads,
+                              int32_t head_dim, int32_t total_q, int32_t total_k,
+                              int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                              void* out, float* lse, void* workspace, size_t workspace_bytes,
+                              const int32_t* cu_prefix, void* cache_k, void* cache_v,
+                              int32_t layer, int32_t num_layers, int64_t capacity,
+                              int32_t* status_dev, void* stream);
 
 /* Same computation as bca_prefill, for callers that cannot allocate device
  * memory or pass a workspace: for example a plugin inside a runtime that owns

@@ -115,6 +115,54 @@ def prefill(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
     return out, lse
 
 
+def prefill_append(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
+                   max_seqlen_k: int, cu_prefix, cache_k, cache_v, layer: int,
+                   softmax_scale: Optional[float] = None, out=None, lse=None, workspace=None,
+                   status=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """``prefill`` with ``prefix_cache_append`` fused in: returns ``(out, lse)`` and writes the
+    first ``cu_prefix[b+1]-cu_prefix[b]`` keys/values of every sequence into cache tokens
+    ``cu_prefix[b]..`` of ``layer`` (cache ``[L, H, capacity, 128]`` bf16)."""
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _need(t, name, torch.bfloat16, 3)
+    _need(block_id, "block_id", torch.int32, 1)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    _need(cu_prefix, "cu_prefix", torch.int32, 1)
+    _need(cache_k, "cache_k", torch.bfloat16, 4)
+    _need(cache_v, "cache_v", torch.bfloat16, 4)
+    total_q, H, D = q.shape
+    total_k = k.shape[0]
+    if k.shape != (total_k, H, D) or v.shape != k.shape or block_id.numel() != total_k:
+        raise ValueError("k, v, block_id shapes do not match")
+    L, Hc, cap, Dc = cache_k.shape
+    if cache_v.shape != cache_k.shape or Hc != H or Dc != D:
+        raise ValueError("cache shape does not match q/k/v")
+    if not 0 <= layer < L:
+        raise ValueError(f"layer {layer} outside [0, {L})")
+    batch = cu_seqlens_q.numel() - 1
+    if cu_prefix.numel() != batch + 1 or cu_seqlens_k.numel() != batch + 1:
+        raise ValueError("cu_prefix / cu_seqlens_k must have batch + 1 entries")
+    if softmax_scale is None:
+        softmax_scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((H, total_q), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, 3)
+    _need(lse, "lse", torch.float32, 2)
+    ws_bytes = prefill_workspace_bytes(batch, total_q, max_seqlen_q)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    code = _native.load().bca_prefill_append(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(block_id), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
+        batch, H, D, total_q, total_k, max_seqlen_q, max_seqlen_k, float(softmax_scale),
+        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(cu_prefix), _ptr(cache_k), _ptr(cache_v), layer, L, cap, _ptr(status),
+        _stream(stream))
+    _native.check(code, "bca_prefill_append")
+    return out, lse
+
+
 def prefix_decode(q_tgt, cache_k, cache_v, layer: int, cu_prefix, k_tgt, v_tgt, cu_seqlens_q,
                   max_seqlen_q: int, max_prefix: int, softmax_scale: Optional[float] = None,
                   out=None, lse=None, status=None, stream=None):

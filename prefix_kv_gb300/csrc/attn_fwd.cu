@@ -40,7 +40,8 @@
 //   warp 8     TMEM allocator and MMA issuer
 //   warp 9     TMA producer (Q0, Q1 once, then K_j, V_j into a ring of smem stages)
 //   warp 10    V tail fix-up (zeroes V rows past the end of a key segment)
-//   warp 11    idle
+//   warp 11    prefix store (prefill with cache append: the CTA of each sequence's
+//              last tile pair writes the prefix K/V tiles to the cache), else idle
 // Launched at 168 registers per thread; the softmax warpgroups raise theirs to
 // 208 and the control warpgroup drops to 88 (2*128*208 + 128*88 = 384*168).
 // TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_i is
@@ -63,6 +64,7 @@ static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsControl == kThreads * kRegsLau
 constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;
 constexpr int kWarpFix = 10;
+constexpr int kWarpStore = 11;   // prefill with cache append: stores the prefix tiles
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -103,6 +105,9 @@ struct FwdParams {
   const int32_t* page_table;  // decode, paged cache: page of prefix tile j of sequence b
   int max_pages;              //   at page_table[b * max_pages + j]; null: contiguous
   int head_groups;            // prefill: grid z = sequence * head_groups + group
+  int batch;
+  __nv_bfloat16* cache_k;     // prefill with cache append: one layer [H][capacity][128], else null
+  __nv_bfloat16* cache_v;
   int decode_pairs_per_seq;   // decode: tile pairs per sequence (grid decoding)
   int decode_split_from;      // decode: first item split into single-tile items
   __nv_bfloat16* out;
@@ -200,6 +205,11 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   if (!kSplit && nkt[1] > 0 && nkt[1] < nkt[0]) nkt[1] = nkt[0];
   const int nk = max(nkt[0], nkt[1]);
   const int k_hi_all = max(k_hi[0], k_hi[1]);
+  // Prefill with cache append: the CTA of a sequence's last tile pair reads every key
+  // tile of the sequence (its last row sees them all), and its store warp writes the
+  // prefix ones to the cache; the stages it stores are released by that warp too.
+  const bool appender = !kDecode && p.cache_k != nullptr &&
+                        m_base == 2 * (((q_len + kBlockM - 1) / kBlockM - 1) / 2);
   const int koff1 = kSplit ? nkt[0] : 0;                  // first key tile of warpgroup 1
   const int n_kv_tiles = kSplit ? nkt[0] + nkt[1] : nk;   // distinct K/V tiles of the item
   // valid keys left in K/V tile j's segment (>= 128: the tile is full)
@@ -216,7 +226,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     mbar_init(&sm.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.kv_full[s], 1);
-      mbar_init(&sm.kv_empty[s], 1);
+      mbar_init(&sm.kv_empty[s], appender ? 2 : 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.s_full[i], 1);
@@ -477,6 +487,62 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.v_fixed);
     }
+   } else if (warp == kWarpStore && appender) {
+    // ============ prefix store (prefill with cache append) ============
+    // Every sequence is checked first and nothing is written if one fails, as
+    // in the standalone append: a prefix longer than its keys (or with no query
+    // row to carry it), a negative offset, or the prefixes past the capacity.
+    int bad = 0;
+    for (int i = lane; i < p.batch; i += 32) {
+      const int pl = p.cu_prefix[i + 1] - p.cu_prefix[i];
+      const int kl = p.cu_k[i + 1] - p.cu_k[i];
+      const int ql = p.cu_q[i + 1] - p.cu_q[i];
+      if (pl < 0 || pl > kl || p.cu_prefix[i] < 0 || (pl > 0 && ql == 0)) bad = BCA_ERR_SEQLENS;
+    }
+    if (lane == 0 && static_cast<int64_t>(p.cu_prefix[p.batch]) > p.capacity)
+      bad = bad != 0 ? bad : BCA_ERR_CAPACITY;
+    bad = __reduce_max_sync(0xffffffffu, bad);
+    if (bad != 0 && lane == 0 && h == 0) report_status(p.status, bad);
+    const int c0 = p.cu_prefix[b];
+    const int n_pre_b = bad == 0 ? p.cu_prefix[b + 1] - c0 : 0;
+    // Follow the ring in load order (K_j = 2j, V_j = 2j + 1): once a tile has
+    // landed, store its prefix rows, then hand the stage back (the producer
+    // waits for this arrival as well as the softmax's).
+    for (int i = 0; i < 2 * nk; ++i) {
+      const int s = stage_of(i);
+      if (!warp_wait(&sm.kv_full[s], phase_of(i), abort_flag)) {
+        if (lane == 0) give_up();
+        break;
+      }
+      const int j = i >> 1;
+      const bool is_v = i & 1;
+      const int rows = min(kBlockN, n_pre_b - j * kBlockN);   // prefix rows in the tile
+      if (rows == kBlockN) {
+        // a whole tile: two TMA stores through the cache map (same 128-byte swizzled
+        // layout as the loads), read out of shared memory before the stage is freed
+        if (lane == 0) {
+          const CUtensorMap* m = is_v ? &tm_v2 : &tm_k2;
+          tma_store_3d(m, sm.kv[s], 0, c0 + j * kBlockN, h);
+          tma_store_3d(m, sm.kv[s] + kHalfBytes, 64, c0 + j * kBlockN, h);
+          bulk_commit_group();
+          bulk_wait_read_all();
+        }
+      } else if (rows > 0) {
+        // the prefix ends inside the tile: copy its rows with 16-byte accesses,
+        // undoing the swizzle (chunk c of row r sits at chunk c ^ (r % 8))
+        __nv_bfloat16* dst = (is_v ? p.cache_v : p.cache_k) +
+                             (static_cast<int64_t>(h) * p.capacity + c0 + j * kBlockN) * kHeadDim;
+        for (int idx = lane; idx < rows * 16; idx += 32) {
+          const int r = idx >> 4, c = idx & 15;
+          const uint4 val = *reinterpret_cast<const uint4*>(
+              sm.kv[s] + (c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) * 16));
+          *reinterpret_cast<uint4*>(dst + static_cast<int64_t>(r) * kHeadDim + c * 8) = val;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.kv_empty[s]);
+    }
+    if (lane == 0) bulk_wait_all();   // the stores are complete before the CTA ends
    }
   } else {
     regs_increase<kRegsSoftmax>();
@@ -801,8 +867,14 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   if (!decode) {
     ok = ok && encode_packed(&tk, a.k, a.num_heads, a.total_k) &&
          encode_packed(&tv, a.v, a.num_heads, a.total_k);
-    tk2 = tk;
-    tv2 = tv;
+    if (a.cache_k != nullptr) {   // cache append: the store maps over one cache layer
+      const int64_t map_cap = a.capacity > 0 ? a.capacity : 1;
+      ok = ok && encode_cache(&tk2, a.cache_k, a.num_heads, map_cap) &&
+           encode_cache(&tv2, a.cache_v, a.num_heads, map_cap);
+    } else {
+      tk2 = tk;
+      tv2 = tv;
+    }
   } else {
     const int64_t map_cap = a.capacity > 0 ? a.capacity : 1;
     ok = ok && encode_cache(&tk, a.k, a.num_heads, map_cap) &&
@@ -825,6 +897,9 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   p.cu_prefix = a.cu_prefix;
   p.page_table = a.page_table;
   p.max_pages = a.max_pages;
+  p.batch = a.batch;
+  p.cache_k = static_cast<__nv_bfloat16*>(a.cache_k);
+  p.cache_v = static_cast<__nv_bfloat16*>(a.cache_v);
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.status = a.status;

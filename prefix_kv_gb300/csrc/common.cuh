@@ -52,6 +52,8 @@ struct AttnLaunch {
   const int32_t* cu_prefix;
   const int32_t* page_table;   // decode over a paged cache: [batch][max_pages], else null
   int max_pages;
+  void* cache_k;               // prefill with cache append: layer base [H][capacity][128], else null
+  void* cache_v;
   int32_t* status;
 };
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream);  // returns bca_status

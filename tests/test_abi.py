@@ -81,6 +81,31 @@ def test_prefill_host_validation(lib):
     assert _prefill(lib, tk=0) == 8
 
 
+def _prefill_append(lib, **kw):
+    a = dict(q=16, k=16, v=16, bid=16, cq=16, ck=16, batch=1, H=2, D=128, tq=8, tk=8, mq=8,
+             mk=8, scale=0.1, out=16, lse=16, ws=16, wsb=1 << 20, cp=16, cck=16, ccv=16,
+             layer=0, L=1, cap=64, status=None, stream=None)
+    a.update(kw)
+    return lib.bca_prefill_append(a["q"], a["k"], a["v"], a["bid"], a["cq"], a["ck"], a["batch"],
+                                  a["H"], a["D"], a["tq"], a["tk"], a["mq"], a["mk"], a["scale"],
+                                  a["out"], a["lse"], a["ws"], a["wsb"], a["cp"], a["cck"],
+                                  a["ccv"], a["layer"], a["L"], a["cap"], a["status"],
+                                  a["stream"])
+
+
+def test_prefill_append_host_validation(lib):
+    assert _prefill_append(lib, D=64) == 2               # UNSUPPORTED head dim
+    assert _prefill_append(lib, layer=1, L=1) == 1       # layer outside the cache
+    assert _prefill_append(lib, layer=-1) == 1
+    assert _prefill_append(lib, cap=-1) == 1
+    assert _prefill_append(lib, cck=None) == 1           # cache missing
+    assert _prefill_append(lib, cp=None) == 1
+    assert _prefill_append(lib, ccv=24) == 1             # misaligned cache
+    assert _prefill_append(lib, scale=0.0) == 1          # the prefill's own checks follow
+    assert _prefill_append(lib, ws=None) == 4
+    assert _prefill_append(lib, tq=0) == 0               # nothing to do
+
+
 def test_decode_and_append_host_validation(lib):
     dec = lib.bca_prefix_decode
     #         q   ck  cv  layer L  cap  cup tk  tv  cq  B  H  D    tq mq mp scale out lse st  s
