@@ -255,38 +255,59 @@ __global__ void __launch_bounds__(256)
   const int64_t rows = static_cast<int64_t>(cu_prefix[batch] - p0) * num_heads;
   const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
   const int lane16 = threadIdx.x & 15;
-  // two rows per warp (16 lanes each); all 32 lanes stay together for the shuffles
-  for (int64_t r2 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       r2 * 2 < rows; r2 += warps) {
-    const int64_t row = r2 * 2 + ((threadIdx.x >> 4) & 1);
-    const bool live = row < rows;
-    const int64_t rr = live ? row : rows - 1;
-    const int c = static_cast<int>(rr / num_heads) + p0;       // cache token
-    const int hh = static_cast<int>(rr % num_heads);
+  // Row (token, head) of the prefix region -> source vector and cache row.
+  struct Where {
+    int64_t src, dst_row;
+  };
+  auto locate = [&](int64_t row) {
+    const int c = static_cast<int>(row / num_heads) + p0;       // cache token
+    const int hh = static_cast<int>(row % num_heads);
     int lo = 0, hi = batch - 1;                                  // sequence of c
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (cu_prefix[mid] <= c) lo = mid; else hi = mid - 1;
     }
     const int64_t src_tok = static_cast<int64_t>(cu_k[lo]) + (c - cu_prefix[lo]);
-    const int64_t src = (src_tok * num_heads + hh) * 16 + lane16;
-    const int64_t dst_row = static_cast<int64_t>(hh) * capacity +
-                            cache_token(page_table, max_pages, cu_prefix, lo, c - cu_prefix[lo]);
-    float scale_v, scale_k;
-    const uint2 qv = quantize8(__ldcs(v + src), &scale_v);
-    if (live) {
-      cv[dst_row * 16 + lane16] = qv;
-      if (lane16 == 0) sv[dst_row] = scale_v;
+    return Where{(src_tok * num_heads + hh) * 16 + lane16,
+                 static_cast<int64_t>(hh) * capacity +
+                     cache_token(page_table, max_pages, cu_prefix, lo, c - cu_prefix[lo])};
+  };
+  // Two rows per warp (16 lanes each; all 32 lanes stay together for the shuffles)
+  // and two such row pairs per pass, with all four loads issued before any
+  // quantisation so that each lane keeps them in flight together.
+  constexpr int kPairs = 2;
+  for (int64_t r2 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+       r2 * 2 < rows; r2 += kPairs * warps) {
+    bool live[kPairs];
+    int64_t src[kPairs], dst_row[kPairs];
+    uint4 vraw[kPairs], kraw[kPairs];
+#pragma unroll
+    for (int u = 0; u < kPairs; ++u) {
+      const int64_t row = (r2 + u * warps) * 2 + ((threadIdx.x >> 4) & 1);
+      live[u] = row < rows;
+      const Where w = locate(live[u] ? row : rows - 1);
+      src[u] = w.src;
+      dst_row[u] = w.dst_row;
+      vraw[u] = __ldcs(v + src[u]);
+      kraw[u] = __ldcs(k + src[u]);
     }
-    const uint4 kraw = __ldcs(k + src);
-    if constexpr (kQuantK) {
-      const uint2 qk = quantize8(kraw, &scale_k);
-      if (live) {
-        static_cast<uint2*>(ck)[dst_row * 16 + lane16] = qk;
-        if (lane16 == 0) sk[dst_row] = scale_k;
+#pragma unroll
+    for (int u = 0; u < kPairs; ++u) {
+      float scale_v, scale_k;
+      const uint2 qv = quantize8(vraw[u], &scale_v);
+      if (live[u]) {
+        cv[dst_row[u] * 16 + lane16] = qv;
+        if (lane16 == 0) sv[dst_row[u]] = scale_v;
       }
-    } else {
-      if (live) static_cast<uint4*>(ck)[dst_row * 16 + lane16] = kraw;
+      if constexpr (kQuantK) {
+        const uint2 qk = quantize8(kraw[u], &scale_k);
+        if (live[u]) {
+          static_cast<uint2*>(ck)[dst_row[u] * 16 + lane16] = qk;
+          if (lane16 == 0) sk[dst_row[u]] = scale_k;
+        }
+      } else {
+        if (live[u]) static_cast<uint4*>(ck)[dst_row[u] * 16 + lane16] = kraw[u];
+      }
     }
   }
 }
