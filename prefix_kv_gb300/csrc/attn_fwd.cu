@@ -83,6 +83,7 @@ struct FwdSmem {
   uint64_t v_fixed;     // fix-up warp zeroed the tail rows of that V tile
   uint64_t drain;
   uint64_t merge;       // key split: warpgroup 1 published its row maxima and sums
+  uint64_t epi[2];      // query tile i's output rows are staged in q[i] for the TMA store
   uint32_t tmem_base;
   int abort;
   int fix_stage;        // the V tile to fix: its ring stage and first row past the segment
@@ -125,7 +126,8 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 template <bool kDecode, bool kSplit>
 __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const CUtensorMap& tm_k2,
-                                          const CUtensorMap& tm_v2, const FwdParams& p, FwdSmem& sm,
+                                          const CUtensorMap& tm_v2, const CUtensorMap& tm_o,
+                                          const FwdParams& p, FwdSmem& sm,
                                           const int h, const int b, const int m_base,
                                           const int n_qt) {
   static_assert(kDecode || !kSplit, "key split is a decode item");
@@ -237,6 +239,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     mbar_init(&sm.v_fixed, 1);
     mbar_init(&sm.drain, 1);
     mbar_init(&sm.merge, kSoftmaxThreads);
+    for (int i = 0; i < 2; ++i) mbar_init(&sm.epi[i], kSoftmaxThreads);
     sm.abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -737,6 +740,13 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       } else if (n_tiles > 0) {
         tc_fence_after();
         const float inv_l = 1.f / l_run;
+        // A whole tile goes out by TMA: the rows, in bf16, are staged in this tile's
+        // Q buffer (idle: the commit behind o_final covers every MMA that read it)
+        // in the 128-byte swizzled layout of the box, then one thread stores the two
+        // 64-column halves.  (Rows written one per thread, 8 KB apart, cost the
+        // launch ~2%.)  A ragged tile writes its valid rows directly.
+        const bool staged = rows_valid[qi] == kBlockM;
+        uint8_t* const stage = sm.q[qi];
         __nv_bfloat16* orow =
             p.out + (static_cast<size_t>(row0 + row) * p.num_heads + h) * kHeadDim;
 #pragma unroll 1
@@ -748,11 +758,33 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
           for (int x = 0; x < 16; ++x)
             w[x] = pack_bf16x2(__uint_as_float(r[2 * x]) * inv_l,
                                __uint_as_float(r[2 * x + 1]) * inv_l);
-          if (row_valid) {
+          if (staged) {
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const int cc = 4 * c + x;   // 16-byte chunk of the row, 0..15
+              *reinterpret_cast<uint4*>(stage + (cc >> 3) * kHalfBytes + row * 128 +
+                                        (((cc & 7) ^ (row & 7)) * 16)) =
+                  make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+            }
+          } else if (row_valid) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
             for (int x = 0; x < 4; ++x)
               dst[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+          }
+        }
+        if (staged) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(&sm.epi[qi]);
+          if (wq == 0 && lane == 0) {
+            if (mbar_wait(&sm.epi[qi], 0, abort_flag, kWaitLimitNs)) {
+              tma_store_3d(&tm_o, stage, 0, h, row0);
+              tma_store_3d(&tm_o, stage + kHalfBytes, 64, h, row0);
+              bulk_commit_group();
+              bulk_wait_all();   // complete before the CTA ends
+            } else {
+              give_up();
+            }
           }
         }
         if (row_valid) {
@@ -786,26 +818,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v,
                     const __grid_constant__ CUtensorMap tm_k2,
-                    const __grid_constant__ CUtensorMap tm_v2, const FwdParams p) {
+                    const __grid_constant__ CUtensorMap tm_v2,
+                    const __grid_constant__ CUtensorMap tm_o, const FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   if constexpr (!kDecode) {
     const int h = blockIdx.x + (blockIdx.z % p.head_groups) * gridDim.x;   // groups are full
-    attn_item<false, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, h, blockIdx.z / p.head_groups,
+    attn_item<false, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, h, blockIdx.z / p.head_groups,
                             2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y)),
                             2);
   } else if constexpr (!kSplit) {
     grid_launch_dependents();
     const int L = blockIdx.x;
     const int rest = L / p.decode_pairs_per_seq;
-    attn_item<true, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, rest % p.num_heads,
+    attn_item<true, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, rest % p.num_heads,
                            rest / p.num_heads, 2 * (L % p.decode_pairs_per_seq), 2);
   } else {
     const int item = p.decode_split_from + static_cast<int>(blockIdx.x) / 2;
     const int sub = blockIdx.x & 1;
     const int rest = item / p.decode_pairs_per_seq;
-    attn_item<true, true>(tm_q, tm_k, tm_v, tm_k2, tm_v2, p, sm, rest % p.num_heads,
+    attn_item<true, true>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, rest % p.num_heads,
                           rest / p.num_heads, 2 * (item % p.decode_pairs_per_seq) + sub, 2);
     // This grid may run beside the pair grid launched before it: do not
     // complete before that grid has, so work queued after both sees its output.
@@ -862,8 +895,9 @@ bool encode_cache(CUtensorMap* m, const void* base, int num_heads, int64_t capac
 }  // namespace
 
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
-  CUtensorMap tq, tk, tv, tk2, tv2;
-  bool ok = encode_packed(&tq, a.q, a.num_heads, a.total_q);
+  CUtensorMap tq, tk, tv, tk2, tv2, to;
+  bool ok = encode_packed(&tq, a.q, a.num_heads, a.total_q) &&
+            encode_packed(&to, a.out, a.num_heads, a.total_q);
   if (!decode) {
     ok = ok && encode_packed(&tk, a.k, a.num_heads, a.total_k) &&
          encode_packed(&tv, a.v, a.num_heads, a.total_k);
@@ -930,7 +964,7 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     }
     p.head_groups = groups;
     const dim3 grid(per_group, (a.tiles_per_seq + 1) / 2, a.batch * groups);
-    attn_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+    attn_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, to, p);
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
   }
@@ -965,7 +999,7 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   }
   if (split_from > 0) {
     const dim3 grid(static_cast<unsigned>(split_from), 1, 1);
-    attn_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, p);
+    attn_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, to, p);
     if (cudaGetLastError() != cudaSuccess) return BCA_ERR_CUDA;
   }
   if (n_split > 0) {
@@ -979,7 +1013,7 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = split_from > 0 ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true, true>, tq, tk, tv, tk2, tv2, p) !=
+    if (cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true, true>, tq, tk, tv, tk2, tv2, to, p) !=
         cudaSuccess)
       return BCA_ERR_CUDA;
   }
