@@ -242,6 +242,15 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     for (int i = 0; i < 2; ++i) mbar_init(&sm.epi[i], kSoftmaxThreads);
     sm.abort = 0;
     fence_mbar_init();
+    // The query tiles are loaded at once, before the rest of the set-up: they
+    // come from DRAM and are the first MMA's operands.
+    const int n_q = !kSplit && rows_valid[1] > 0 ? 2 : 1;
+    mbar_arrive_expect_tx(&sm.q_full, n_q * kTileBytes);
+    for (int i = 0; i < n_q; ++i) {
+      const int row0 = q_seq0 + (m_base + i) * kBlockM;
+      tma_load_3d(&tm_q, &sm.q_full, sm.q[i], 0, h, row0);
+      tma_load_3d(&tm_q, &sm.q_full, sm.q[i] + kHalfBytes, 64, h, row0);
+    }
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -275,13 +284,6 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     if (lane == 0) {
       uint32_t armed = 0;   // bit s: stage s has been loaded at least once
       uint32_t parity = 0;  // bit s: parity of the last load into stage s
-      const int n_q = !kSplit && rows_valid[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&sm.q_full, n_q * kTileBytes);
-      for (int i = 0; i < n_q; ++i) {
-        const int row0 = q_seq0 + (m_base + i) * kBlockM;
-        tma_load_3d(&tm_q, &sm.q_full, sm.q[i], 0, h, row0);
-        tma_load_3d(&tm_q, &sm.q_full, sm.q[i] + kHalfBytes, 64, h, row0);
-      }
       // Load number idx (ring stage idx % kStages) of K or V tile g.
       auto load = [&](int idx, bool is_v, int g) {
         const int s = stage_of(idx);
