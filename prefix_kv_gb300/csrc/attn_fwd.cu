@@ -12,10 +12,10 @@
 // also covers PV_i(j): the softmax may rescale O_i right after seeing S_i(j+1).
 // Decode items that would fill less than half of a last wave run in a second
 // grid as single query tiles whose key range is split in two: warpgroup i runs
-// the same loop over its part with its own K/V tiles (the stages are handed
-// back by MMA commits), and warpgroup 0 merges the two partial rows, each
-// against its own reference max, at the end.  Such an item takes about half a
-// pair's time, where a single tile on one warpgroup would take 0.7.
+// the same loop over its part with its own K/V tiles, and warpgroup 0 merges
+// the two partial rows, each against its own reference max, at the end.  Such
+// an item takes ~0.6 of a pair's time, where a single tile on one warpgroup
+// would take 0.7.
 // The reference max is taken exactly on the first K tile; afterwards P is
 // formed against it directly and the max is only recomputed (with O and l
 // rescaled) for a tile whose row sum would exceed 2^16.  O and l share the
@@ -32,7 +32,8 @@
 // block-causal mask).  Prefix tile j of sequence b starts at cache token
 // cu_prefix[b] + 128 j, or with a page table at page_table[b][j] * 128 (a
 // 128-token page is one tile).  The last softmax warpgroup to read S(j) hands
-// the ring stages of V(j-1) and K(j) back to the producer.
+// the ring stages of V(j-1) and K(j) back to the producer (in a key-split item
+// each warpgroup hands back its own).
 //
 // Warp roles (384 threads, three warpgroups):
 //   warps 0-3  softmax + epilogue of Q0 (thread t owns TMEM lane t = query row t)
@@ -426,15 +427,14 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
           }
         }
       } else {
-        // Key split: every operand is used once, in the producer's load order, and
-        // its stage is handed back by a commit as soon as its MMA completes.
+        // Key split: every operand is used once, in the producer's load order; the
+        // softmax warpgroup that owns it hands its stage back (see below).
         int c = 0;
         for (int i = 0; i < 2 && ok; ++i) {
           if (nkt[i] == 0) continue;
           ok = landed(c);
           if (ok) {
             issue_s(i, stage_of(c));
-            umma_commit(&sm.kv_empty[stage_of(c)]);
             ++c;
           }
         }
@@ -447,14 +447,12 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
               if (!ok) break;
               tc_fence_after();
               issue_pv(i, vs, j);
-              umma_commit(&sm.kv_empty[vs]);
               ++c;
             }
             if (j + 1 < nkt[i]) {
               ok = landed(c);
               if (!ok) break;
               issue_s(i, stage_of(c));
-              umma_commit(&sm.kv_empty[stage_of(c)]);
               ++c;
             }
           }
@@ -580,6 +578,16 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       // last tile in issue order (Q1, or Q0 alone) that includes all readers
       // of V_{j-1} and K_j, so their ring stages can be handed back to the
       // producer here, without a commit on the MMA thread's critical path.
+      if constexpr (kSplit) {
+        // Key split: each warpgroup releases its own K(j) and V(j-1), read only by
+        // S(j) and PV(j-1), both covered by the commit behind S(j).  In the load
+        // order K0(0), K1(0), then V0(j-1), K0(j), V1(j-1), K1(j) for j >= 1, they
+        // are loads 4j-1 and 4j-2 (warpgroup 0), 4j+1 and 4j (warpgroup 1).
+        if (wq == 0 && lane == 0) {
+          if (j > 0) mbar_arrive(&sm.kv_empty[stage_of(qi == 0 ? 4 * j - 2 : 4 * j)]);
+          mbar_arrive(&sm.kv_empty[stage_of(j == 0 ? qi : (qi == 0 ? 4 * j - 1 : 4 * j + 1))]);
+        }
+      }
       if (releaser && wq == 0 && lane == 0) {
         if (j > 0) mbar_arrive(&sm.kv_empty[stage_of(2 * j - 1)]);   // V_{j-1}
         mbar_arrive(&sm.kv_empty[stage_of(2 * j)]);                  // K_j
