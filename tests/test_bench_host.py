@@ -27,3 +27,16 @@ def test_oracle_sample_flag_prints_json():
     assert d["flops"] > 0 and d["seconds"] > 0
     # threadpoolctl (when installed) reports the BLAS pool, else the variables are read
     assert 1 <= d["threads"] <= 2
+
+
+def test_decode_grid_count_follows_the_tail_rule():
+    # pairs fill whole waves of the SMs; a last wave at most half full becomes a second
+    # grid of key-split tiles (the launch rule of the decode call)
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.decode_grids(32, 4096, 1, 152) == 2       # 512 pairs: 56 left over
+    assert bench.decode_grids(32, 16384, 2, 152) == 1      # 4096 pairs: 144 > 76 left over
+    assert bench.decode_grids(3, 200, 4, 152) == 1         # 12 pairs: all key-split, one grid
+    assert bench.decode_grids(8, 1024, 19, 152) == 1       # 608 pairs: 4 whole waves
+    assert bench.decode_grids(8, 1000, 5, 152) == 2        # 160 pairs: 8 left over
+    assert bench.decode_grids(1, 0, 1, 152) == 0           # nothing to launch
