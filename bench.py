@@ -279,7 +279,7 @@ class Problem:
             self.launches += 2 * n_pieces - 2
         # the bf16 contiguous cache is written by the prefill launch itself
         # (bca_prefill_append) unless the two separate calls are asked for
-        self.fused = (self.decode and self.fp8_mode is None and not paged and not piecewise
+        self.fused = (self.decode and self.fp8_mode is None and not piecewise
                       and not prologue and not separate_append)
         if self.fused:
             self.launches -= 1
@@ -326,6 +326,7 @@ class Problem:
             bca.prefill_append(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"],
                                self.max_s, self.max_s, d["cu_pre"], self.cache_k, self.cache_v,
                                0, self.scale, out=self.out, lse=self.lse, workspace=self.ws,
+                               page_table=self.page_table if self.paged else None,
                                status=self.status)
         else:
             bca.prefill(d["q"], d["k"], d["v"], d["block_id"], d["cu"], d["cu"], self.max_s,
@@ -382,8 +383,12 @@ def time_standalone_append(prob: "Problem", flush, n: int = 10) -> float:
         flush.max()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], prob.cache_k, prob.cache_v,
-                                0, status=prob.status)
+        if prob.paged:
+            bca.prefix_cache_append_paged(d["k"], d["v"], d["cu"], d["cu_pre"], prob.page_table,
+                                          prob.cache_k, prob.cache_v, 0, status=prob.status)
+        else:
+            bca.prefix_cache_append(d["k"], d["v"], d["cu"], d["cu_pre"], prob.cache_k,
+                                    prob.cache_v, 0, status=prob.status)
         e1.record()
         torch.cuda.synchronize()
         if i >= 2:

@@ -31,7 +31,7 @@
  *
  * Beyond the prefill / decode / append path, the same library carries:
  *   - the prefill with the cache append fused in (one launch fewer):
- *     bca_prefill_append;
+ *     bca_prefill_append, bca_prefill_append_paged;
  *   - an FP8 E4M3 prefix cache with one fp32 scale per (token, head)
  *     (deployment notes, prefix-cache section): bca_prefix_cache_append_fp8,
  *     bca_prefix_cache_dequant_fp8, bca_prefix_decode_fp8;
@@ -163,6 +163,26 @@ bca_status bca_prefill_append(const void* q, const void* k, const void* v,
                               const int32_t* cu_prefix, void* cache_k, void* cache_v,
                               int32_t layer, int32_t num_layers, int64_t capacity,
                               int32_t* status_dev, void* stream);
+
+/* bca_prefill_append over a paged cache: the rows bca_prefix_cache_append_paged
+ * would write (prefix token t of sequence b to cache token
+ * page_table[b * max_pages + t / 128] * 128 + t % 128 of a pool of num_pages
+ * 128-token pages per layer and head, cache_k/v device bf16
+ * [num_layers][H][num_pages * 128][128]; page_table device int32).  Nothing is
+ * written when a prefix needs more than max_pages pages or a page id lies
+ * outside [0, num_pages) (BCA_ERR_CAPACITY), or on the errors of
+ * bca_prefill_append.
+ */
+bca_status bca_prefill_append_paged(const void* q, const void* k, const void* v,
+                                    const int32_t* block_id, const int32_t* cu_seqlens_q,
+                                    const int32_t* cu_seqlens_k, int32_t batch, int32_t num_heads,
+                                    int32_t head_dim, int32_t total_q, int32_t total_k,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                    float softmax_scale, void* out, float* lse, void* workspace,
+                                    size_t workspace_bytes, const int32_t* cu_prefix,
+                                    const int32_t* page_table, int32_t max_pages, void* cache_k,
+                                    void* cache_v, int32_t layer, int32_t num_layers,
+                                    int32_t num_pages, int32_t* status_dev, void* stream);
 
 /* Same computation as bca_prefill, for callers that cannot allocate device
  * memory or pass a workspace: for example a plugin inside a runtime that owns

@@ -30,6 +30,10 @@ SIGNATURES = {
     "bca_prefill_append": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32,
                                    c_i32, c_i32, c_i32, c_i32, c_f32, c_vp, c_vp, c_vp, c_size,
                                    c_vp, c_vp, c_vp, c_i32, c_i32, c_i64, c_vp, c_vp]),
+    "bca_prefill_append_paged": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
+                                         c_i32, c_i32, c_i32, c_i32, c_i32, c_f32, c_vp, c_vp,
+                                         c_vp, c_size, c_vp, c_vp, c_i32, c_vp, c_vp, c_i32,
+                                         c_i32, c_i32, c_vp, c_vp]),
     "bca_prefill_noalloc": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
                                     c_i32, c_i32, c_i32, c_f32, c_vp, c_vp, c_vp, c_vp]),
     "bca_prefix_decode": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,

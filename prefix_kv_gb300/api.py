@@ -118,10 +118,12 @@ def prefill(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
 def prefill_append(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int,
                    max_seqlen_k: int, cu_prefix, cache_k, cache_v, layer: int,
                    softmax_scale: Optional[float] = None, out=None, lse=None, workspace=None,
-                   status=None, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+                   page_table=None, status=None,
+                   stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """``prefill`` with ``prefix_cache_append`` fused in: returns ``(out, lse)`` and writes the
     first ``cu_prefix[b+1]-cu_prefix[b]`` keys/values of every sequence into cache tokens
-    ``cu_prefix[b]..`` of ``layer`` (cache ``[L, H, capacity, 128]`` bf16)."""
+    ``cu_prefix[b]..`` of ``layer`` (cache ``[L, H, capacity, 128]`` bf16), or, with
+    ``page_table [batch, max_pages]``, through it (as ``prefix_cache_append_paged``)."""
     for name, t in (("q", q), ("k", k), ("v", v)):
         _need(t, name, torch.bfloat16, 3)
     _need(block_id, "block_id", torch.int32, 1)
@@ -142,6 +144,10 @@ def prefill_append(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: 
     batch = cu_seqlens_q.numel() - 1
     if cu_prefix.numel() != batch + 1 or cu_seqlens_k.numel() != batch + 1:
         raise ValueError("cu_prefix / cu_seqlens_k must have batch + 1 entries")
+    if page_table is not None:
+        _, _, n_pages, _ = _paged_shapes(cache_k, cache_v, page_table)
+        if page_table.shape[0] != batch:
+            raise ValueError("page_table needs one row per sequence")
     if softmax_scale is None:
         softmax_scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -153,13 +159,20 @@ def prefill_append(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: 
     ws_bytes = prefill_workspace_bytes(batch, total_q, max_seqlen_q)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
-    code = _native.load().bca_prefill_append(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(block_id), _ptr(cu_seqlens_q), _ptr(cu_seqlens_k),
-        batch, H, D, total_q, total_k, max_seqlen_q, max_seqlen_k, float(softmax_scale),
-        _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _ptr(cu_prefix), _ptr(cache_k), _ptr(cache_v), layer, L, cap, _ptr(status),
-        _stream(stream))
-    _native.check(code, "bca_prefill_append")
+    lib = _native.load()
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(block_id), _ptr(cu_seqlens_q),
+            _ptr(cu_seqlens_k), batch, H, D, total_q, total_k, max_seqlen_q, max_seqlen_k,
+            float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(cu_prefix))
+    if page_table is None:
+        code = lib.bca_prefill_append(*args, _ptr(cache_k), _ptr(cache_v), layer, L, cap,
+                                      _ptr(status), _stream(stream))
+        _native.check(code, "bca_prefill_append")
+    else:
+        code = lib.bca_prefill_append_paged(*args, _ptr(page_table), page_table.shape[1],
+                                            _ptr(cache_k), _ptr(cache_v), layer, L, n_pages,
+                                            _ptr(status), _stream(stream))
+        _native.check(code, "bca_prefill_append_paged")
     return out, lse
 
 

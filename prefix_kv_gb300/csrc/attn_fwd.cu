@@ -494,7 +494,8 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     // ============ prefix store (prefill with cache append) ============
     // Every sequence is checked first and nothing is written if one fails, as
     // in the standalone append: a prefix longer than its keys (or with no query
-    // row to carry it), a negative offset, or the prefixes past the capacity.
+    // row to carry it), a negative offset, or the prefixes past the capacity
+    // (paged: more pages than the table holds, or a page outside the pool).
     int bad = 0;
     for (int i = lane; i < p.batch; i += 32) {
       const int pl = p.cu_prefix[i + 1] - p.cu_prefix[i];
@@ -502,8 +503,20 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       const int ql = p.cu_q[i + 1] - p.cu_q[i];
       if (pl < 0 || pl > kl || p.cu_prefix[i] < 0 || (pl > 0 && ql == 0)) bad = BCA_ERR_SEQLENS;
     }
-    if (lane == 0 && static_cast<int64_t>(p.cu_prefix[p.batch]) > p.capacity)
-      bad = bad != 0 ? bad : BCA_ERR_CAPACITY;
+    if (p.page_table == nullptr) {
+      if (lane == 0 && static_cast<int64_t>(p.cu_prefix[p.batch]) > p.capacity)
+        bad = bad != 0 ? bad : BCA_ERR_CAPACITY;
+    } else {
+      const int64_t n_pages = p.capacity / kBlockN;
+      for (int i = 0; i < p.batch; ++i) {
+        const int n = (p.cu_prefix[i + 1] - p.cu_prefix[i] + kBlockN - 1) / kBlockN;
+        if (n > p.max_pages) bad = bad != 0 ? bad : BCA_ERR_CAPACITY;
+        for (int jj = lane; jj < n && jj < p.max_pages; jj += 32) {
+          const int pg = p.page_table[static_cast<int64_t>(i) * p.max_pages + jj];
+          if (pg < 0 || pg >= n_pages) bad = bad != 0 ? bad : BCA_ERR_CAPACITY;
+        }
+      }
+    }
     bad = __reduce_max_sync(0xffffffffu, bad);
     if (bad != 0 && lane == 0 && h == 0) report_status(p.status, bad);
     const int c0 = p.cu_prefix[b];
@@ -520,21 +533,28 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       const int j = i >> 1;
       const bool is_v = i & 1;
       const int rows = min(kBlockN, n_pre_b - j * kBlockN);   // prefix rows in the tile
+      // cache token of the tile's first row (a paged cache: one 128-token page)
+      const int64_t tok0 = rows <= 0                ? 0
+                           : p.page_table != nullptr
+                               ? static_cast<int64_t>(
+                                     p.page_table[static_cast<int64_t>(b) * p.max_pages + j]) *
+                                     kBlockN
+                               : static_cast<int64_t>(c0) + j * kBlockN;
       if (rows == kBlockN) {
         // a whole tile: two TMA stores through the cache map (same 128-byte swizzled
         // layout as the loads), read out of shared memory before the stage is freed
         if (lane == 0) {
           const CUtensorMap* m = is_v ? &tm_v2 : &tm_k2;
-          tma_store_3d(m, sm.kv[s], 0, c0 + j * kBlockN, h);
-          tma_store_3d(m, sm.kv[s] + kHalfBytes, 64, c0 + j * kBlockN, h);
+          tma_store_3d(m, sm.kv[s], 0, static_cast<int>(tok0), h);
+          tma_store_3d(m, sm.kv[s] + kHalfBytes, 64, static_cast<int>(tok0), h);
           bulk_commit_group();
           bulk_wait_read_all();
         }
       } else if (rows > 0) {
         // the prefix ends inside the tile: copy its rows with 16-byte accesses,
         // undoing the swizzle (chunk c of row r sits at chunk c ^ (r % 8))
-        __nv_bfloat16* dst = (is_v ? p.cache_v : p.cache_k) +
-                             (static_cast<int64_t>(h) * p.capacity + c0 + j * kBlockN) * kHeadDim;
+        __nv_bfloat16* dst =
+            (is_v ? p.cache_v : p.cache_k) + (static_cast<int64_t>(h) * p.capacity + tok0) * kHeadDim;
         for (int idx = lane; idx < rows * 16; idx += 32) {
           const int r = idx >> 4, c = idx & 15;
           const uint4 val = *reinterpret_cast<const uint4*>(

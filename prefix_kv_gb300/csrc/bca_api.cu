@@ -195,7 +195,8 @@ bca_status prefill_impl(const void* q, const void* k, const void* v, const int32
                        int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
                        void* out, float* lse, void* workspace, size_t workspace_bytes,
                        const int32_t* cu_prefix, void* cache_k, void* cache_v, int64_t capacity,
-                       int32_t* status_dev, void* stream) {
+                       const int32_t* page_table, int32_t max_pages, int32_t* status_dev,
+                       void* stream) {
   if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
   if (batch < 0 || num_heads <= 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
       max_seqlen_k < 0 || max_seqlen_q > max_seqlen_k)
@@ -239,6 +240,8 @@ bca_status prefill_impl(const void* q, const void* k, const void* v, const int32
   a.cache_k = cache_k;
   a.cache_v = cache_v;
   a.capacity = capacity;
+  a.page_table = page_table;
+  a.max_pages = max_pages;
   return launch_attention(a, /*decode=*/false, s);
 }
 
@@ -254,8 +257,8 @@ bca_status bca_prefill(const void* q, const void* k, const void* v, const int32_
                        int32_t* status_dev, void* stream) {
   return prefill_impl(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, batch, num_heads, head_dim,
                       total_q, total_k, max_seqlen_q, max_seqlen_k, softmax_scale, out, lse,
-                      workspace, workspace_bytes, nullptr, nullptr, nullptr, 0, status_dev,
-                      stream);
+                      workspace, workspace_bytes, nullptr, nullptr, nullptr, 0, nullptr, 0,
+                      status_dev, stream);
 }
 
 bca_status bca_prefill_append(const void* q, const void* k, const void* v,
@@ -278,7 +281,34 @@ bca_status bca_prefill_append(const void* q, const void* k, const void* v,
                       workspace, workspace_bytes, cu_prefix,
                       static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems,
                       static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, capacity,
-                      status_dev, stream);
+                      nullptr, 0, status_dev, stream);
+}
+
+bca_status bca_prefill_append_paged(const void* q, const void* k, const void* v,
+                                    const int32_t* block_id, const int32_t* cu_seqlens_q,
+                                    const int32_t* cu_seqlens_k, int32_t batch, int32_t num_heads,
+                                    int32_t head_dim, int32_t total_q, int32_t total_k,
+                                    int32_t max_seqlen_q, int32_t max_seqlen_k,
+                                    float softmax_scale, void* out, float* lse, void* workspace,
+                                    size_t workspace_bytes, const int32_t* cu_prefix,
+                                    const int32_t* page_table, int32_t max_pages, void* cache_k,
+                                    void* cache_v, int32_t layer, int32_t num_layers,
+                                    int32_t num_pages, int32_t* status_dev, void* stream) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (num_pages <= 0 || num_pages > (1 << 24) || max_pages < 0 || layer < 0 ||
+      num_layers <= 0 || layer >= num_layers || num_heads <= 0)
+    return BCA_ERR_INVALID_ARG;
+  if (!cu_prefix || !page_table || !cache_k || !cache_v || !aligned16(cache_k) ||
+      !aligned16(cache_v))
+    return BCA_ERR_INVALID_ARG;
+  const int64_t capacity = static_cast<int64_t>(num_pages) * kBlockN;
+  const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
+  return prefill_impl(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, batch, num_heads, head_dim,
+                      total_q, total_k, max_seqlen_q, max_seqlen_k, softmax_scale, out, lse,
+                      workspace, workspace_bytes, cu_prefix,
+                      static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems,
+                      static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, capacity,
+                      page_table, max_pages, status_dev, stream);
 }
 
 bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void* cache_v,

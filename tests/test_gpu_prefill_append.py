@@ -121,3 +121,56 @@ def test_prefill_append_full_size_edit():
     assert torch.equal(ck[1], kd[:P].permute(1, 0, 2))
     assert torch.equal(cv[1], vd[:P].permute(1, 0, 2))
     assert (ck[0] == 0).all() and (cv[0] == 0).all()
+
+
+def _page_table(pre, pool, seed):
+    """Shuffled distinct pages of a pool, ceil(P_b / 128) per sequence, rows padded with -1."""
+    need = [(p + 127) // 128 for p in pre]
+    perm = np.random.default_rng(seed).permutation(pool)
+    rows, at = [], 0
+    width = max(need + [1])
+    for n in need:
+        rows.append(list(perm[at:at + n]) + [-1] * (width - n))
+        at += n
+    return torch.tensor(rows, dtype=torch.int32, device=DEV)
+
+
+@pytest.mark.parametrize("seed,kv,pre,heads", [
+    (96, [300, 5, 129, 1000], [299, 0, 128, 777], 3),
+    (97, [640, 200], [640, 199], 16),
+])
+def test_prefill_append_paged_matches_standalone(seed, kv, pre, heads):
+    case = ragged_case(seed, kv, heads=heads)
+    cu_p = np.concatenate([[0], np.cumsum(pre)]).astype(np.int32)
+    pool = sum((p + 127) // 128 for p in pre) + 3
+    pt = _page_table(pre, pool, seed)
+    d = lambda x: x.to(DEV)
+    ti = lambda x: torch.from_numpy(np.asarray(x, dtype=np.int32)).to(DEV)
+    args = (d(case.q), d(case.k), d(case.v), ti(case.block_id), ti(case.cu_q), ti(case.cu_k),
+            case.max_q, case.max_k)
+    out1, lse1 = bca.prefill(*args)
+    ck, cv = _sentinel_cache(2, heads, pool * 128)
+    st = _status()
+    out2, lse2 = bca.prefill_append(*args, ti(cu_p), ck, cv, 1, page_table=pt, status=st)
+    assert bca.read_status(st) == 0
+    assert torch.equal(out1, out2) and torch.equal(lse1, lse2)
+    sk, sv = _sentinel_cache(2, heads, pool * 128)
+    bca.prefix_cache_append_paged(d(case.k), d(case.v), ti(case.cu_k), ti(cu_p), pt, sk, sv, 1)
+    assert torch.equal(sk.view(torch.int16), ck.view(torch.int16))
+    assert torch.equal(sv.view(torch.int16), cv.view(torch.int16))
+
+
+def test_prefill_append_paged_rejects_bad_page():
+    case = ragged_case(98, [300, 200], heads=2)
+    cu_p = np.array([0, 250, 450], dtype=np.int32)
+    pt = _page_table([250, 200], 6, 98)
+    pt[1, 1] = 6                                   # outside the 6-page pool
+    d = lambda x: x.to(DEV)
+    ti = lambda x: torch.from_numpy(np.asarray(x, dtype=np.int32)).to(DEV)
+    ck, cv = _sentinel_cache(1, 2, 6 * 128)
+    st = _status()
+    bca.prefill_append(d(case.q), d(case.k), d(case.v), ti(case.block_id), ti(case.cu_q),
+                       ti(case.cu_k), case.max_q, case.max_k, ti(cu_p), ck, cv, 0,
+                       page_table=pt, status=st)
+    assert bca.read_status(st) == 5                # BCA_ERR_CAPACITY
+    assert (ck.view(torch.int16) == -1).all() and (cv.view(torch.int16) == -1).all()
