@@ -106,6 +106,23 @@ def test_prefill_append_host_validation(lib):
     assert _prefill_append(lib, tq=0) == 0               # nothing to do
 
 
+def test_prefill_append_paged_host_validation(lib):
+    def call(**kw):
+        a = dict(D=128, pt=16, mp=2, cck=16, ccv=16, layer=0, L=1, pages=4, cp=16)
+        a.update(kw)
+        return lib.bca_prefill_append_paged(16, 16, 16, 16, 16, 16, 1, 2, a["D"], 8, 8, 8, 8, 0.1,
+                                            16, 16, 16, 1 << 20, a["cp"], a["pt"], a["mp"],
+                                            a["cck"], a["ccv"], a["layer"], a["L"], a["pages"],
+                                            None, None)
+    assert call(D=64) == 2
+    assert call(pages=0) == 1                  # empty pool
+    assert call(pages=(1 << 24) + 1) == 1
+    assert call(mp=-1) == 1
+    assert call(pt=None) == 1
+    assert call(layer=1) == 1
+    assert call(ccv=24) == 1                   # misaligned cache
+
+
 def test_decode_and_append_host_validation(lib):
     dec = lib.bca_prefix_decode
     #         q   ck  cv  layer L  cap  cup tk  tv  cq  B  H  D    tq mq mp scale out lse st  s
