@@ -66,6 +66,10 @@ constexpr int kWarpMma = 8;
 constexpr int kWarpTma = 9;
 constexpr int kWarpFix = 10;
 constexpr int kWarpStore = 11;   // prefill with cache append: stores the prefix tiles
+// Prefill kernels: one instance with the cache append into a contiguous cache when
+// cache_k is set (or none), one with it through a page table.  (Three instances, one
+// without any append code, measured 1.4% slower for the plain prefill: ptxas lays the
+// shared code out differently.)
 constexpr int kSoftmaxThreads = 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColO = 256;
@@ -124,7 +128,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // One work item: head h, sequence b and its query tiles m_base .. m_base + n_qt - 1
 // (kSplit: the single tile m_base for both softmax warpgroups, each over part
 // of the key range; their partial results are merged at the end).
-template <bool kDecode, bool kSplit>
+template <bool kDecode, bool kSplit, bool kPagedAppend>
 __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const CUtensorMap& tm_k2,
                                           const CUtensorMap& tm_v2, const CUtensorMap& tm_o,
@@ -132,6 +136,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
                                           const int h, const int b, const int m_base,
                                           const int n_qt) {
   static_assert(kDecode || !kSplit, "key split is a decode item");
+  static_assert(!kPagedAppend || !kDecode, "the cache append is a prefill option");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Another CTA already gave up waiting: do not start new work.
@@ -503,7 +508,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       const int ql = p.cu_q[i + 1] - p.cu_q[i];
       if (pl < 0 || pl > kl || p.cu_prefix[i] < 0 || (pl > 0 && ql == 0)) bad = BCA_ERR_SEQLENS;
     }
-    if (p.page_table == nullptr) {
+    if constexpr (!kPagedAppend) {
       if (lane == 0 && static_cast<int64_t>(p.cu_prefix[p.batch]) > p.capacity)
         bad = bad != 0 ? bad : BCA_ERR_CAPACITY;
     } else {
@@ -534,12 +539,12 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       const bool is_v = i & 1;
       const int rows = min(kBlockN, n_pre_b - j * kBlockN);   // prefix rows in the tile
       // cache token of the tile's first row (a paged cache: one 128-token page)
-      const int64_t tok0 = rows <= 0                ? 0
-                           : p.page_table != nullptr
-                               ? static_cast<int64_t>(
-                                     p.page_table[static_cast<int64_t>(b) * p.max_pages + j]) *
-                                     kBlockN
-                               : static_cast<int64_t>(c0) + j * kBlockN;
+      int64_t tok0 = static_cast<int64_t>(c0) + j * kBlockN;
+      if constexpr (kPagedAppend) {
+        if (rows > 0)
+          tok0 = static_cast<int64_t>(p.page_table[static_cast<int64_t>(b) * p.max_pages + j]) *
+                 kBlockN;
+      }
       if (rows == kBlockN) {
         // a whole tile: two TMA stores through the cache map (same 128-byte swizzled
         // layout as the loads), read out of shared memory before the stage is freed
@@ -842,7 +847,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
 // filled wave become single-tile items (kSplit: two CTAs per pair, each with its
 // key range split between the two softmax warpgroups), launched as a second
 // grid that may start as soon as every pair CTA has started.
-template <bool kDecode, bool kSplit>
+template <bool kDecode, bool kSplit, bool kPagedAppend = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -855,20 +860,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   if constexpr (!kDecode) {
     const int h = blockIdx.x + (blockIdx.z % p.head_groups) * gridDim.x;   // groups are full
-    attn_item<false, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, h, blockIdx.z / p.head_groups,
+    attn_item<false, false, kPagedAppend>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, h, blockIdx.z / p.head_groups,
                             2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y)),
                             2);
   } else if constexpr (!kSplit) {
     grid_launch_dependents();
     const int L = blockIdx.x;
     const int rest = L / p.decode_pairs_per_seq;
-    attn_item<true, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, rest % p.num_heads,
+    attn_item<true, false, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, rest % p.num_heads,
                            rest / p.num_heads, 2 * (L % p.decode_pairs_per_seq), 2);
   } else {
     const int item = p.decode_split_from + static_cast<int>(blockIdx.x) / 2;
     const int sub = blockIdx.x & 1;
     const int rest = item / p.decode_pairs_per_seq;
-    attn_item<true, true>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, rest % p.num_heads,
+    attn_item<true, true, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, rest % p.num_heads,
                           rest / p.num_heads, 2 * (item % p.decode_pairs_per_seq) + sub, 2);
     // This grid may run beside the pair grid launched before it: do not
     // complete before that grid has, so work queued after both sees its output.
@@ -969,13 +974,18 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   p.status = a.status;
 
   if (!decode) {
-    static bool attr_set = false;
-    if (!attr_set) {
-      if (cudaFuncSetAttribute(attn_fwd_kernel<false, false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int mode = a.cache_k != nullptr && a.page_table != nullptr ? 1 : 0;   // paged append
+    using Kernel = void (*)(const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                            const CUtensorMap, const CUtensorMap, const CUtensorMap,
+                            const FwdParams);
+    const Kernel kernels[2] = {attn_fwd_kernel<false, false, false>,
+                               attn_fwd_kernel<false, false, true>};
+    static bool attr_set[2] = {false, false};
+    if (!attr_set[mode]) {
+      if (cudaFuncSetAttribute(kernels[mode], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(kSmemBytes)) != cudaSuccess)
         return BCA_ERR_CUDA;
-      attr_set = true;
+      attr_set[mode] = true;
     }
     // Groups of 8 heads (about 50 MB of K/V at 12.5k keys, well inside L2), else
     // of the largest divisor of the head count down to 4, else one group: every
@@ -994,7 +1004,7 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     }
     p.head_groups = groups;
     const dim3 grid(per_group, (a.tiles_per_seq + 1) / 2, a.batch * groups);
-    attn_fwd_kernel<false, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, to, p);
+    kernels[mode]<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, to, p);
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
   }
