@@ -68,8 +68,8 @@ enum {
                                 id outside the pool                                   */
   BCA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, ...)    */
   BCA_ERR_TIMEOUT = 7,       /* a bounded device wait ran out; outputs are undefined   */
-  BCA_ERR_SEQLENS = 8        /* cu_seqlens not monotone, q_len > kv_len, or a length
-                                above max_seqlen_*                                     */
+  BCA_ERR_SEQLENS = 8        /* cu_seqlens not monotone, q_len > kv_len, a length above
+                                max_seqlen_*, or a cache prefix longer than its keys   */
 };
 
 /* Human-readable name of a status code (static string). */
