@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                          const int32_t* __restrict__ cu_k, int tiles_per_seq,
                          int32_t* __restrict__ row_end, PrefillTile* __restrict__ tiles,
                          int32_t* status) {
-  __shared__ int ids[kChunk + 1];
+  __shared__ __align__(16) int ids[kChunk + 4];   // + the id past the chunk, padded
   __shared__ int run_end[kMaxRuns];
   __shared__ int run_id[kMaxRuns];
   __shared__ int warp_buf[kWarps + 1];
@@ -95,7 +95,16 @@ __global__ void __launch_bounds__(kPrepThreads)
       }
       if (tid == 0 && kChunk < n) ids[kChunk] = bid[k0 + base + kChunk];
       __syncthreads();
-      // thread t looks at positions base + 8t .. base + 8t + 7
+      // thread t looks at positions base + 8t .. base + 8t + 7 (read as two 16-byte
+      // vectors plus the next id: scalar reads 8 words apart conflicted 8-way)
+      int my[kPerThread + 1];
+      {
+        const int4 lo4 = *reinterpret_cast<const int4*>(&ids[tid * kPerThread]);
+        const int4 hi4 = *reinterpret_cast<const int4*>(&ids[tid * kPerThread + 4]);
+        my[0] = lo4.x; my[1] = lo4.y; my[2] = lo4.z; my[3] = lo4.w;
+        my[4] = hi4.x; my[5] = hi4.y; my[6] = hi4.z; my[7] = hi4.w;
+        my[8] = ids[tid * kPerThread + kPerThread];
+      }
       int cnt = 0;
       unsigned ends = 0;
 #pragma unroll
@@ -103,9 +112,9 @@ __global__ void __launch_bounds__(kPrepThreads)
         const int jl = tid * kPerThread + u;
         const int j = base + jl;
         if (j < kv_len) {
-          const int id = ids[jl];
+          const int id = my[u];
           if (id < -1) err = BCA_ERR_BLOCK_ID;
-          if (id >= 0 && (j == kv_len - 1 || ids[jl + 1] != id)) {
+          if (id >= 0 && (j == kv_len - 1 || my[u + 1] != id)) {
             ends |= 1u << u;
             ++cnt;
           }
@@ -119,7 +128,7 @@ __global__ void __launch_bounds__(kPrepThreads)
           const int jl = tid * kPerThread + u;
           if (rank < kMaxRuns) {
             run_end[rank] = base + jl + 1;
-            run_id[rank] = ids[jl];
+            run_id[rank] = my[u];
           }
           ++rank;
         }
@@ -183,15 +192,9 @@ __global__ void __launch_bounds__(kPrepThreads)
         }
         row_end[q0 + i] = e;
       }
-      int vmax = valid ? e : 0;
-      int vmin = valid ? e : 0x7fffffff;
-      int cnt = valid ? 1 : 0;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
-        vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
-        cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-      }
+      const int vmax = __reduce_max_sync(0xffffffffu, valid ? e : 0);
+      const int vmin = __reduce_min_sync(0xffffffffu, valid ? e : 0x7fffffff);
+      const int cnt = static_cast<int>(__reduce_add_sync(0xffffffffu, valid ? 1u : 0u));
       if (lane == 0) {
         red[0][u][wid] = vmax;
         red[1][u][wid] = vmin;
