@@ -40,3 +40,18 @@ def test_decode_grid_count_follows_the_tail_rule():
     assert bench.decode_grids(8, 1024, 19, 152) == 1       # 608 pairs: 4 whole waves
     assert bench.decode_grids(8, 1000, 5, 152) == 2        # 160 pairs: 8 left over
     assert bench.decode_grids(1, 0, 1, 152) == 0           # nothing to launch
+
+
+def test_reference_arm_line():
+    # the reference arm times the oracle on the host and prints the contract's JSON line
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "0", "--workload", "tiny_mixed_s40"],
+                         env=env, capture_output=True, text=True, timeout=300, check=True).stdout
+    d = json.loads(out.strip().splitlines()[-1])
+    assert d["impl"] == "reference" and d["higher_is_better"] is True
+    assert d["unit"] == "TFLOP/s" and d["value"] > 0 and d["dtype"] == "f64"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+    assert d["config"]["workload"] == "tiny_mixed_s40"
