@@ -109,11 +109,16 @@ bca_status bca_selftest_wait_timeout(uint64_t limit_ns, int32_t* status_dev,
  *            the tile's valid rows, k_min = min e, valid rows, 0}; all zero
  *            for a tile past the sequence end or a sequence that failed
  *            validation.
+ *   total_q, total_k  lengths of the packed query rows and keys (row_end and
+ *            block_id hold that many entries).  A sequence with cu_q[b] < 0,
+ *            cu_k[b] < 0, cu_q[b+1] > total_q or cu_k[b+1] > total_k fails with
+ *            BCA_ERR_SEQLENS in *status_dev before any of its row ends is
+ *            written or any of its block ids is read.
  */
 bca_status bca_schedule_prep(const int32_t* block_id, const int32_t* cu_seqlens_q,
-                             const int32_t* cu_seqlens_k, int32_t batch, int32_t max_seqlen_q,
-                             int32_t* row_end, int32_t* tiles, int32_t* status_dev,
-                             void* stream);
+                             const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
+                             int32_t total_k, int32_t max_seqlen_q, int32_t* row_end,
+                             int32_t* tiles, int32_t* status_dev, void* stream);
 
 /* Bytes of device workspace bca_prefill needs (row_end + tile records). */
 size_t bca_prefill_workspace_bytes(int32_t batch, int32_t total_q, int32_t max_seqlen_q);
@@ -193,9 +198,12 @@ bca_status bca_prefill_append_paged(const void* q, const void* k, const void* v,
  * The scratch is a fixed 2 MiB array in the library's own device memory, held
  * by every GPU that loads the library until the process exits.  Problems with
  * total_q > 262144 or batch * ceil(max_seqlen_q / 128) > 65536 are rejected
- * with BCA_ERR_WORKSPACE.  The first call on each device looks up the array's
- * device address (cudaGetSymbolAddress) with that device current; make that
- * first call before any stream capture.  The call allocates nothing.  All
+ * with BCA_ERR_WORKSPACE.  Every call looks up the array's device address on
+ * the current device (cudaGetSymbolAddress; the first lookup on a device loads
+ * the library's module there, so make the first call before any stream
+ * capture).  Since the address is not cached, calls after a device reset or a
+ * re-created primary context use the array's new location.  The call
+ * allocates nothing.  All
  * calls share the array: calls whose kernels may overlap on the GPU (other
  * streams or host threads) race and must be serialised by the caller.
  * Arguments, layouts and errors are otherwise those of bca_prefill.

@@ -23,7 +23,8 @@ SIGNATURES = {
     "bca_version": (c_i32, []),
     "bca_read_device_status": (c_i32, [c_vp, c_vp]),
     "bca_selftest_wait_timeout": (c_i32, [ctypes.c_uint64, c_vp, c_vp, c_vp]),
-    "bca_schedule_prep": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp]),
+    "bca_schedule_prep": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp,
+                                  c_vp]),
     "bca_prefill_workspace_bytes": (c_size, [c_i32, c_i32, c_i32]),
     "bca_prefill": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32,
                             c_i32, c_i32, c_i32, c_f32, c_vp, c_vp, c_vp, c_size, c_vp, c_vp]),

@@ -62,21 +62,25 @@ def prefill_workspace_bytes(batch: int, total_q: int, max_seqlen_q: int) -> int:
 
 
 def schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, status=None,
-                  stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Per-row visible-key ends e(r) and per-tile records ``[B, tiles, 4]``."""
+                  stream=None, total_q: Optional[int] = None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Per-row visible-key ends e(r) and per-tile records ``[B, tiles, 4]``.
+
+    ``total_q`` (the length of the returned ``row_end``) defaults to the last query
+    offset; the keys are all of ``block_id``."""
     _need(block_id, "block_id", torch.int32, 1)
     _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
     _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
     batch = cu_seqlens_q.numel() - 1
-    total_q = int(cu_seqlens_q[-1].item()) if batch > 0 else 0
+    if total_q is None:
+        total_q = int(cu_seqlens_q[-1].item()) if batch > 0 else 0
     tiles_per_seq = (max_seqlen_q + 127) // 128
     dev = block_id.device
     row_end = torch.zeros(total_q, dtype=torch.int32, device=dev)
     tiles = torch.zeros((batch, tiles_per_seq, 4), dtype=torch.int32, device=dev)
     code = _native.load().bca_schedule_prep(_ptr(block_id), _ptr(cu_seqlens_q),
-                                            _ptr(cu_seqlens_k), batch, max_seqlen_q,
-                                            _ptr(row_end), _ptr(tiles), _ptr(status),
-                                            _stream(stream))
+                                            _ptr(cu_seqlens_k), batch, total_q,
+                                            block_id.numel(), max_seqlen_q, _ptr(row_end),
+                                            _ptr(tiles), _ptr(status), _stream(stream))
     _native.check(code, "bca_schedule_prep")
     return row_end, tiles
 

@@ -146,6 +146,14 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   // ---- the work item (uniform over the CTA) ---------------------------------
   const int q_seq0 = p.cu_q[b];
   const int q_len = p.cu_q[b + 1] - q_seq0;
+  if constexpr (kDecode) {
+    // the sequence's query rows must lie in [0, total_q) (prefill sequences are
+    // checked by the schedule prep, whose zeroed tile records end them below)
+    if (q_seq0 < 0 || q_len < 0 || q_seq0 > p.total_q - q_len) {
+      if (threadIdx.x == 0) report_status(p.status, BCA_ERR_SEQLENS);
+      return;
+    }
+  }
   int rows_valid[2], nkt[2];
   int k_min[2] = {0, 0}, k_hi[2] = {0, 0};
   for (int i = 0; i < 2; ++i) {

@@ -36,6 +36,32 @@ PrefillWorkspace carve(void* base, int batch, int total_q, int max_seqlen_q) {
 
 }  // namespace
 
+namespace bca {
+
+bca_status check_prefill_args(const void* q, const void* k, const void* v,
+                              const int32_t* block_id, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_k, int32_t batch, int32_t num_heads,
+                              int32_t head_dim, int32_t total_q, int32_t total_k,
+                              int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                              const void* out, const float* lse) {
+  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
+  if (batch < 0 || num_heads <= 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
+      max_seqlen_k < 0 || max_seqlen_q > max_seqlen_k)
+    return BCA_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BCA_ERR_INVALID_ARG;
+  if (batch == 0 || total_q == 0) return BCA_OK;
+  if (total_k == 0) return BCA_ERR_SEQLENS;
+  if (!q || !k || !v || !block_id || !cu_seqlens_q || !cu_seqlens_k || !out || !lse)
+    return BCA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return BCA_ERR_INVALID_ARG;
+  if (num_heads > 65535 || batch > 65535 || tiles_for(max_seqlen_q) > 65535)
+    return BCA_ERR_UNSUPPORTED;
+  return BCA_OK;
+}
+
+}  // namespace bca
+
 namespace {
 
 // Decode over one layer's bf16 K and V ([H][capacity][128] each).
@@ -169,16 +195,16 @@ size_t bca_prefill_workspace_bytes(int32_t batch, int32_t total_q, int32_t max_s
 }
 
 bca_status bca_schedule_prep(const int32_t* block_id, const int32_t* cu_seqlens_q,
-                             const int32_t* cu_seqlens_k, int32_t batch, int32_t max_seqlen_q,
-                             int32_t* row_end, int32_t* tiles, int32_t* status_dev,
-                             void* stream) {
-  if (batch < 0 || max_seqlen_q < 0) return BCA_ERR_INVALID_ARG;
+                             const int32_t* cu_seqlens_k, int32_t batch, int32_t total_q,
+                             int32_t total_k, int32_t max_seqlen_q, int32_t* row_end,
+                             int32_t* tiles, int32_t* status_dev, void* stream) {
+  if (batch < 0 || max_seqlen_q < 0 || total_q < 0 || total_k < 0) return BCA_ERR_INVALID_ARG;
   if (batch == 0 || max_seqlen_q == 0) return BCA_OK;
   if (!block_id || !cu_seqlens_q || !cu_seqlens_k || !row_end || !tiles)
     return BCA_ERR_INVALID_ARG;
   if (batch > 65535) return BCA_ERR_UNSUPPORTED;
-  cudaError_t e = launch_schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, batch,
-                                       tiles_for(max_seqlen_q), row_end,
+  cudaError_t e = launch_schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, batch, total_q,
+                                       total_k, tiles_for(max_seqlen_q), row_end,
                                        reinterpret_cast<PrefillTile*>(tiles), status_dev,
                                        static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
@@ -197,27 +223,18 @@ bca_status prefill_impl(const void* q, const void* k, const void* v, const int32
                        const int32_t* cu_prefix, void* cache_k, void* cache_v, int64_t capacity,
                        const int32_t* page_table, int32_t max_pages, int32_t* status_dev,
                        void* stream) {
-  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
-  if (batch < 0 || num_heads <= 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
-      max_seqlen_k < 0 || max_seqlen_q > max_seqlen_k)
-    return BCA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return BCA_ERR_INVALID_ARG;
-  if (batch == 0 || total_q == 0) return BCA_OK;
-  if (total_k == 0) return BCA_ERR_SEQLENS;
-  if (!q || !k || !v || !block_id || !cu_seqlens_q || !cu_seqlens_k || !out || !lse)
-    return BCA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
-    return BCA_ERR_INVALID_ARG;
-  if (num_heads > 65535 || batch > 65535 || tiles_for(max_seqlen_q) > 65535)
-    return BCA_ERR_UNSUPPORTED;
+  const bca_status arg = check_prefill_args(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, batch,
+                                           num_heads, head_dim, total_q, total_k, max_seqlen_q,
+                                           max_seqlen_k, softmax_scale, out, lse);
+  if (arg != BCA_OK || batch == 0 || total_q == 0) return arg;
   PrefillWorkspace w = carve(workspace, batch, total_q, max_seqlen_q);
   if (workspace == nullptr || workspace_bytes < w.bytes || !aligned16(workspace))
     return BCA_ERR_WORKSPACE;
 
   auto s = static_cast<cudaStream_t>(stream);
   const int tps = tiles_for(max_seqlen_q);
-  if (launch_schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, batch, tps, w.row_end, w.tiles,
-                           status_dev, s) != cudaSuccess)
+  if (launch_schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, tps,
+                           w.row_end, w.tiles, status_dev, s) != cudaSuccess)
     return BCA_ERR_CUDA;
   AttnLaunch a{};
   a.q = q;

@@ -27,9 +27,21 @@ struct PrefillTile {  // one record per (sequence, 128-row query tile)
 };
 
 // ---- host-side launchers (defined in the .cu files) ----------------------------------
+// Host-side argument checks of the prefill entry points (bca_prefill and its
+// variants): BCA_OK when the call may proceed; batch == 0 or total_q == 0 pass
+// (nothing to launch).
+bca_status check_prefill_args(const void* q, const void* k, const void* v,
+                              const int32_t* block_id, const int32_t* cu_seqlens_q,
+                              const int32_t* cu_seqlens_k, int32_t batch, int32_t num_heads,
+                              int32_t head_dim, int32_t total_q, int32_t total_k,
+                              int32_t max_seqlen_q, int32_t max_seqlen_k, float softmax_scale,
+                              const void* out, const float* lse);
+
+// A sequence whose offsets leave [0, total_q) / [0, total_k) fails with BCA_ERR_SEQLENS.
 cudaError_t launch_schedule_prep(const int32_t* block_id, const int32_t* cu_q, const int32_t* cu_k,
-                                 int batch, int tiles_per_seq, int32_t* row_end,
-                                 PrefillTile* tiles, int32_t* status, cudaStream_t stream);
+                                 int batch, int total_q, int total_k, int tiles_per_seq,
+                                 int32_t* row_end, PrefillTile* tiles, int32_t* status,
+                                 cudaStream_t stream);
 
 struct AttnLaunch {
   // tensors

@@ -19,8 +19,6 @@
 // other host threads) race on the array: callers must serialise them.
 #include "common.cuh"
 
-#include <mutex>
-
 namespace {
 
 constexpr int kNoAllocMaxRows = 262144;   // query rows            (1 MiB of int32)
@@ -28,34 +26,17 @@ constexpr int kNoAllocMaxTiles = 65536;   // (sequence, 128-row tile) records (1
 constexpr size_t kRowBytes = static_cast<size_t>(kNoAllocMaxRows) * sizeof(int32_t);
 constexpr size_t kScratchBytes =
     kRowBytes + static_cast<size_t>(kNoAllocMaxTiles) * sizeof(bca::PrefillTile);
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-// In host code g_noalloc_scratch names a host-side stand-in, not device memory:
-// its device address is looked up once per device and cached here.
-std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device.  The first
-// bca_prefill_noalloc call made on a device performs the lookup.
+// In host code g_noalloc_scratch names a host-side stand-in, not device memory.
+// Its device address on the current device is looked up on every call (the
+// lookup allocates nothing and is cheap): a cached address would go stale when
+// the device is reset or its primary context is re-created, since the module,
+// and with it the array, is then loaded again, possibly elsewhere.
 cudaError_t scratch_for_current_device(void** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
-  return cudaSuccess;
+  return cudaGetSymbolAddress(out, g_noalloc_scratch);
 }
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 
@@ -66,19 +47,11 @@ extern "C" bca_status bca_prefill_noalloc(
     int32_t max_seqlen_k, float softmax_scale, void* out, float* lse, int32_t* status_dev,
     void* stream) {
   using namespace bca;
-  if (head_dim != kHeadDim) return BCA_ERR_UNSUPPORTED;
-  if (batch < 0 || num_heads <= 0 || total_q < 0 || total_k < 0 || max_seqlen_q < 0 ||
-      max_seqlen_k < 0 || max_seqlen_q > max_seqlen_k)
-    return BCA_ERR_INVALID_ARG;
-  if (!(softmax_scale > 0.f) || !(softmax_scale < 3.0e38f)) return BCA_ERR_INVALID_ARG;
-  if (batch == 0 || total_q == 0) return BCA_OK;
-  if (total_k == 0) return BCA_ERR_SEQLENS;
-  if (!q || !k || !v || !block_id || !cu_seqlens_q || !cu_seqlens_k || !out || !lse)
-    return BCA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
-    return BCA_ERR_INVALID_ARG;
+  const bca_status arg = check_prefill_args(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, batch,
+                                           num_heads, head_dim, total_q, total_k, max_seqlen_q,
+                                           max_seqlen_k, softmax_scale, out, lse);
+  if (arg != BCA_OK || batch == 0 || total_q == 0) return arg;
   const int tiles_per_seq = (max_seqlen_q + kBlockM - 1) / kBlockM;
-  if (num_heads > 65535 || batch > 65535 || tiles_per_seq > 65535) return BCA_ERR_UNSUPPORTED;
   if (total_q > kNoAllocMaxRows ||
       static_cast<int64_t>(batch) * tiles_per_seq > kNoAllocMaxTiles)
     return BCA_ERR_WORKSPACE;  // larger than this entry point's fixed scratch
@@ -90,8 +63,8 @@ extern "C" bca_status bca_prefill_noalloc(
       reinterpret_cast<PrefillTile*>(static_cast<unsigned char*>(scratch) + kRowBytes);
 
   auto s = static_cast<cudaStream_t>(stream);
-  if (launch_schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, batch, tiles_per_seq, row_end,
-                           tiles, status_dev, s) != cudaSuccess)
+  if (launch_schedule_prep(block_id, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k,
+                           tiles_per_seq, row_end, tiles, status_dev, s) != cudaSuccess)
     return BCA_ERR_CUDA;
   AttnLaunch a{};
   a.q = q;

@@ -129,8 +129,8 @@ bca_status bca_prefill_piecewise(const void* q, const void* k, const void* v,
     const Piece& p = pcs[i];
     const int q_len = p.e - p.a, kv_len = p.e - p.s;
     const int tps = (q_len + kBlockM - 1) / kBlockM;
-    if (launch_schedule_prep(block_id + p.s, d_cu + 4 * i, d_cu + 4 * i + 2, 1, tps, row_end,
-                             tiles, status_dev, st) != cudaSuccess)
+    if (launch_schedule_prep(block_id + p.s, d_cu + 4 * i, d_cu + 4 * i + 2, 1, q_len, kv_len,
+                             tps, row_end, tiles, status_dev, st) != cudaSuccess)
       return BCA_ERR_CUDA;
     AttnLaunch a{};
     a.q = static_cast<const uint8_t*>(q) + p.a * row_bytes;

@@ -58,9 +58,9 @@ __device__ __forceinline__ int block_excl_scan(int x, int* warp_buf, int& total)
 
 __global__ void __launch_bounds__(kPrepThreads)
     schedule_prep_kernel(const int32_t* __restrict__ bid, const int32_t* __restrict__ cu_q,
-                         const int32_t* __restrict__ cu_k, int tiles_per_seq,
-                         int32_t* __restrict__ row_end, PrefillTile* __restrict__ tiles,
-                         int32_t* status) {
+                         const int32_t* __restrict__ cu_k, int total_q, int total_k,
+                         int tiles_per_seq, int32_t* __restrict__ row_end,
+                         PrefillTile* __restrict__ tiles, int32_t* status) {
   __shared__ __align__(16) int ids[kChunk + 4];   // + the id past the chunk, padded
   __shared__ int run_end[kMaxRuns];
   __shared__ int run_id[kMaxRuns];
@@ -79,7 +79,10 @@ __global__ void __launch_bounds__(kPrepThreads)
   if (tid == 0) {
     n_runs = 0;
     err = 0;
-    if (kv_len < 0 || q_len < 0 || q_len > kv_len || q_len > tiles_per_seq * kBlockM)
+    // the sequence's rows and keys must lie inside the packed arrays: nothing below
+    // writes a row end or reads a block id before this check has passed
+    if (kv_len < 0 || q_len < 0 || q_len > kv_len || q_len > tiles_per_seq * kBlockM ||
+        q0 < 0 || k0 < 0 || q0 > total_q - q_len || k0 > total_k - kv_len)
       err = BCA_ERR_SEQLENS;
   }
   __syncthreads();
@@ -226,10 +229,11 @@ __global__ void __launch_bounds__(kPrepThreads)
 }  // namespace
 
 cudaError_t launch_schedule_prep(const int32_t* block_id, const int32_t* cu_q, const int32_t* cu_k,
-                                 int batch, int tiles_per_seq, int32_t* row_end,
-                                 PrefillTile* tiles, int32_t* status, cudaStream_t stream) {
-  schedule_prep_kernel<<<batch, kPrepThreads, 0, stream>>>(block_id, cu_q, cu_k, tiles_per_seq,
-                                                           row_end, tiles, status);
+                                 int batch, int total_q, int total_k, int tiles_per_seq,
+                                 int32_t* row_end, PrefillTile* tiles, int32_t* status,
+                                 cudaStream_t stream) {
+  schedule_prep_kernel<<<batch, kPrepThreads, 0, stream>>>(block_id, cu_q, cu_k, total_q, total_k,
+                                                           tiles_per_seq, row_end, tiles, status);
   return cudaGetLastError();
 }
 

@@ -42,6 +42,24 @@ def test_binding_signatures_cover_header():
     assert set(_native.SIGNATURES) == set(declared_functions())
 
 
+def declared_arity():
+    """Number of parameters of every function the header declares."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    out = {}
+    for m in re.finditer(r"\b(bca_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;", text):
+        params = m.group(2).strip()
+        out[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arity_matches_header():
+    from prefix_kv_gb300 import _native
+    arity = declared_arity()
+    assert set(arity) == set(declared_functions())
+    for name, (_, argtypes) in _native.SIGNATURES.items():
+        assert len(argtypes) == arity[name], name
+
+
 def test_status_strings(lib):
     assert lib.bca_status_string(0) == b"ok"
     for code in range(1, 9):

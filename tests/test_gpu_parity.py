@@ -11,7 +11,7 @@ import torch
 import oracle
 import prefix_kv_gb300 as bca
 from prefix_kv_gb300 import workloads as W
-from gpu_cases import (DEV, DecodeCase, PrefillCase, assert_close, ragged_case,
+from gpu_cases import (DEV, SCALE, DecodeCase, PrefillCase, assert_close, ragged_case,
                        tile_boundary_rows)
 
 pytestmark = pytest.mark.gpu
@@ -99,6 +99,31 @@ def test_schedule_rejects_bad_id_and_lengths():
                       torch.tensor([0, 5], dtype=torch.int32, device=DEV),
                       torch.from_numpy(cu).to(DEV), 5, status=st)      # q_len > kv_len
     assert bca.read_status(st) == 8
+
+
+def test_schedule_rejects_offsets_past_the_arrays():
+    """A sequence whose offsets run past total_q (or total_k) fails with
+    BCA_ERR_SEQLENS before any row end is written: a guard region behind row_end
+    keeps its fill, and the sequence's tile records are zero."""
+    from prefix_kv_gb300 import _native
+    lib = _native.load()
+    bid = torch.full((400,), -1, dtype=torch.int32, device=DEV)
+    for cu_q, cu_k, total_q, total_k in (
+            ([0, 200, 400], [0, 200, 400], 272, 400),     # cu_q[2] = total_q + 128
+            ([0, 200, 400], [0, 200, 400], 400, 272),     # cu_k[2] past total_k
+            ([0, -8, 400], [0, 200, 400], 400, 400)):     # negative offset
+        cq = torch.tensor(cu_q, dtype=torch.int32, device=DEV)
+        ck = torch.tensor(cu_k, dtype=torch.int32, device=DEV)
+        row_end = torch.full((total_q + 256,), -5, dtype=torch.int32, device=DEV)
+        tiles = torch.full((2, 2, 4), -5, dtype=torch.int32, device=DEV)
+        st = _status()
+        code = lib.bca_schedule_prep(bid.data_ptr(), cq.data_ptr(), ck.data_ptr(), 2, total_q,
+                                     total_k, 256, row_end.data_ptr(), tiles.data_ptr(),
+                                     st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+        assert code == 0
+        assert bca.read_status(st) == 8, (cu_q, cu_k, total_q, total_k)
+        assert (row_end[total_q:] == -5).all()
+        assert (tiles[1] == 0).all()
 
 
 # ---------------------------------------------------------------- prefill
@@ -286,6 +311,40 @@ def test_decode_capacity_overflow_reported():
                       case.v_tgt.to(DEV), torch.from_numpy(case.cu_q).to(DEV), 16, 24,
                       status=st)
     assert bca.read_status(st) == 5
+
+
+def test_decode_rejects_query_offsets_past_total_q():
+    """Target offsets that run past total_q: that sequence fails with BCA_ERR_SEQLENS
+    and nothing is written behind the output or the LSE; the first sequence is
+    still computed."""
+    from prefix_kv_gb300 import _native
+    lib = _native.load()
+    H, P = 2, 200
+    tq_all = 300
+    q = W.randn_bf16((tq_all, H, 128), 91).to(DEV)
+    kt = W.randn_bf16((tq_all, H, 128), 92).to(DEV)
+    vt = W.randn_bf16((tq_all, H, 128), 93).to(DEV)
+    ck = W.randn_bf16((1, H, 2 * P, 128), 94).to(DEV)
+    cv = W.randn_bf16((1, H, 2 * P, 128), 95).to(DEV)
+    cu_q = torch.tensor([0, 100, 300], dtype=torch.int32, device=DEV)
+    cu_p = torch.tensor([0, P, 2 * P], dtype=torch.int32, device=DEV)
+    total_q = 172                                   # cu_q[2] = total_q + 128
+    out_buf = torch.full((total_q + 256, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    lse_buf = torch.full((H * total_q + 256,), float("nan"), dtype=torch.float32, device=DEV)
+    st = _status()
+    code = lib.bca_prefix_decode(q.data_ptr(), ck.data_ptr(), cv.data_ptr(), 0, 1, 2 * P,
+                                 cu_p.data_ptr(), kt.data_ptr(), vt.data_ptr(), cu_q.data_ptr(),
+                                 2, H, 128, total_q, 200, P, SCALE, out_buf.data_ptr(),
+                                 lse_buf.data_ptr(), st.data_ptr(),
+                                 torch.cuda.current_stream().cuda_stream)
+    assert code == 0
+    assert bca.read_status(st) == 8
+    assert torch.isnan(out_buf[100:].float()).all() and torch.isnan(lse_buf[H * total_q:]).all()
+    lse = lse_buf[:H * total_q].view(H, total_q)
+    ref_out, ref_lse = oracle.prefix_decode(
+        q[:100].cpu(), ck[0, :, :P].permute(1, 0, 2).cpu(), cv[0, :, :P].permute(1, 0, 2).cpu(),
+        np.array([0, P]), kt[:100].cpu(), vt[:100].cpu(), np.array([0, 100]), SCALE)
+    assert_close(out_buf[:100], lse[:, :100], ref_out, ref_lse, what="first sequence")
 
 
 # ---------------------------------------------------------------- cache append
