@@ -140,6 +140,19 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
                 "reasons": sorted(reasons), "samples": len(sm)}
 
+    def bins(self, width: int = 60):
+        """SM clock samples counted in `width`-MHz bins, keyed by the bin's lower edge."""
+        out = {}
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            try:
+                mhz = float(parts[1])
+            except (IndexError, ValueError):
+                continue
+            lo = int(mhz // width * width)
+            out[f"{lo}-{lo + width}"] = out.get(f"{lo}-{lo + width}", 0) + 1
+        return dict(sorted(out.items()))
+
 
 # ----------------------------------------------------------------------------- ranks
 
@@ -561,6 +574,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sustained-seconds", type=float, default=3.0,
+                    help="length of the sustained leg (steps back to back, L2 not flushed, "
+                         "clocks sampled throughout); 0 skips it")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="another config's workload (tiny_mixed_s40, t2i_1024_s4352, "
                          "cfg_edit_4ref_varlen, neo_mixed_32seq); the default is the headline")
@@ -661,6 +677,37 @@ def main():
     else:
         s_app = seg["append"]
         app_gbs = prob.append_bytes / (s_app / K * 1e-3) / 1e9 if prob.decode else 0.0
+
+    # ---- sustained: seconds of back-to-back steps, as a model's layers run them -----
+    # The timed region above is tens of milliseconds, short enough to finish before
+    # the power limit pulls the clocks down.  Here the same step runs back to back
+    # (no L2 flush) for a few seconds, timed by one pair of events, with the SM
+    # clock sampled every 100 ms; the figure is set against the sustained GEMM peak.
+    sustained = None
+    if args.sustained_seconds > 0:
+        n_sus = max(10, int(args.sustained_seconds * 1e3 / max(tot_ms / K, 1e-3)))
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+        with ClockSampler(local) as sus_clocks:
+            ev0.record()
+            for _ in range(n_sus):
+                prob.step(prob.dev)
+            ev1.record()
+            torch.cuda.synchronize()
+        code = bca.read_status(prob.status)
+        if code != 0:
+            raise SystemExit(f"device status {code} after the sustained leg")
+        sus_ms, _ = max_over_ranks(ev0.elapsed_time(ev1), [], dist, dev)
+        sus_tf = whole_job_tflops(world, n_sus, step_flops, sus_ms)
+        sustained = {"value": round(sus_tf, 2), "unit": UNIT, "steps": n_sus,
+                     "seconds": round(sus_ms / 1e3, 3), "ms_per_step": round(sus_ms / n_sus, 4),
+                     "peak": peaks["bf16_sustained"],
+                     "frac_of_sustained_peak": round(sus_tf / world / peaks["bf16_sustained"], 4),
+                     "frac_of_burst_peak": round(sus_tf / world / peaks["bf16"], 4),
+                     "l2": "not flushed (steps back to back)",
+                     "clocks": sus_clocks.summary(), "clock_bins_mhz": sus_clocks.bins()}
 
     # ---- FP8 cache: PSNR of the decode output against a bf16 cache (untimed) ---------
     psnr = None
@@ -798,6 +845,7 @@ def main():
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
+        "sustained": sustained,
         "gpu_launches": prob.launches * K,
         "clocks": clocks.summary(),
     }

@@ -68,8 +68,11 @@ enum {
                                 id outside the pool                                   */
   BCA_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, ...)    */
   BCA_ERR_TIMEOUT = 7,       /* a bounded device wait ran out; outputs are undefined   */
-  BCA_ERR_SEQLENS = 8        /* cu_seqlens not monotone, q_len > kv_len, a length above
+  BCA_ERR_SEQLENS = 8,       /* cu_seqlens not monotone, q_len > kv_len, a length above
                                 max_seqlen_*, or a cache prefix longer than its keys   */
+  BCA_ERR_BOUNDS = 9         /* bounds-checked build only (libbca_gb300_debug.so): a
+                                computed index, TMA coordinate or store address fell
+                                outside its buffer; the access was skipped            */
 };
 
 /* Human-readable name of a status code (static string). */
@@ -272,8 +275,8 @@ bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void*
  * compute-for-memory trade": two tensors per layer, H heads x 128 values).
  * k, v: device bf16 [total_k, H, 128] packed by cu_seqlens_k; cache_k/v:
  * device bf16 [num_layers][H][capacity][128].  Nothing is written when
- * cu_prefix[batch] > capacity (BCA_ERR_CAPACITY) or a prefix is longer than
- * its sequence (BCA_ERR_SEQLENS).
+ * cu_prefix[batch] > capacity (BCA_ERR_CAPACITY), or a prefix is longer than
+ * its sequence or its source keys run past total_k (BCA_ERR_SEQLENS).
  */
 bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* cu_seqlens_k,
                                    const int32_t* cu_prefix, int32_t batch, int32_t num_heads,
@@ -366,7 +369,8 @@ bca_status bca_prefix_decode_fp8(const void* q_tgt, const void* cache_k, const v
  * device int32 [batch][n_ids] (n_ids <= 4096, else BCA_ERR_UNSUPPORTED).  A
  * sequence with an id >= n_ids or < -1, an id in two runs, or a block whose
  * length is not a multiple of its width is reported as BCA_ERR_BLOCK_ID and
- * its coordinates are not written. */
+ * its coordinates are not written; so is (as BCA_ERR_SEQLENS) a sequence whose
+ * tokens [cu_seqlens[b], cu_seqlens[b+1]) do not lie in [0, total). */
 bca_status bca_rope_positions(const int32_t* block_id, const int32_t* cu_seqlens, int32_t batch,
                               int32_t total, const int32_t* grid_w, int32_t n_ids,
                               int32_t* pos3, int32_t* status_dev, void* stream);

@@ -3,16 +3,24 @@
 The library is built in-tree by ``prefix_kv_gb300.build_native`` (or
 ``__graft_entry__.build()``).  If it is missing, every call raises: there is no
 fallback implementation.
+
+``libbca_gb300_debug.so`` is the same library compiled with device-side bounds
+checks (a failed check skips the access and reports ``BCA_ERR_BOUNDS``);
+``using_debug()`` routes every binding call through it for a ``with`` block.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
 
-_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libbca_gb300.so")
+_LIB_DIR = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib")
+_LIB_PATH = os.path.join(_LIB_DIR, "libbca_gb300.so")
+_DEBUG_PATH = os.path.join(_LIB_DIR, "libbca_gb300_debug.so")
 _lock = threading.Lock()
-_lib = None
+_libs = {}
+_lib = None          # the library the bindings call (release unless using_debug() is active)
 
 c_i32, c_i64, c_f32, c_size, c_vp = (ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                       ctypes.c_size_t, ctypes.c_void_p)
@@ -90,24 +98,47 @@ def lib_path() -> str:
     return _LIB_PATH
 
 
-def load():
-    """Load the shared library (once) and attach the C signatures."""
-    global _lib
-    if _lib is not None:
-        return _lib
+def _open(path: str):
     with _lock:
-        if _lib is None:
-            if not os.path.exists(_LIB_PATH):
+        if path not in _libs:
+            if not os.path.exists(path):
                 raise RuntimeError(
-                    f"CUDA library {_LIB_PATH} is not built; run "
+                    f"CUDA library {path} is not built; run "
                     "`python -c 'import __graft_entry__ as g; g.build()'` first")
-            lib = ctypes.CDLL(_LIB_PATH)
+            lib = ctypes.CDLL(path)
             for name, (res, args) in SIGNATURES.items():
                 fn = getattr(lib, name)
                 fn.restype = res
                 fn.argtypes = args
-            _lib = lib
+            _libs[path] = lib
+        return _libs[path]
+
+
+def load():
+    """The library the bindings call: the release build (loaded once with its C
+    signatures), or the bounds-checked build inside ``using_debug()``."""
+    global _lib
+    if _lib is None:
+        _lib = _open(_LIB_PATH)
     return _lib
+
+
+def load_debug():
+    """The bounds-checked build, ``libbca_gb300_debug.so``."""
+    return _open(_DEBUG_PATH)
+
+
+@contextlib.contextmanager
+def using_debug():
+    """Route every binding call through the bounds-checked build (not thread-safe:
+    meant for tests)."""
+    global _lib
+    prev = load()
+    _lib = load_debug()
+    try:
+        yield _lib
+    finally:
+        _lib = prev
 
 
 class BcaError(RuntimeError):

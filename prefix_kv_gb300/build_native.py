@@ -115,6 +115,13 @@ def build(force: bool = False, verbose: bool = False, debug: bool = False) -> st
     return lib
 
 
+def build_all(force: bool = False) -> None:
+    """Build the release and the bounds-checked library side by side."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        for f in [ex.submit(build, force, False, d) for d in (False, True)]:
+            f.result()
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
                 debug="--debug" in sys.argv))

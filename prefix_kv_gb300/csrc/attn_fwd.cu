@@ -100,6 +100,7 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 struct FwdParams {
   int num_heads;
   int total_q;
+  int total_k;                // prefill: rows of k and v
   int tiles_per_seq;
   float scale_log2;
   int64_t capacity;
@@ -170,7 +171,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     for (int i = 0; i < 2; ++i) {
       nkt[i] = 0;
       const int m = m_base + i;
-      if (rows_valid[i] > 0 && m < p.tiles_per_seq) {
+      if (rows_valid[i] > 0 && m < p.tiles_per_seq && BCA_IN_BOUNDS(p.status, b < p.batch)) {
         const PrefillTile t = p.tiles[b * p.tiles_per_seq + m];
         k_hi[i] = t.k_hi;
         k_min[i] = t.k_min;
@@ -238,6 +239,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   };
 
   // ---- set-up -----------------------------------------------------------------
+  bool q_armed = false;   // (TMA producer lane) the query loads were issued
   if (warp == kWarpTma && lane == 0) {
     mbar_init(&sm.q_full, 1);
     for (int s = 0; s < kStages; ++s) {
@@ -259,11 +261,17 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     // The query tiles are loaded at once, before the rest of the set-up: they
     // come from DRAM and are the first MMA's operands.
     const int n_q = !kSplit && rows_valid[1] > 0 ? 2 : 1;
-    mbar_arrive_expect_tx(&sm.q_full, n_q * kTileBytes);
-    for (int i = 0; i < n_q; ++i) {
-      const int row0 = q_seq0 + (m_base + i) * kBlockM;
-      tma_load_3d(&tm_q, &sm.q_full, sm.q[i], 0, h, row0);
-      tma_load_3d(&tm_q, &sm.q_full, sm.q[i] + kHalfBytes, 64, h, row0);
+    q_armed = BCA_IN_BOUNDS(p.status, h < p.num_heads && q_seq0 + m_base * kBlockM >= 0 &&
+                                          q_seq0 + (m_base + n_q - 1) * kBlockM < p.total_q);
+    if (q_armed) {
+      mbar_arrive_expect_tx(&sm.q_full, n_q * kTileBytes);
+      for (int i = 0; i < n_q; ++i) {
+        const int row0 = q_seq0 + (m_base + i) * kBlockM;
+        tma_load_3d(&tm_q, &sm.q_full, sm.q[i], 0, h, row0);
+        tma_load_3d(&tm_q, &sm.q_full, sm.q[i] + kHalfBytes, 64, h, row0);
+      }
+    } else {
+      sm.abort = 1;
     }
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -306,28 +314,39 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
           give_up();
           return false;
         }
+        // the tile's map and its (dim 1, dim 2) coordinates
+        const CUtensorMap* m;
+        int c1, c2;
+        bool in_map;   // the tile starts inside its tensor (always true in the release build)
+        if constexpr (!kDecode) {
+          m = is_v ? &tm_v : &tm_k;
+          c1 = h;
+          c2 = kv_seq0 + g * kBlockN;
+          in_map = BCA_IN_BOUNDS(p.status, c2 >= 0 && c2 < p.total_k && h < p.num_heads);
+        } else if (g < n_pre_tiles) {
+          m = is_v ? &tm_v : &tm_k;
+          c1 = p.page_table != nullptr
+                   ? p.page_table[static_cast<int64_t>(b) * p.max_pages + g] * kBlockN
+                   : pre0 + g * kBlockN;
+          c2 = h;
+          in_map = BCA_IN_BOUNDS(p.status, (p.page_table == nullptr || g < p.max_pages) &&
+                                               c1 >= 0 && c1 < p.capacity && h < p.num_heads);
+        } else {
+          m = is_v ? &tm_v2 : &tm_k2;
+          c1 = h;
+          c2 = q_seq0 + (g - n_pre_tiles) * kBlockN;
+          in_map = BCA_IN_BOUNDS(p.status, c2 >= 0 && c2 < p.total_q && h < p.num_heads);
+        }
+        if (!in_map) {
+          *abort_flag = 1;
+          return false;
+        }
         mbar_arrive_expect_tx(&sm.kv_full[s], kTileBytes);
         armed |= 1u << s;
         parity = (parity & ~(1u << s)) | (static_cast<uint32_t>(r & 1) << s);
         uint8_t* dst = sm.kv[s];
-        if constexpr (!kDecode) {
-          const CUtensorMap* m = is_v ? &tm_v : &tm_k;
-          const int tok = kv_seq0 + g * kBlockN;
-          tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
-          tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
-        } else if (g < n_pre_tiles) {
-          const CUtensorMap* m = is_v ? &tm_v : &tm_k;
-          const int tok = p.page_table != nullptr
-                              ? p.page_table[static_cast<int64_t>(b) * p.max_pages + g] * kBlockN
-                              : pre0 + g * kBlockN;
-          tma_load_3d(m, &sm.kv_full[s], dst, 0, tok, h);
-          tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, tok, h);
-        } else {
-          const CUtensorMap* m = is_v ? &tm_v2 : &tm_k2;
-          const int tok = q_seq0 + (g - n_pre_tiles) * kBlockN;
-          tma_load_3d(m, &sm.kv_full[s], dst, 0, h, tok);
-          tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, h, tok);
-        }
+        tma_load_3d(m, &sm.kv_full[s], dst, 0, c1, c2);
+        tma_load_3d(m, &sm.kv_full[s], dst + kHalfBytes, 64, c1, c2);
         return true;
       };
       if constexpr (!kSplit) {
@@ -351,7 +370,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       if (*abort_flag) {
         for (int s = 0; s < kStages; ++s)
           if (armed >> s & 1) mbar_wait(&sm.kv_full[s], parity >> s & 1, nullptr, kWaitLimitNs / 4);
-        mbar_wait(&sm.q_full, 0, nullptr, kWaitLimitNs / 4);
+        if (q_armed) mbar_wait(&sm.q_full, 0, nullptr, kWaitLimitNs / 4);
       }
     }
    } else if (warp == kWarpMma) {
@@ -490,9 +509,13 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
         if (lane == 0) give_up();
         break;
       }
-      uint8_t* vb = sm.kv[*reinterpret_cast<volatile int*>(&sm.fix_stage)];
+      const int fix_stage = *reinterpret_cast<volatile int*>(&sm.fix_stage);
       const int seg_left = *reinterpret_cast<volatile int*>(&sm.fix_from);
-      const int nrows = kBlockN - seg_left;
+      uint8_t* vb = sm.kv[fix_stage];
+      const int nrows = BCA_IN_BOUNDS(p.status, fix_stage >= 0 && fix_stage < kStages &&
+                                                    seg_left >= 0 && seg_left < kBlockN)
+                            ? kBlockN - seg_left
+                            : 0;
       for (int idx = lane; idx < nrows * 16; idx += 32) {
         const int row = seg_left + (idx >> 4);
         const int chunk = idx & 15;
@@ -553,7 +576,13 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
           tok0 = static_cast<int64_t>(p.page_table[static_cast<int64_t>(b) * p.max_pages + j]) *
                  kBlockN;
       }
-      if (rows == kBlockN) {
+      // the tile's cache rows [tok0, tok0 + rows) lie in the layer (bounds-checked build)
+      const bool rows_in = rows <= 0 || BCA_IN_BOUNDS(p.status, tok0 >= 0 && tok0 + rows <= p.capacity &&
+                                                                    h < p.num_heads &&
+                                                                    (!kPagedAppend || j < p.max_pages));
+      if (!rows_in) {
+        // skip the tile
+      } else if (rows == kBlockN) {
         // a whole tile: two TMA stores through the cache map (same 128-byte swizzled
         // layout as the loads), read out of shared memory before the stage is freed
         if (lane == 0) {
@@ -598,7 +627,10 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     const bool row_valid = row < rows_valid[qi];
     const bool releaser = !kSplit && (qi == 1 || nkt[1] == 0);
     int e_row = 0;
-    if constexpr (!kDecode) e_row = row_valid ? p.row_end[row0 + row] : k_hi[qi];
+    if constexpr (!kDecode)
+      e_row = row_valid && BCA_IN_BOUNDS(p.status, row0 + row >= 0 && row0 + row < p.total_q)
+                  ? p.row_end[row0 + row]
+                  : k_hi[qi];
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY;   // reference max of the row, log2 domain
     float l_run = 0.f;
@@ -748,6 +780,9 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
           const float c0 = a0 * inv_l, c1 = a1 * inv_l;
           __nv_bfloat16* orow =
               p.out + (static_cast<size_t>(row0 + row) * p.num_heads + h) * kHeadDim;
+          const bool row_out = row_valid && BCA_IN_BOUNDS(p.status, row0 + row >= 0 &&
+                                                                        row0 + row < p.total_q &&
+                                                                        h < p.num_heads);
 #pragma unroll 1
           for (int c = 0; c < 8; ++c) {
             uint32_t r0[16], r1[16];
@@ -764,13 +799,13 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
               w[x] = pack_bf16x2(
                   __uint_as_float(r0[2 * x]) * c0 + __uint_as_float(r1[2 * x]) * c1,
                   __uint_as_float(r0[2 * x + 1]) * c0 + __uint_as_float(r1[2 * x + 1]) * c1);
-            if (row_valid) {
+            if (row_out) {
               uint4* dst = reinterpret_cast<uint4*>(orow + c * 16);
               dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
               dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
             }
           }
-          if (row_valid) {
+          if (row_out) {
             p.lse[static_cast<size_t>(h) * p.total_q + row0 + row] =
                 (m_fin + log2f(l_fin)) * 0.69314718055994530942f;
           }
@@ -792,6 +827,9 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
         uint8_t* const stage = sm.q[qi];
         __nv_bfloat16* orow =
             p.out + (static_cast<size_t>(row0 + row) * p.num_heads + h) * kHeadDim;
+        const bool row_out = row_valid && BCA_IN_BOUNDS(p.status, row0 + row >= 0 &&
+                                                                      row0 + row < p.total_q &&
+                                                                      h < p.num_heads);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t r[32];
@@ -809,7 +847,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
                                         (((cc & 7) ^ (row & 7)) * 16)) =
                   make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
             }
-          } else if (row_valid) {
+          } else if (row_out) {
             uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
             for (int x = 0; x < 4; ++x)
@@ -821,16 +859,19 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
           mbar_arrive(&sm.epi[qi]);
           if (wq == 0 && lane == 0) {
             if (mbar_wait(&sm.epi[qi], 0, abort_flag, kWaitLimitNs)) {
-              tma_store_3d(&tm_o, stage, 0, h, row0);
-              tma_store_3d(&tm_o, stage + kHalfBytes, 64, h, row0);
-              bulk_commit_group();
-              bulk_wait_all();   // complete before the CTA ends
+              if (BCA_IN_BOUNDS(p.status, row0 >= 0 && row0 + kBlockM <= p.total_q &&
+                                              h < p.num_heads)) {
+                tma_store_3d(&tm_o, stage, 0, h, row0);
+                tma_store_3d(&tm_o, stage + kHalfBytes, 64, h, row0);
+                bulk_commit_group();
+                bulk_wait_all();   // complete before the CTA ends
+              }
             } else {
               give_up();
             }
           }
         }
-        if (row_valid) {
+        if (row_out) {
           p.lse[static_cast<size_t>(h) * p.total_q + row0 + row] =
               (m_ref + log2f(l_run)) * 0.69314718055994530942f;
         }
@@ -964,6 +1005,7 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   FwdParams p{};
   p.num_heads = a.num_heads;
   p.total_q = a.total_q;
+  p.total_k = a.total_k;
   p.tiles_per_seq = a.tiles_per_seq;
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
   p.capacity = a.capacity;

@@ -150,7 +150,7 @@ bca_status append_fp8_impl(const void* k, const void* v, const int32_t* cu_seqle
   const size_t rows = static_cast<size_t>(num_heads) * capacity;   // per layer
   const size_t k_bytes = quant_k ? 1 : 2;
   cudaError_t e = launch_cache_append_fp8(
-      k, v, cu_seqlens_k, cu_prefix, batch, num_heads, quant_k,
+      k, v, cu_seqlens_k, cu_prefix, batch, num_heads, total_k, quant_k,
       static_cast<uint8_t*>(cache_k) + layer * rows * kHeadDim * k_bytes,
       static_cast<uint8_t*>(cache_v) + layer * rows * kHeadDim,
       quant_k ? scale_k + layer * rows : nullptr, scale_v + layer * rows, capacity, page_table,
@@ -173,6 +173,7 @@ const char* bca_status_string(bca_status s) {
     case BCA_ERR_CUDA: return "CUDA runtime error";
     case BCA_ERR_TIMEOUT: return "device wait timed out";
     case BCA_ERR_SEQLENS: return "invalid cu_seqlens / lengths";
+    case BCA_ERR_BOUNDS: return "index outside its buffer (bounds-checked build)";
     default: return "unknown status";
   }
 }
@@ -464,7 +465,7 @@ bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* 
     return BCA_ERR_INVALID_ARG;
   const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
   cudaError_t e = launch_cache_append(
-      k, v, cu_seqlens_k, cu_prefix, batch, num_heads,
+      k, v, cu_seqlens_k, cu_prefix, batch, num_heads, total_k,
       static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems,
       static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, capacity, nullptr, 0,
       status_dev, static_cast<cudaStream_t>(stream));
@@ -490,7 +491,7 @@ bca_status bca_prefix_cache_append_paged(const void* k, const void* v,
   const int64_t capacity = static_cast<int64_t>(num_pages) * kBlockN;
   const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
   cudaError_t e = launch_cache_append(
-      k, v, cu_seqlens_k, cu_prefix, batch, num_heads,
+      k, v, cu_seqlens_k, cu_prefix, batch, num_heads, total_k,
       static_cast<__nv_bfloat16*>(cache_k) + layer * layer_elems,
       static_cast<__nv_bfloat16*>(cache_v) + layer * layer_elems, capacity, page_table,
       max_pages, status_dev, static_cast<cudaStream_t>(stream));
@@ -598,7 +599,7 @@ bca_status bca_rope_positions(const int32_t* block_id, const int32_t* cu_seqlens
   if (batch == 0 || total == 0) return BCA_OK;
   if (!block_id || !cu_seqlens || !pos3 || (n_ids > 0 && !grid_w)) return BCA_ERR_INVALID_ARG;
   if (n_ids > 4096 || batch > 65535) return BCA_ERR_UNSUPPORTED;
-  const cudaError_t e = launch_rope_positions(block_id, cu_seqlens, batch, grid_w, n_ids, pos3,
+  const cudaError_t e = launch_rope_positions(block_id, cu_seqlens, batch, total, grid_w, n_ids, pos3,
                                               status_dev, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
 }

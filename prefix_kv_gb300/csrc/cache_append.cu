@@ -54,7 +54,8 @@ __device__ int check_pages(const int32_t* __restrict__ page_table, int max_pages
 __global__ void __launch_bounds__(kAppendThreads)
     cache_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                         const int32_t* __restrict__ cu_k, const int32_t* __restrict__ cu_prefix,
-                        int batch, int num_heads, uint4* __restrict__ ck, uint4* __restrict__ cv,
+                        int batch, int num_heads, int total_k, uint4* __restrict__ ck,
+                        uint4* __restrict__ cv,
                         int64_t capacity, const int32_t* __restrict__ page_table, int max_pages,
                         int32_t* status) {
   __shared__ int s_cp[kMaxBatchSmem + 1];
@@ -77,7 +78,9 @@ __global__ void __launch_bounds__(kAppendThreads)
   for (int i = threadIdx.x; i < batch; i += blockDim.x) {
     const int pl = cp[i + 1] - cp[i];
     const int kl = ckk[i + 1] - ckk[i];
-    if (pl < 0 || pl > kl || cp[i] < 0) s_bad = BCA_ERR_SEQLENS;
+    // the prefix's source keys [cu_k[i], cu_k[i] + pl) must lie in [0, total_k)
+    if (pl < 0 || pl > kl || cp[i] < 0 || ckk[i] < 0 || ckk[i] > total_k - pl)
+      s_bad = BCA_ERR_SEQLENS;
   }
   if (page_table == nullptr) {
     if (threadIdx.x == 0 && static_cast<int64_t>(cp[batch]) > capacity) s_bad = BCA_ERR_CAPACITY;
@@ -115,9 +118,12 @@ __global__ void __launch_bounds__(kAppendThreads)
         const int64_t src_tok = static_cast<int64_t>(ckk[lo]) + (c - cp[lo]);
         const int64_t src = (src_tok * num_heads + hh) * 16 + x;
         const int64_t ctok = cache_token(page_table, max_pages, cp, lo, c - cp[lo]);
-        dst[u] = (static_cast<int64_t>(hh) * capacity + ctok) * 16 + x;
-        rk[u] = __ldcs(k + src);
-        rv[u] = __ldcs(v + src);
+        if (BCA_IN_BOUNDS(status, src_tok >= 0 && src_tok < total_k && ctok >= 0 &&
+                                      ctok < capacity)) {
+          dst[u] = (static_cast<int64_t>(hh) * capacity + ctok) * 16 + x;
+          rk[u] = __ldcs(k + src);
+          rv[u] = __ldcs(v + src);
+        }
       }
     }
 #pragma unroll
@@ -133,7 +139,7 @@ __global__ void __launch_bounds__(kAppendThreads)
 }  // namespace
 
 cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_k,
-                                const int32_t* cu_prefix, int batch, int num_heads,
+                                const int32_t* cu_prefix, int batch, int num_heads, int total_k,
                                 void* cache_k_layer, void* cache_v_layer, int64_t capacity,
                                 const int32_t* page_table, int max_pages, int32_t* status,
                                 cudaStream_t stream) {
@@ -143,8 +149,8 @@ cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_
   const int grid = sms * 8;
   cache_append_kernel<<<grid, kAppendThreads, 0, stream>>>(
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
-      num_heads, static_cast<uint4*>(cache_k_layer), static_cast<uint4*>(cache_v_layer), capacity,
-      page_table, max_pages, status);
+      num_heads, total_k, static_cast<uint4*>(cache_k_layer), static_cast<uint4*>(cache_v_layer),
+      capacity, page_table, max_pages, status);
   return cudaGetLastError();
 }
 
@@ -228,7 +234,8 @@ template <bool kQuantK>
 __global__ void __launch_bounds__(256)
     cache_append_fp8_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
                             const int32_t* __restrict__ cu_k, const int32_t* __restrict__ cu_prefix,
-                            int batch, int num_heads, void* __restrict__ ck, uint2* __restrict__ cv,
+                            int batch, int num_heads, int total_k, void* __restrict__ ck,
+                            uint2* __restrict__ cv,
                             float* __restrict__ sk, float* __restrict__ sv, int64_t capacity,
                             const int32_t* __restrict__ page_table, int max_pages,
                             int32_t* status) {
@@ -238,7 +245,8 @@ __global__ void __launch_bounds__(256)
   for (int i = threadIdx.x; i < batch; i += blockDim.x) {
     const int pl = cu_prefix[i + 1] - cu_prefix[i];
     const int kl = cu_k[i + 1] - cu_k[i];
-    if (pl < 0 || pl > kl || cu_prefix[i] < 0) s_bad = BCA_ERR_SEQLENS;
+    if (pl < 0 || pl > kl || cu_prefix[i] < 0 || cu_k[i] < 0 || cu_k[i] > total_k - pl)
+      s_bad = BCA_ERR_SEQLENS;
   }
   if (page_table == nullptr) {
     if (threadIdx.x == 0 && static_cast<int64_t>(cu_prefix[batch]) > capacity)
@@ -258,6 +266,7 @@ __global__ void __launch_bounds__(256)
   // Row (token, head) of the prefix region -> source vector and cache row.
   struct Where {
     int64_t src, dst_row;
+    bool in;   // source token and cache row inside their buffers (bounds-checked build)
   };
   auto locate = [&](int64_t row) {
     const int c = static_cast<int>(row / num_heads) + p0;       // cache token
@@ -268,9 +277,11 @@ __global__ void __launch_bounds__(256)
       if (cu_prefix[mid] <= c) lo = mid; else hi = mid - 1;
     }
     const int64_t src_tok = static_cast<int64_t>(cu_k[lo]) + (c - cu_prefix[lo]);
+    const int64_t ctok = cache_token(page_table, max_pages, cu_prefix, lo, c - cu_prefix[lo]);
     return Where{(src_tok * num_heads + hh) * 16 + lane16,
-                 static_cast<int64_t>(hh) * capacity +
-                     cache_token(page_table, max_pages, cu_prefix, lo, c - cu_prefix[lo])};
+                 static_cast<int64_t>(hh) * capacity + ctok,
+                 BCA_IN_BOUNDS(status, src_tok >= 0 && src_tok < total_k && ctok >= 0 &&
+                                           ctok < capacity)};
   };
   // Two rows per warp (16 lanes each; all 32 lanes stay together for the shuffles)
   // and two such row pairs per pass, with all four loads issued before any
@@ -286,6 +297,13 @@ __global__ void __launch_bounds__(256)
       const int64_t row = (r2 + u * warps) * 2 + ((threadIdx.x >> 4) & 1);
       live[u] = row < rows;
       const Where w = locate(live[u] ? row : rows - 1);
+      if (!w.in) {   // skip the row (bounds-checked build); the lanes stay together
+        live[u] = false;
+        src[u] = 0;
+        dst_row[u] = 0;
+        vraw[u] = kraw[u] = make_uint4(0, 0, 0, 0);
+        continue;
+      }
       src[u] = w.src;
       dst_row[u] = w.dst_row;
       vraw[u] = __ldcs(v + src[u]);
@@ -316,7 +334,7 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t* cu_k,
                                     const int32_t* cu_prefix, int batch, int num_heads,
-                                    bool quant_k, void* cache_k_layer, void* cache_v_layer,
+                                    int total_k, bool quant_k, void* cache_k_layer, void* cache_v_layer,
                                     float* scale_k_layer, float* scale_v_layer, int64_t capacity,
                                     const int32_t* page_table, int max_pages, int32_t* status,
                                     cudaStream_t stream) {
@@ -327,12 +345,12 @@ cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t*
   if (quant_k) {
     cache_append_fp8_kernel<true><<<grid, 256, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
-        num_heads, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
+        num_heads, total_k, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
         scale_v_layer, capacity, page_table, max_pages, status);
   } else {
     cache_append_fp8_kernel<false><<<grid, 256, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
-        num_heads, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
+        num_heads, total_k, cache_k_layer, static_cast<uint2*>(cache_v_layer), scale_k_layer,
         scale_v_layer, capacity, page_table, max_pages, status);
   }
   return cudaGetLastError();
@@ -368,6 +386,9 @@ __global__ void __launch_bounds__(256)
     const int hh = static_cast<int>(row_in / tokens);
     const int64_t row = static_cast<int64_t>(hh) * capacity + p0 + (row_in - hh * tokens);
     const int x = static_cast<int>(c & 7);
+    if (!BCA_IN_BOUNDS(status, hh < num_heads && row >= 0 &&
+                                   row < static_cast<int64_t>(num_heads) * capacity))
+      continue;
     const uint4 raw = __ldcs(codes + row * 8 + x);
     const float sc = __ldg(scales + row);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -449,6 +470,10 @@ __global__ void __launch_bounds__(256)
                                                           c - cu_prefix[lo]);
     const int64_t dst_row = static_cast<int64_t>(hh) * out_rows + c;
     const int x = static_cast<int>(ch & 7);
+    if (!BCA_IN_BOUNDS(status, hh < num_heads && src_row >= 0 &&
+                                   src_row < static_cast<int64_t>(num_heads) * capacity &&
+                                   c >= 0 && c < out_rows))
+      continue;
     if constexpr (kFp8) {
       const uint4 raw = __ldcs(static_cast<const uint4*>(src) + src_row * 8 + x);
       const float sc = __ldg(scales + src_row);

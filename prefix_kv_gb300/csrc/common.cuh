@@ -19,6 +19,22 @@ __device__ __forceinline__ void report_status(int32_t* status, int32_t code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
+// Bounds-checked build (-DBCA_BOUNDS_CHECK, libbca_gb300_debug.so): the kernels test
+// every computed global index, TMA coordinate and workspace or cache index against
+// the extent of its buffer before the access.  A failed test skips the access and
+// writes BCA_ERR_BOUNDS to the status word; it never traps.  It stands in for a
+// memory checker.  In the release build BCA_IN_BOUNDS is the constant true and
+// its condition is not evaluated.
+#ifdef BCA_BOUNDS_CHECK
+__device__ __forceinline__ bool bounds_ok(bool ok, int32_t* status) {
+  if (!ok) report_status(status, BCA_ERR_BOUNDS);
+  return ok;
+}
+#define BCA_IN_BOUNDS(status, cond) (::bca::bounds_ok((cond), (status)))
+#else
+#define BCA_IN_BOUNDS(status, cond) (true)
+#endif
+
 struct PrefillTile {  // one record per (sequence, 128-row query tile)
   int32_t k_hi;       // max visible-key end over the tile's valid rows (0: no work)
   int32_t k_min;      // min visible-key end over the tile's valid rows

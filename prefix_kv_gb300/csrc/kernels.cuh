@@ -8,7 +8,7 @@ namespace bca {
 
 // page_table (device int32 [batch][max_pages]) or null for the contiguous cache
 cudaError_t launch_cache_append(const void* k, const void* v, const int32_t* cu_k,
-                                const int32_t* cu_prefix, int batch, int num_heads,
+                                const int32_t* cu_prefix, int batch, int num_heads, int total_k,
                                 void* cache_k_layer, void* cache_v_layer, int64_t capacity,
                                 const int32_t* page_table, int max_pages, int32_t* status,
                                 cudaStream_t stream);
@@ -19,7 +19,7 @@ cudaError_t launch_cache_copy_rows(void* cache_k_layer, void* cache_v_layer, int
 
 cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t* cu_k,
                                     const int32_t* cu_prefix, int batch, int num_heads,
-                                    bool quant_k, void* cache_k_layer, void* cache_v_layer,
+                                    int total_k, bool quant_k, void* cache_k_layer, void* cache_v_layer,
                                     float* scale_k_layer, float* scale_v_layer, int64_t capacity,
                                     const int32_t* page_table, int max_pages, int32_t* status,
                                     cudaStream_t stream);
@@ -39,7 +39,7 @@ cudaError_t launch_cache_dequant_fp8(const void* codes_layer, const float* scale
 
 // Three-axis RoPE coordinates [total][3] (frame, height, width) of packed tokens.
 cudaError_t launch_rope_positions(const int32_t* block_id, const int32_t* cu_seqlens, int batch,
-                                  const int32_t* grid_w, int n_ids, int32_t* pos3,
+                                  int total, const int32_t* grid_w, int n_ids, int32_t* pos3,
                                   int32_t* status, cudaStream_t stream);
 // (cos, sin) of the 64 dimension pairs per token, float [total][64][2].
 cudaError_t launch_rope_table(const int32_t* pos3, int64_t total, float* table,

@@ -67,7 +67,7 @@ __device__ __forceinline__ int block_incl_scan(int x, int* buf, int& all) {
 
 __global__ void __launch_bounds__(kPosThreads)
     rope_positions_kernel(const int32_t* __restrict__ bid, const int32_t* __restrict__ cu,
-                          const int32_t* __restrict__ grid_w, int n_ids,
+                          const int32_t* __restrict__ grid_w, int n_ids, int total,
                           int32_t* __restrict__ pos3, int32_t* status) {
   extern __shared__ int dyn[];
   int* cnt = dyn;                 // tokens of each image id in this sequence
@@ -80,7 +80,8 @@ __global__ void __launch_bounds__(kPosThreads)
     cnt[i] = 0;
     starts[i] = 0;
   }
-  if (tid == 0) err = (t1 < t0) ? BCA_ERR_SEQLENS : 0;
+  // the sequence's tokens must lie in [0, total): nothing is read or written otherwise
+  if (tid == 0) err = (t1 < t0 || t0 < 0 || t1 > total) ? BCA_ERR_SEQLENS : 0;
   __syncthreads();
   // pass 1: image block sizes, one run per id
   for (int t = t0 + tid; t < t1; t += kPosThreads) {
@@ -117,7 +118,9 @@ __global__ void __launch_bounds__(kPosThreads)
     const int s = max(carry_start, block_incl_scan<true>(start ? t : -1, buf, max_all));
     if (valid) {
       int32_t* out = pos3 + static_cast<int64_t>(t) * 3;
-      if (id < 0) {
+      if (!BCA_IN_BOUNDS(status, t >= 0 && t < total)) {
+        // skipped (bounds-checked build)
+      } else if (id < 0) {
         out[0] = a_excl;
         out[1] = a_excl;
         out[2] = a_excl;
@@ -298,7 +301,8 @@ __global__ void __launch_bounds__(kPrologueThreads, 4)
     if (!live) continue;
     q_out[rr * 16 + l16] = qo;
     k_out[rr * 16 + l16] = ko;
-    if (kAppend && crow >= 0) {
+    if (kAppend && crow >= 0 &&
+        BCA_IN_BOUNDS(status, crow < static_cast<int64_t>(num_heads) * capacity)) {
       ck[crow * 16 + l16] = ko;
       cv[crow * 16 + l16] = vraw;
     }
@@ -308,11 +312,11 @@ __global__ void __launch_bounds__(kPrologueThreads, 4)
 }  // namespace
 
 cudaError_t launch_rope_positions(const int32_t* block_id, const int32_t* cu_seqlens, int batch,
-                                  const int32_t* grid_w, int n_ids, int32_t* pos3,
+                                  int total, const int32_t* grid_w, int n_ids, int32_t* pos3,
                                   int32_t* status, cudaStream_t stream) {
   const size_t smem = static_cast<size_t>(2) * n_ids * sizeof(int);
   rope_positions_kernel<<<batch, kPosThreads, smem, stream>>>(block_id, cu_seqlens, grid_w, n_ids,
-                                                              pos3, status);
+                                                              total, pos3, status);
   return cudaGetLastError();
 }
 

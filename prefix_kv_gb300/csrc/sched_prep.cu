@@ -94,9 +94,10 @@ __global__ void __launch_bounds__(kPrepThreads)
 #pragma unroll
       for (int u = 0; u < kPerThread; ++u) {
         const int j = u * kPrepThreads + tid;
-        if (j < n) ids[j] = bid[k0 + base + j];
+        if (j < n && BCA_IN_BOUNDS(status, k0 + base + j < total_k)) ids[j] = bid[k0 + base + j];
       }
-      if (tid == 0 && kChunk < n) ids[kChunk] = bid[k0 + base + kChunk];
+      if (tid == 0 && kChunk < n && BCA_IN_BOUNDS(status, k0 + base + kChunk < total_k))
+        ids[kChunk] = bid[k0 + base + kChunk];
       __syncthreads();
       // thread t looks at positions base + 8t .. base + 8t + 7 (read as two 16-byte
       // vectors plus the next id: scalar reads 8 words apart conflicted 8-way)
@@ -158,7 +159,8 @@ __global__ void __launch_bounds__(kPrepThreads)
   if (err != 0) {
     if (tid == 0) report_status(status, err);
     for (int m = tid; m < tiles_per_seq; m += kPrepThreads)
-      tiles[b * tiles_per_seq + m] = PrefillTile{0, 0, 0, 0};
+      if (BCA_IN_BOUNDS(status, b < static_cast<int>(gridDim.x)))
+        tiles[b * tiles_per_seq + m] = PrefillTile{0, 0, 0, 0};
     return;
   }
 
@@ -174,7 +176,9 @@ __global__ void __launch_bounds__(kPrepThreads)
 #pragma unroll
     for (int u = 0; u < kPerThread; ++u) {
       const int i = base + u * kPrepThreads + tid;
-      ids_row[u] = i < q_len ? bid[k0 + kv_len - q_len + i] : -1;
+      ids_row[u] = i < q_len && BCA_IN_BOUNDS(status, k0 + kv_len - q_len + i < total_k)
+                       ? bid[k0 + kv_len - q_len + i]
+                       : -1;
     }
 #pragma unroll
     for (int u = 0; u < kPerThread; ++u) {
@@ -193,7 +197,7 @@ __global__ void __launch_bounds__(kPrepThreads)
           }
           e = run_end[lo];
         }
-        row_end[q0 + i] = e;
+        if (BCA_IN_BOUNDS(status, q0 + i >= 0 && q0 + i < total_q)) row_end[q0 + i] = e;
       }
       const int vmax = __reduce_max_sync(0xffffffffu, valid ? e : 0);
       const int vmin = __reduce_min_sync(0xffffffffu, valid ? e : 0x7fffffff);
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(kPrepThreads)
       const int u = tid / (kPrepThreads / kBlockM);
       const int w0 = (tid % (kPrepThreads / kBlockM)) * (kBlockM / 32);
       const int m = (base + u * kPrepThreads) / kBlockM + tid % (kPrepThreads / kBlockM);
-      if (m < tiles_per_seq) {
+      if (m < tiles_per_seq && BCA_IN_BOUNDS(status, b < static_cast<int>(gridDim.x))) {
         int tmax = 0, tmin = 0x7fffffff, tcnt = 0;
         for (int w = w0; w < w0 + kBlockM / 32; ++w) {
           tmax = max(tmax, red[0][u][w]);

@@ -62,7 +62,7 @@ def test_binding_arity_matches_header():
 
 def test_status_strings(lib):
     assert lib.bca_status_string(0) == b"ok"
-    for code in range(1, 9):
+    for code in range(1, 10):
         assert lib.bca_status_string(code) not in (b"ok", b"unknown status")
     assert lib.bca_status_string(99) == b"unknown status"
     assert lib.bca_version() >= 100

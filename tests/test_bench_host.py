@@ -55,3 +55,18 @@ def test_reference_arm_line():
     assert d["cpu_baseline"]["value"] == d["value"] == d["e2e"]["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"] == "tiny_mixed_s40"
+
+
+def test_clock_sampler_summary_and_bins():
+    # nvidia-smi lines (index, sm, max, power, active, hw, hw_thermal, sw_thermal, sw_power)
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler(0)
+    c.lines = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1950, 2070, 1400.2, 0x4, Not Active, Not Active, Not Active, Active",
+               "0, 1440, 2070, 1405.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "garbage"]
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 1950 and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"]
+    assert c.bins(60) == {"1440-1500": 1, "1920-1980": 1, "2040-2100": 1}
