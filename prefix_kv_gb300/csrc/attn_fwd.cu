@@ -388,29 +388,42 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       // key 16 kk (2048 B).  Descriptor start fields are in 16-byte units; a
       // ring stage is kTileBytes / 16 apart.
       // (a key-split item has its one query tile in q[0], used by both S MMAs)
-      const uint64_t desc_q[2] = {smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024),
-                                  smem_desc_sw128(smem_u32(sm.q[kSplit ? 0 : 1]), 16, 1024)};
-      const uint64_t desc_k0 = smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024);
-      const uint64_t desc_v0 = smem_desc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024);
+      // Every descriptor shares its high word (stride, version, swizzle); the low
+      // word holds the start address and the leading-byte offset, so each MMA
+      // below costs one 32-bit add per shared-memory operand.
+      const uint64_t desc_q0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+      const uint32_t desc_hi = static_cast<uint32_t>(desc_q0 >> 32);
+      const uint32_t q_lo0 = static_cast<uint32_t>(desc_q0);
+      const uint32_t q_lo1 =
+          static_cast<uint32_t>(smem_desc_sw128(smem_u32(sm.q[kSplit ? 0 : 1]), 16, 1024));
+      const uint32_t k_lo0 = static_cast<uint32_t>(smem_desc_sw128(smem_u32(sm.kv[0]), 16, 1024));
+      const uint32_t v_lo0 =
+          static_cast<uint32_t>(smem_desc_sw128(smem_u32(sm.kv[0]), kHalfBytes, 1024));
+      constexpr uint32_t kStageLo = kTileBytes >> 4;   // one ring stage, in 16-byte units
       auto issue_s = [&](int i, int stage) {  // S_i = Q_i K^T
-        const uint64_t dk = desc_k0 + static_cast<uint64_t>(stage) * (kTileBytes >> 4);
+        const uint32_t qa = i == 0 ? q_lo0 : q_lo1;
+        const uint32_t kb = k_lo0 + static_cast<uint32_t>(stage) * kStageLo;
         const uint32_t d = tmem + kColS + i * 128;
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk) {
-          const uint64_t off = static_cast<uint64_t>((kk >> 2) * (kHalfBytes >> 4) + (kk & 3) * 2);
-          umma_ss(d, desc_q[i] + off, dk + off, idesc_qk, kk > 0);
+          constexpr uint32_t kHalfLo = kHalfBytes >> 4;
+          const uint32_t off = (kk >> 2) * kHalfLo + (kk & 3) * 2;
+          if (kk == 0)
+            umma_ss<0>(d, qa + off, kb + off, desc_hi, idesc_qk);
+          else
+            umma_ss<1>(d, qa + off, kb + off, desc_hi, idesc_qk);
         }
         umma_commit(&sm.s_full[i]);
       };
-      auto issue_pv = [&](int i, int stage, int j) {  // O_i += P_i V
-        const uint64_t dv = desc_v0 + static_cast<uint64_t>(stage) * (kTileBytes >> 4);
+      auto issue_pv = [&](int i, int stage, int j, bool last) {  // O_i += P_i V
+        const uint32_t vb = v_lo0 + static_cast<uint32_t>(stage) * kStageLo;
         const uint32_t a = tmem + kColS + i * 128;
         const uint32_t d = tmem + kColO + i * 128;
+        umma_ts<-1>(d, a, vb, desc_hi, idesc_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          umma_ts(d, a + kk * 8, dv + static_cast<uint64_t>(kk * (2048 >> 4)), idesc_pv,
-                  (j > 0 || kk > 0) ? 1u : 0u);
-        if (j == nkt[i] - 1) umma_commit(&sm.o_final[i]);
+        for (int kk = 1; kk < kBlockN / 16; ++kk)
+          umma_ts<1>(d, a + kk * 8, vb + kk * (2048 >> 4), desc_hi, idesc_pv);
+        if (last) umma_commit(&sm.o_final[i]);
       };
 
       // V tile g in stage s has landed; if its segment ends inside it, have the
@@ -446,7 +459,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
               ok = mbar_wait(&sm.p_full[i], j & 1, abort_flag, kWaitLimitNs);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(i, vs, j);
+              issue_pv(i, vs, j, j == nkt[i] - 1);
             }
             if (j + 1 < nkt[i]) {
               if (!k_next_ready) {
@@ -478,7 +491,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
                    mbar_wait(&sm.p_full[i], j & 1, abort_flag, kWaitLimitNs);
               if (!ok) break;
               tc_fence_after();
-              issue_pv(i, vs, j);
+              issue_pv(i, vs, j, j == nkt[i] - 1);
               ++c;
             }
             if (j + 1 < nkt[i]) {

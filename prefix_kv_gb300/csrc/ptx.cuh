@@ -136,24 +136,35 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]
-__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
+// tcgen05.mma, kind::f16, one CTA.  The shared-memory descriptors are passed as
+// their low words plus the high word they share: the start address and the
+// leading-byte offset sit in the low word, so moving an operand is one 32-bit
+// add, and nothing is left between two MMAs of a group but that add and the
+// predicate.  (A single issuing thread keeps the tensor pipe full only when it
+// issues an M=128, N=128 MMA within its 64-cycle execution time; 64-bit
+// descriptor arithmetic per MMA measured 72-108 cycles per MMA instead.)
+// kAcc: 1 accumulate into D, 0 overwrite it, -1 taken from `acc` at run time.
+template <int kAcc>
+__device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                        uint32_t desc_hi, uint32_t idesc, uint32_t acc = 0) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(kAcc < 0 ? acc : static_cast<uint32_t>(kAcc))
       : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                        uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] * B[smem] (B descriptor as above).
+template <int kAcc>
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                        uint32_t desc_hi, uint32_t idesc, uint32_t acc = 0) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(desc_hi), "r"(idesc), "r"(kAcc < 0 ? acc : static_cast<uint32_t>(kAcc))
       : "memory");
 }
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread has completed.
