@@ -450,7 +450,35 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
               if (nkt[i] > 0) issue_s(i, stage_of(0));
           }
         }
-        for (int j = 0; j < nk && ok; ++j) {
+        // Steady state: while both query tiles have a next key tile, every iteration
+        // issues PV0, S0, PV1, S1 with no per-tile conditions; a loop body free of
+        // branches on the tile counts measured 5.5% (prefill) and 3.7% (decode)
+        // faster than the general loop below, which then finishes the item.
+        int j = 0;
+        const int n_both = min(nkt[0], nkt[1]) - 1;
+        for (; j < n_both && ok; ++j) {
+          const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
+          if (!(landed(2 * j + 1) && fix_tail(j, vs) &&
+                mbar_wait(&sm.p_full[0], j & 1, abort_flag, kWaitLimitNs))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(0, vs, j, false);
+          if (!landed(2 * j + 2)) {
+            ok = false;
+            break;
+          }
+          issue_s(0, ks);
+          if (!mbar_wait(&sm.p_full[1], j & 1, abort_flag, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(1, vs, j, false);
+          issue_s(1, ks);
+        }
+        for (; j < nk && ok; ++j) {
           const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
           ok = landed(2 * j + 1) && fix_tail(j, vs);
           bool k_next_ready = false;
