@@ -341,7 +341,15 @@ cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t*
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = sms * 8;
+  // One wave of the grid-stride loop: as many CTAs as fit on the SMs at once (the
+  // kernel's registers allow 5 per SM, so 8 per SM ran as 1.6 uneven waves).
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          &per_sm, quant_k ? cache_append_fp8_kernel<true> : cache_append_fp8_kernel<false>, 256,
+          0) != cudaSuccess ||
+      per_sm <= 0)
+    per_sm = 4;
+  const int grid = sms * per_sm;
   if (quant_k) {
     cache_append_fp8_kernel<true><<<grid, 256, 0, stream>>>(
         static_cast<const uint4*>(k), static_cast<const uint4*>(v), cu_k, cu_prefix, batch,
