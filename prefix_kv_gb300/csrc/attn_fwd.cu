@@ -155,7 +155,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       return;
     }
   }
-  int rows_valid[2], nkt[2];
+  int rows_valid[2], nkt[2] = {0, 0};
   int k_min[2] = {0, 0}, k_hi[2] = {0, 0};
   for (int i = 0; i < 2; ++i) {
     const int m = m_base + (kSplit ? 0 : i);   // a key-split item's warpgroups share one tile
@@ -167,20 +167,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   int n_pre = 0;       // decode: prefix keys
   int pre0 = 0;        // decode: first cache token of the prefix
   int n_pre_tiles = 0;
-  if constexpr (!kDecode) {
-    for (int i = 0; i < 2; ++i) {
-      nkt[i] = 0;
-      const int m = m_base + i;
-      if (rows_valid[i] > 0 && m < p.tiles_per_seq && BCA_IN_BOUNDS(p.status, b < p.batch)) {
-        const PrefillTile t = p.tiles[b * p.tiles_per_seq + m];
-        k_hi[i] = t.k_hi;
-        k_min[i] = t.k_min;
-        nkt[i] = (t.k_hi + kBlockN - 1) / kBlockN;
-      }
-    }
-    if (nkt[0] <= 0) return;  // empty tile, or a sequence that failed validation
-    kv_seq0 = p.cu_k[b];
-  } else {
+  if constexpr (kDecode) {
     pre0 = p.cu_prefix[b];
     const int pre1 = p.cu_prefix[b + 1];
     n_pre = pre1 - pre0;
@@ -219,16 +206,16 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   // Row ends never decrease along a sequence, so a present Q1 needs at least as
   // many key tiles as Q0; keep that invariant explicitly (extra tiles would be
   // fully masked), since ring stages are released by Q1's softmax (below).
-  if (!kSplit && nkt[1] > 0 && nkt[1] < nkt[0]) nkt[1] = nkt[0];
-  const int nk = max(nkt[0], nkt[1]);
-  const int k_hi_all = max(k_hi[0], k_hi[1]);
-  // Prefill with cache append: the CTA of a sequence's last tile pair reads every key
-  // tile of the sequence (its last row sees them all), and its store warp writes the
-  // prefix ones to the cache; the stages it stores are released by that warp too.
-  const bool appender = !kDecode && p.cache_k != nullptr &&
-                        m_base == 2 * (((q_len + kBlockM - 1) / kBlockM - 1) / 2);
-  const int koff1 = kSplit ? nkt[0] : 0;                  // first key tile of warpgroup 1
-  const int n_kv_tiles = kSplit ? nkt[0] + nkt[1] : nk;   // distinct K/V tiles of the item
+  // (Prefill: once the tile records have been read, after the set-up.)
+  int nk = 0, k_hi_all = 0, koff1 = 0, n_kv_tiles = 0;
+  auto derive_ranges = [&]() {
+    if (!kSplit && nkt[1] > 0 && nkt[1] < nkt[0]) nkt[1] = nkt[0];
+    nk = max(nkt[0], nkt[1]);
+    k_hi_all = max(k_hi[0], k_hi[1]);
+    koff1 = kSplit ? nkt[0] : 0;                  // first key tile of warpgroup 1
+    n_kv_tiles = kSplit ? nkt[0] + nkt[1] : nk;   // distinct K/V tiles of the item
+  };
+  if constexpr (kDecode) derive_ranges();
   // valid keys left in K/V tile j's segment (>= 128: the tile is full)
   auto seg_left_of = [&](int j) {
     if constexpr (!kDecode) {
@@ -237,6 +224,11 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       return j < n_pre_tiles ? n_pre - j * kBlockN : q_len - (j - n_pre_tiles) * kBlockN;
     }
   };
+  // Prefill with cache append: the CTA of a sequence's last tile pair reads every key
+  // tile of the sequence (its last row sees them all), and its store warp writes the
+  // prefix ones to the cache; the stages it stores are released by that warp too.
+  const bool appender = !kDecode && p.cache_k != nullptr &&
+                        m_base == 2 * (((q_len + kBlockM - 1) / kBlockM - 1) / 2);
 
   // ---- set-up -----------------------------------------------------------------
   bool q_armed = false;   // (TMA producer lane) the query loads were issued
@@ -290,6 +282,33 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
   volatile int* abort_flag = &sm.abort;
+
+  if constexpr (!kDecode) {
+    // The tile records are written by the schedule prep launched just before this
+    // grid, which may start this one early (programmatic dependent launch): the
+    // set-up and query loads above overlap the prep, and nothing it writes is read
+    // before this wait.
+    grid_dependency_wait();
+    for (int i = 0; i < 2; ++i) {
+      const int m = m_base + i;
+      if (rows_valid[i] > 0 && m < p.tiles_per_seq && BCA_IN_BOUNDS(p.status, b < p.batch)) {
+        const PrefillTile t = p.tiles[b * p.tiles_per_seq + m];
+        k_hi[i] = t.k_hi;
+        k_min[i] = t.k_min;
+        nkt[i] = (t.k_hi + kBlockN - 1) / kBlockN;
+      }
+    }
+    if (nkt[0] <= 0) {
+      // an empty tile, or a sequence that failed validation: let the query loads
+      // land before the CTA's shared memory is released, and free the TMEM
+      if (warp == kWarpTma && lane == 0 && q_armed)
+        mbar_wait(&sm.q_full, 0, abort_flag, kWaitLimitNs);
+      if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
+      return;
+    }
+    kv_seq0 = p.cu_k[b];
+    derive_ranges();
+  }
 
   auto give_up = [&]() {
     sm.abort = 1;
@@ -1094,8 +1113,21 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
       groups = 1;
     }
     p.head_groups = groups;
-    const dim3 grid(per_group, (a.tiles_per_seq + 1) / 2, a.batch * groups);
-    kernels[mode]<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, to, p);
+    // A programmatic dependent of the schedule prep that every caller launches just
+    // before this grid on the same stream: its CTAs start while the prep runs and
+    // wait for it only where they read its tile records.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(per_group, (a.tiles_per_seq + 1) / 2, a.batch * groups);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kernels[mode], tq, tk, tv, tk2, tv2, to, p) != cudaSuccess)
+      return BCA_ERR_CUDA;
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
   }

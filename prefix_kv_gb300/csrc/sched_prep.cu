@@ -9,14 +9,18 @@
 // notes, "NEO-Unify 多模态 Prefill 的注意力") and k_min = min e (below it no key
 // tile needs a mask).
 //
-// One CTA of 1024 threads per sequence:
+// A grid of (sequence, 1024-row chunk) CTAs of 1024 threads.  Every CTA of a
+// sequence with rows to do runs steps 1 and 2 over the whole sequence (a few
+// block-id reads from L2, so that no CTA waits on another), step 3 for its own rows:
 //   1. stage 8192 block ids at a time in shared memory, mark the last position
 //      of every image run (and reject ids < -1), and append the run ends, in
 //      order, to a shared list with a block-wide scan;
 //   2. reject an id that appears in two separate runs (flozi.net, "Block-causal
 //      attention is the cache-enabling boundary": each image has its own id);
-//   3. e per query row by binary search over the run ends; per-tile min / max.
+//   3. e per query row of the chunk by binary search over the run ends; min / max
+//      of its eight 128-row tiles.
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace bca {
 namespace {
@@ -26,6 +30,7 @@ constexpr int kPerThread = 8;
 constexpr int kChunk = kPrepThreads * kPerThread;  // positions or rows per pass
 constexpr int kMaxRuns = 1024;  // image runs per sequence (BCA_ERR_UNSUPPORTED above)
 constexpr int kWarps = kPrepThreads / 32;
+constexpr int kTilesPerCta = kPrepThreads / kBlockM;   // one row per thread in step 3
 
 __device__ __forceinline__ int warp_incl_scan(int x) {
   const int lane = threadIdx.x & 31;
@@ -65,12 +70,18 @@ __global__ void __launch_bounds__(kPrepThreads)
   __shared__ int run_end[kMaxRuns];
   __shared__ int run_id[kMaxRuns];
   __shared__ int warp_buf[kWarps + 1];
+  __shared__ int red[3][kWarps];
   __shared__ int n_runs;
   __shared__ int err;
 
+  // The attention grid launched next may start at once: it waits for this grid's
+  // results where it reads them.
+  grid_launch_dependents();
   const int b = blockIdx.x;
+  const int chunk = blockIdx.y;   // query rows [chunk * 1024, chunk * 1024 + 1024)
   const int tid = threadIdx.x;
   const int lane = tid & 31, wid = tid >> 5;
+  const int row = chunk * kPrepThreads + tid;   // this thread's query row in step 3
   const int k0 = cu_k[b];
   const int kv_len = cu_k[b + 1] - k0;
   const int q0 = cu_q[b];
@@ -86,6 +97,24 @@ __global__ void __launch_bounds__(kPrepThreads)
       err = BCA_ERR_SEQLENS;
   }
   __syncthreads();
+  // this CTA's eight tile records, zeroed (a chunk past the sequence's rows, or a
+  // sequence that failed validation: the attention kernel skips zeroed tiles)
+  auto zero_tiles = [&]() {
+    if (tid < kTilesPerCta) {
+      const int m = chunk * kTilesPerCta + tid;
+      if (m < tiles_per_seq && BCA_IN_BOUNDS(status, b < static_cast<int>(gridDim.x)))
+        tiles[b * tiles_per_seq + m] = PrefillTile{0, 0, 0, 0};
+    }
+  };
+  if (err == 0 && chunk > 0 && chunk * kPrepThreads >= q_len) {
+    zero_tiles();   // no rows here; the first chunk's CTA reports any bad id
+    return;
+  }
+  const bool valid = err == 0 && row < q_len;
+  // the row's own id, read now so that the load overlaps steps 1 and 2
+  const int row_id = valid && BCA_IN_BOUNDS(status, k0 + kv_len - q_len + row < total_k)
+                         ? bid[k0 + kv_len - q_len + row]
+                         : -1;
 
   // ---- 1. image runs ------------------------------------------------------------
   if (err == 0) {
@@ -157,76 +186,49 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
 
   if (err != 0) {
-    if (tid == 0) report_status(status, err);
-    for (int m = tid; m < tiles_per_seq; m += kPrepThreads)
-      if (BCA_IN_BOUNDS(status, b < static_cast<int>(gridDim.x)))
-        tiles[b * tiles_per_seq + m] = PrefillTile{0, 0, 0, 0};
+    if (tid == 0 && chunk == 0) report_status(status, err);
+    zero_tiles();
     return;
   }
 
   // ---- 3. e per row, min / max per 128-row tile ------------------------------------
-  // A pass covers 8192 rows: sub-pass u handles rows base + u*1024 + tid, so each
-  // warp owns 32 consecutive rows and each 128-row tile is four consecutive warps
-  // of one sub-pass.  All eight block-id loads of a thread are issued up front.
-  __shared__ int red[3][kPerThread][kWarps];
-  const int R = n_runs;
-  const int n_tiles_seq = (q_len + kBlockM - 1) / kBlockM;
-  for (int base = 0; base < tiles_per_seq * kBlockM; base += kChunk) {
-    int ids_row[kPerThread];
-#pragma unroll
-    for (int u = 0; u < kPerThread; ++u) {
-      const int i = base + u * kPrepThreads + tid;
-      ids_row[u] = i < q_len && BCA_IN_BOUNDS(status, k0 + kv_len - q_len + i < total_k)
-                       ? bid[k0 + kv_len - q_len + i]
-                       : -1;
-    }
-#pragma unroll
-    for (int u = 0; u < kPerThread; ++u) {
-      const int i = base + u * kPrepThreads + tid;
-      const bool valid = i < q_len;
-      int e = 0;
-      if (valid) {
-        const int pos = kv_len - q_len + i;
-        if (ids_row[u] < 0) {
-          e = pos + 1;
-        } else {  // first run end > pos
-          int lo = 0, hi = R;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (run_end[mid] > pos) hi = mid; else lo = mid + 1;
-          }
-          e = run_end[lo];
-        }
-        if (BCA_IN_BOUNDS(status, q0 + i >= 0 && q0 + i < total_q)) row_end[q0 + i] = e;
+  // Each warp owns 32 consecutive rows, each 128-row tile four consecutive warps.
+  int e = 0;
+  if (valid) {
+    const int pos = kv_len - q_len + row;
+    if (row_id < 0) {
+      e = pos + 1;
+    } else {  // first run end > pos
+      int lo = 0, hi = n_runs;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (run_end[mid] > pos) hi = mid; else lo = mid + 1;
       }
-      const int vmax = __reduce_max_sync(0xffffffffu, valid ? e : 0);
-      const int vmin = __reduce_min_sync(0xffffffffu, valid ? e : 0x7fffffff);
-      const int cnt = static_cast<int>(__reduce_add_sync(0xffffffffu, valid ? 1u : 0u));
-      if (lane == 0) {
-        red[0][u][wid] = vmax;
-        red[1][u][wid] = vmin;
-        red[2][u][wid] = cnt;
-      }
+      e = run_end[lo];
     }
-    __syncthreads();
-    // 64 tiles per pass: thread t < 64 reduces sub-pass t/8, warps 4*(t%8) .. +3
-    if (tid < kChunk / kBlockM) {
-      const int u = tid / (kPrepThreads / kBlockM);
-      const int w0 = (tid % (kPrepThreads / kBlockM)) * (kBlockM / 32);
-      const int m = (base + u * kPrepThreads) / kBlockM + tid % (kPrepThreads / kBlockM);
-      if (m < tiles_per_seq && BCA_IN_BOUNDS(status, b < static_cast<int>(gridDim.x))) {
-        int tmax = 0, tmin = 0x7fffffff, tcnt = 0;
-        for (int w = w0; w < w0 + kBlockM / 32; ++w) {
-          tmax = max(tmax, red[0][u][w]);
-          tmin = min(tmin, red[1][u][w]);
-          tcnt += red[2][u][w];
-        }
-        tiles[b * tiles_per_seq + m] = (tcnt > 0 && m < n_tiles_seq)
-                                           ? PrefillTile{tmax, tmin, tcnt, 0}
-                                           : PrefillTile{0, 0, 0, 0};
+    if (BCA_IN_BOUNDS(status, q0 + row >= 0 && q0 + row < total_q)) row_end[q0 + row] = e;
+  }
+  const int vmax = __reduce_max_sync(0xffffffffu, valid ? e : 0);
+  const int vmin = __reduce_min_sync(0xffffffffu, valid ? e : 0x7fffffff);
+  const int cnt = static_cast<int>(__reduce_add_sync(0xffffffffu, valid ? 1u : 0u));
+  if (lane == 0) {
+    red[0][wid] = vmax;
+    red[1][wid] = vmin;
+    red[2][wid] = cnt;
+  }
+  __syncthreads();
+  if (tid < kTilesPerCta) {
+    const int m = chunk * kTilesPerCta + tid;
+    if (m < tiles_per_seq && BCA_IN_BOUNDS(status, b < static_cast<int>(gridDim.x))) {
+      int tmax = 0, tmin = 0x7fffffff, tcnt = 0;
+      for (int w = tid * (kBlockM / 32); w < (tid + 1) * (kBlockM / 32); ++w) {
+        tmax = max(tmax, red[0][w]);
+        tmin = min(tmin, red[1][w]);
+        tcnt += red[2][w];
       }
+      tiles[b * tiles_per_seq + m] = tcnt > 0 ? PrefillTile{tmax, tmin, tcnt, 0}
+                                              : PrefillTile{0, 0, 0, 0};
     }
-    __syncthreads();
   }
 }
 
@@ -236,8 +238,10 @@ cudaError_t launch_schedule_prep(const int32_t* block_id, const int32_t* cu_q, c
                                  int batch, int total_q, int total_k, int tiles_per_seq,
                                  int32_t* row_end, PrefillTile* tiles, int32_t* status,
                                  cudaStream_t stream) {
-  schedule_prep_kernel<<<batch, kPrepThreads, 0, stream>>>(block_id, cu_q, cu_k, total_q, total_k,
-                                                           tiles_per_seq, row_end, tiles, status);
+  // at least one chunk, so that a sequence with rows but no tiles still reports
+  const dim3 grid(batch, max(1, (tiles_per_seq + kTilesPerCta - 1) / kTilesPerCta));
+  schedule_prep_kernel<<<grid, kPrepThreads, 0, stream>>>(block_id, cu_q, cu_k, total_q, total_k,
+                                                          tiles_per_seq, row_end, tiles, status);
   return cudaGetLastError();
 }
 
