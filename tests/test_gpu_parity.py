@@ -126,6 +126,91 @@ def test_schedule_rejects_offsets_past_the_arrays():
         assert (tiles[1] == 0).all()
 
 
+def _ids(*runs):
+    """Block ids from (id, length) runs."""
+    return np.concatenate([np.full(n, i, np.int32) for i, n in runs])
+
+
+def _raw_prep(bid, cu_q, cu_k, max_q):
+    """bca_schedule_prep into buffers filled with -5 (so that zeroed records are the
+    kernel's writes): (status, row_end, tiles) on the host."""
+    from prefix_kv_gb300 import _native
+    ti = lambda a: torch.from_numpy(np.asarray(a, np.int32)).to(DEV)
+    bid_d, cq, ck = ti(bid), ti(cu_q), ti(cu_k)
+    batch, tps = len(cu_q) - 1, (max_q + 127) // 128
+    row_end = torch.full((int(cu_q[-1]),), -5, dtype=torch.int32, device=DEV)
+    tiles = torch.full((batch, tps, 4), -5, dtype=torch.int32, device=DEV)
+    st = _status()
+    code = _native.load().bca_schedule_prep(
+        bid_d.data_ptr(), cq.data_ptr(), ck.data_ptr(), batch, int(cu_q[-1]), len(bid), max_q,
+        row_end.data_ptr(), tiles.data_ptr(), st.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert code == 0
+    return bca.read_status(st), row_end.cpu().numpy(), tiles.cpu().numpy()
+
+
+def _packed_case(seqs):
+    """(block ids, q_len or None for q_len = kv_len) per sequence -> a schedule-only case."""
+    kv = [len(s) for s, _ in seqs]
+    ql = [len(s) if q is None else q for s, q in seqs]
+    cu_k = np.concatenate([[0], np.cumsum(kv)]).astype(np.int32)
+    cu_q = np.concatenate([[0], np.cumsum(ql)]).astype(np.int32)
+    return PrefillCase(torch.zeros(0), torch.zeros(0), torch.zeros(0),
+                       np.concatenate([s for s, _ in seqs]), cu_q, cu_k)
+
+
+def test_schedule_rows_over_several_chunks():
+    """The prep works in 1024-row chunks of a sequence: image runs crossing chunk
+    edges, a sequence whose last chunk holds one row, bottom-right rows whose first
+    row lies inside an image, and shorter sequences whose last chunks have no rows
+    (their tile records stay zero)."""
+    case = _packed_case([
+        (_ids((-1, 100), (0, 1900), (-1, 30), (1, 1019)), None),     # run 0 spans rows 100..1999
+        (_ids((-1, 1), (0, 1024)), None),                            # 1025 rows
+        (_ids((-1, 5), (3, 4000), (-1, 7), (4, 1300)), 2500),        # rows = keys 2812..5311
+        (_ids((2, 1023)), None),                                     # one image, one chunk
+        (_ids((-1, 700)), None),                                     # text only
+    ])
+    _check_schedule(case)
+    # the same into buffers filled with -5: every row end and every record (zeroed
+    # ones included) is written by the kernel
+    code, row_end, tiles = _raw_prep(case.block_id, case.cu_q, case.cu_k, case.max_q)
+    assert code == 0 and (row_end >= 1).all()
+    for b in range(len(case.cu_q) - 1):
+        n_t = (int(case.cu_q[b + 1] - case.cu_q[b]) + 127) // 128
+        assert (tiles[b, :n_t, :3] > 0).all() and (tiles[b, n_t:] == 0).all()
+
+
+def test_schedule_split_id_past_the_first_chunks():
+    """An id split into two runs beyond the first 8192 positions fails its whole
+    sequence (every chunk's tile records zero); the other sequence of the batch
+    is scheduled as usual."""
+    good = _ids((-1, 64), (0, 2000), (-1, 16))
+    bad = _ids((-1, 9000), (7, 50), (-1, 200), (7, 10), (-1, 40))
+    case = _packed_case([(good, None), (bad, None)])
+    code, row_end, tiles = _raw_prep(case.block_id, case.cu_q, case.cu_k, case.max_q)
+    assert code == 3
+    assert (tiles[1] == 0).all()
+    n = len(good)
+    m = oracle.visibility(good, n, np.arange(n))
+    assert (m == (np.arange(n)[None, :] < row_end[:n, None])).all()
+    for t in range((n + 127) // 128):
+        er = row_end[t * 128: min(n, t * 128 + 128)]
+        assert tuple(tiles[0, t, :3]) == (er.max(), er.min(), er.size)
+    assert (tiles[0, (n + 127) // 128:] == 0).all()
+
+
+def test_schedule_run_count_limit():
+    """1024 image runs in a sequence are scheduled; 1025 give BCA_ERR_UNSUPPORTED
+    with zeroed tile records."""
+    at_limit = np.repeat(np.arange(1024, dtype=np.int32), 2)      # 1024 two-token images
+    _check_schedule(_packed_case([(at_limit, None)]))
+    over = np.arange(1025, dtype=np.int32)                         # 1025 one-token images
+    cu = np.array([0, 1025], np.int32)
+    code, _, tiles = _raw_prep(over, cu, cu, 1025)
+    assert code == 2
+    assert (tiles == 0).all()
+
+
 # ---------------------------------------------------------------- prefill
 
 def test_prefill_tiny_all_outputs():
