@@ -475,10 +475,18 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
         // faster than the general loop below, which then finishes the item.
         int j = 0;
         const int n_both = min(nkt[0], nkt[1]) - 1;
+        // V(j + 1) is checked (and its fix-up requested) before S1(j + 1) is issued,
+        // while the pipe still holds PV1(j): between S1(j + 1) and PV0(j + 1), where
+        // the pipe runs dry, only the wait for P0(j + 1) is left (1.0% prefill, 0.8%
+        // decode).
+        bool v_ready = false;   // V(j) landed and fixed ahead of iteration j
+        if (n_both > 0 && ok) {
+          ok = landed(1) && fix_tail(0, stage_of(1));
+          v_ready = true;
+        }
         for (; j < n_both && ok; ++j) {
           const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
-          if (!(landed(2 * j + 1) && fix_tail(j, vs) &&
-                mbar_wait(&sm.p_full[0], j & 1, abort_flag, kWaitLimitNs))) {
+          if (!mbar_wait(&sm.p_full[0], j & 1, abort_flag, kWaitLimitNs)) {
             ok = false;
             break;
           }
@@ -495,11 +503,15 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
           }
           tc_fence_after();
           issue_pv(1, vs, j, false);
+          if (!(landed(2 * j + 3) && fix_tail(j + 1, stage_of(2 * j + 3)))) {
+            ok = false;
+            break;
+          }
           issue_s(1, ks);
         }
         for (; j < nk && ok; ++j) {
           const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
-          ok = landed(2 * j + 1) && fix_tail(j, vs);
+          ok = (v_ready && j == n_both) || (landed(2 * j + 1) && fix_tail(j, vs));
           bool k_next_ready = false;
           for (int i = 0; i < 2 && ok; ++i) {
             if (j < nkt[i]) {
