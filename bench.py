@@ -174,6 +174,24 @@ def whole_job_tflops(world: int, steps: int, step_flops: float, total_ms: float)
 
 # ----------------------------------------------------------------------------- inputs
 
+def prefill_grids(num_heads, max_q, batch, sms):
+    """Grids one prefill attention call launches: tile pairs (head in group x pair x
+    sequence x head group) and, for a grid of at most four waves past two whole ones
+    whose last wave is partly filled, a second grid of key-split single tiles."""
+    per_group = num_heads
+    for d in range(8, 3, -1):
+        if num_heads > d and num_heads % d == 0:
+            per_group = d
+            break
+    groups = num_heads // per_group
+    if batch * groups > 65535:
+        per_group, groups = num_heads, 1
+    pairs = (-(-max_q // 128) + 1) // 2
+    total = per_group * pairs * batch * groups
+    tail = total % sms
+    return 1 + int(0 < tail and total - tail >= 2 * sms and total <= 4 * sms)
+
+
 def decode_grids(num_heads, max_q, batch, sms):
     """Grids one decode call launches: tile pairs (head x pair x sequence) fill
     whole waves of the SMs; a last wave at most half full becomes a second grid
@@ -254,11 +272,14 @@ class Problem:
         else:                                                    # K and V quantised
             self.append_bytes = rows * 2 * (256 + 128 + 4)
         # kernel launches per step: schedule prep, prefill, append, [expansions], decode
-        # (one grid of tile pairs and, for a short last wave, one of key-split tiles)
+        # (prefill and decode: one grid of tile pairs and, for a short last wave, one of
+        # key-split tiles)
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        self.launches = (3 + {None: 0, "v": 1, "kv": 2}[self.fp8_mode] +
+        self.sms = sms
+        pre_grids = prefill_grids(self.H, self.max_s, self.batch, sms)
+        self.launches = (2 + pre_grids + {None: 0, "v": 1, "kv": 2}[self.fp8_mode] +
                          decode_grids(self.H, self.max_n, self.batch, sms) if wl.decode
-                         else 2)          # prefill only: schedule prep + attention
+                         else 1 + pre_grids)   # prefill only: schedule prep + attention
         # optional Q/K prologue (RMS norm + three-axis RoPE; the prefill-side call also
         # appends): coordinates and rotation table once per layout, outside the step
         self.prologue = prologue
@@ -287,9 +308,14 @@ class Problem:
             self.cu_host = wl.cu_seqlens()
             self.pw_ws = torch.empty(bca.prefill_piecewise_workspace_bytes(
                 self.bid_host, self.cu_host, self.H), dtype=torch.uint8, device=dev)
-            n_pieces = sum(int(np.count_nonzero(np.diff(self.bid_host[a:e]))) + 1
-                           for a, e in zip(self.cu_host[:-1], self.cu_host[1:]) if e > a)
-            self.launches += 2 * n_pieces - 2
+            # one schedule prep and one attention call per run of equal ids
+            piece_lens = []
+            for a, e in zip(self.cu_host[:-1], self.cu_host[1:]):
+                if e > a:
+                    cuts = np.flatnonzero(np.diff(self.bid_host[a:e])) + 1
+                    piece_lens += np.diff(np.concatenate([[0], cuts, [e - a]])).tolist()
+            self.launches += (sum(1 + prefill_grids(self.H, int(n), 1, sms) for n in piece_lens)
+                              - 1 - pre_grids)
         # the bf16 contiguous cache is written by the prefill launch itself
         # (bca_prefill_append) unless the two separate calls are asked for
         self.fused = (self.decode and self.fp8_mode is None and not piecewise

@@ -117,10 +117,22 @@ struct FwdParams {
   __nv_bfloat16* cache_v;
   int decode_pairs_per_seq;   // decode: tile pairs per sequence (grid decoding)
   int decode_split_from;      // decode: first item split into single-tile items
+  int64_t prefill_split_from; // prefill: first pair CTA, in the grid's launch order
+                              //   (x fastest, then y, then z), done as two key-split
+                              //   single-tile items instead; >= the grid size: none
+  int prefill_x, prefill_y;   // prefill: x and y extents of the pair grid
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
 };
+
+// Prefill with cache append: the CTA of a sequence's last tile pair also writes the
+// sequence's prefix K/V to the cache (it reads every key tile of the sequence).
+__device__ __forceinline__ bool pair_appends(const FwdParams& p, int b, int m_base) {
+  if (p.cache_k == nullptr) return false;
+  const int q_len = p.cu_q[b + 1] - p.cu_q[b];
+  return m_base == 2 * (((q_len + kBlockM - 1) / kBlockM - 1) / 2);
+}
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort, kWaitLimitNs));
@@ -136,7 +148,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
                                           const FwdParams& p, FwdSmem& sm,
                                           const int h, const int b, const int m_base,
                                           const int n_qt) {
-  static_assert(kDecode || !kSplit, "key split is a decode item");
+  static_assert(!(kSplit && kPagedAppend), "a key-split item never appends");
   static_assert(!kPagedAppend || !kDecode, "the cache append is a prefill option");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -227,8 +239,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   // Prefill with cache append: the CTA of a sequence's last tile pair reads every key
   // tile of the sequence (its last row sees them all), and its store warp writes the
   // prefix ones to the cache; the stages it stores are released by that warp too.
-  const bool appender = !kDecode && p.cache_k != nullptr &&
-                        m_base == 2 * (((q_len + kBlockM - 1) / kBlockM - 1) / 2);
+  const bool appender = !kDecode && !kSplit && pair_appends(p, b, m_base);
 
   // ---- set-up -----------------------------------------------------------------
   bool q_armed = false;   // (TMA producer lane) the query loads were issued
@@ -288,14 +299,32 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     // grid, which may start this one early (programmatic dependent launch): the
     // set-up and query loads above overlap the prep, and nothing it writes is read
     // before this wait.
-    grid_dependency_wait();
-    for (int i = 0; i < 2; ++i) {
-      const int m = m_base + i;
-      if (rows_valid[i] > 0 && m < p.tiles_per_seq && BCA_IN_BOUNDS(p.status, b < p.batch)) {
-        const PrefillTile t = p.tiles[b * p.tiles_per_seq + m];
-        k_hi[i] = t.k_hi;
-        k_min[i] = t.k_min;
-        nkt[i] = (t.k_hi + kBlockN - 1) / kBlockN;
+    // (A key-split item belongs to a grid launched after the pair grid, which it may
+    // run beside: it reads the records without that wait.  It starts only after
+    // every pair CTA has started, and the host splits only past two full waves of
+    // pair CTAs, so some pair CTA has ended, after its own wait for the prep.  The
+    // records are read through L2.)
+    if constexpr (!kSplit) {
+      grid_dependency_wait();
+      for (int i = 0; i < 2; ++i) {
+        const int m = m_base + i;
+        if (rows_valid[i] > 0 && m < p.tiles_per_seq && BCA_IN_BOUNDS(p.status, b < p.batch)) {
+          const PrefillTile t = p.tiles[b * p.tiles_per_seq + m];
+          k_hi[i] = t.k_hi;
+          k_min[i] = t.k_min;
+          nkt[i] = (t.k_hi + kBlockN - 1) / kBlockN;
+        }
+      }
+    } else {
+      // one query tile, its key tiles cut in two: warpgroup 0 takes the first half
+      // (or one more), warpgroup 1 the rest
+      if (rows_valid[0] > 0 && m_base < p.tiles_per_seq && BCA_IN_BOUNDS(p.status, b < p.batch)) {
+        const int4 t = __ldcg(reinterpret_cast<const int4*>(p.tiles + b * p.tiles_per_seq + m_base));
+        const int n_all = (t.x + kBlockN - 1) / kBlockN;
+        nkt[1] = n_all / 2;
+        nkt[0] = n_all - nkt[1];
+        k_hi[0] = k_hi[1] = t.x;
+        k_min[0] = k_min[1] = t.y;
       }
     }
     if (nkt[0] <= 0) {
@@ -699,10 +728,16 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     const bool row_valid = row < rows_valid[qi];
     const bool releaser = !kSplit && (qi == 1 || nkt[1] == 0);
     int e_row = 0;
-    if constexpr (!kDecode)
-      e_row = row_valid && BCA_IN_BOUNDS(p.status, row0 + row >= 0 && row0 + row < p.total_q)
-                  ? p.row_end[row0 + row]
-                  : k_hi[qi];
+    if constexpr (!kDecode) {
+      const bool e_in =
+          row_valid && BCA_IN_BOUNDS(p.status, row0 + row >= 0 && row0 + row < p.total_q);
+      if constexpr (kSplit)
+        e_row = e_in ? __ldcg(p.row_end + row0 + row) : k_hi[qi];
+      else
+        e_row = e_in ? p.row_end[row0 + row] : k_hi[qi];
+    }
+    // first key tile of this warpgroup (warpgroup 1 of a key-split item: koff1)
+    const int jg0 = kSplit && qi == 1 ? koff1 : 0;
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY;   // reference max of the row, log2 domain
     float l_run = 0.f;
@@ -737,8 +772,8 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       int lim;
       bool need_mask;
       if constexpr (!kDecode) {
-        lim = e_row - j * kBlockN;
-        need_mask = (j + 1) * kBlockN > k_min[qi];
+        lim = e_row - (jg0 + j) * kBlockN;
+        need_mask = (jg0 + j + 1) * kBlockN > k_min[qi];
       } else {
         lim = j < tgt0 ? pre_left0 - j * kBlockN : q_len - (j - tgt0) * kBlockN;
         need_mask = lim < kBlockN;
@@ -791,7 +826,15 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       // it): O and l share the reference, so out = O / l is exact either way and
       // in the common case no max needs to be taken at all.
       float alpha = 1.f;
-      if (j == 0) m_ref = tile_max();   // key 0 is visible to every row: finite
+      if (j == 0) {
+        m_ref = tile_max();   // key 0 is visible to every row: finite
+        if constexpr (kSplit && !kDecode) {
+          // except in warpgroup 1 of a key-split prefill item, whose keys start at
+          // tile koff1: a row that ends before them sees none, and any finite
+          // reference gives it P = 0, l = 0, O = 0 for the merge
+          if (m_ref == -INFINITY) m_ref = 0.f;
+        }
+      }
       float tsum = write_p();
       if (j > 0 && __any_sync(0xffffffffu, !(tsum <= kSumLimit))) {
         const float m_new = fmaxf(m_ref, tile_max());
@@ -979,11 +1022,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   FwdSmem& sm = *reinterpret_cast<FwdSmem*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  if constexpr (!kDecode) {
+  if constexpr (!kDecode && !kSplit) {
+    // the key-split grid launched after this one may start once every CTA here has
+    grid_launch_dependents();
     const int h = blockIdx.x + (blockIdx.z % p.head_groups) * gridDim.x;   // groups are full
-    attn_item<false, false, kPagedAppend>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, h, blockIdx.z / p.head_groups,
-                            2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y)),
-                            2);
+    const int b = blockIdx.z / p.head_groups;
+    const int m_base = 2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y));
+    const int64_t launch_idx =
+        blockIdx.x + static_cast<int64_t>(gridDim.x) * (blockIdx.y + static_cast<int64_t>(gridDim.y) * blockIdx.z);
+    // a pair of the last, partly filled wave is done by the key-split grid (never
+    // the pair that appends to the cache)
+    if (launch_idx >= p.prefill_split_from && !pair_appends(p, b, m_base)) return;
+    attn_item<false, false, kPagedAppend>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, h, b,
+                                          m_base, 2);
+  } else if constexpr (!kDecode) {
+    // Prefill key split: CTA 2i + s does query tile s of the pair CTA at launch
+    // index prefill_split_from + i of the pair grid.
+    const int64_t launch_idx = p.prefill_split_from + blockIdx.x / 2;
+    const int x = static_cast<int>(launch_idx % p.prefill_x);
+    const int64_t yz = launch_idx / p.prefill_x;
+    const int y = static_cast<int>(yz % p.prefill_y);
+    const int z = static_cast<int>(yz / p.prefill_y);
+    const int h = x + (z % p.head_groups) * p.prefill_x;
+    const int b = z / p.head_groups;
+    const int m_base = 2 * (p.prefill_y - 1 - y);
+    if (!pair_appends(p, b, m_base))
+      attn_item<false, true, false>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, h, b,
+                                    m_base + static_cast<int>(blockIdx.x & 1), 2);
+    // do not complete before the pair grid has (work queued after the call sees both)
+    grid_dependency_wait();
   } else if constexpr (!kSplit) {
     grid_launch_dependents();
     const int L = blockIdx.x;
@@ -1125,11 +1192,36 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
       groups = 1;
     }
     p.head_groups = groups;
+    // The pair CTAs of a last, partly filled wave (in launch order: the cheapest
+    // pairs of the last head group) become key-split single-tile items, two CTAs
+    // each, in a second grid that may start as soon as every pair CTA has started.
+    // Only past two full waves of pair CTAs: before every pair CTA has started, at
+    // least one must have ended, which it cannot do before the schedule prep has
+    // completed; the split grid reads the prep's records without waiting for it.
+    // And only for grids of at most four waves: a split item does its keys ~40%
+    // slower than a pair (two K/V streams, its own set-up), which the last wave's
+    // idle SMs pay back in a short grid (text-to-image layer: 226 -> 213 us) but not
+    // in a long one (two-reference edit, 10 waves: 1059 -> 1067 us).
+    static int sms = 0;
+    if (sms == 0) {
+      int dev = 0;
+      if (cudaGetDevice(&dev) != cudaSuccess ||
+          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        sms = 1;
+    }
+    const int pairs = (a.tiles_per_seq + 1) / 2;
+    const int64_t total = static_cast<int64_t>(per_group) * pairs * a.batch * groups;
+    const int64_t tail = total % sms;
+    const bool split = tail > 0 && total - tail >= 2 * static_cast<int64_t>(sms) &&
+                       total <= 4 * static_cast<int64_t>(sms);
+    p.prefill_split_from = split ? total - tail : total;
+    p.prefill_x = per_group;
+    p.prefill_y = pairs;
     // A programmatic dependent of the schedule prep that every caller launches just
     // before this grid on the same stream: its CTAs start while the prep runs and
     // wait for it only where they read its tile records.
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(per_group, (a.tiles_per_seq + 1) / 2, a.batch * groups);
+    cfg.gridDim = dim3(per_group, pairs, a.batch * groups);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
@@ -1140,6 +1232,20 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, kernels[mode], tq, tk, tv, tk2, tv2, to, p) != cudaSuccess)
       return BCA_ERR_CUDA;
+    if (split) {
+      static bool split_attr = false;
+      if (!split_attr) {
+        if (cudaFuncSetAttribute(attn_fwd_kernel<false, true, false>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes)) != cudaSuccess)
+          return BCA_ERR_CUDA;
+        split_attr = true;
+      }
+      cfg.gridDim = dim3(static_cast<unsigned>(2 * tail), 1, 1);   // the pair grid's dependent
+      if (cudaLaunchKernelEx(&cfg, attn_fwd_kernel<false, true, false>, tq, tk, tv, tk2, tv2, to,
+                             p) != cudaSuccess)
+        return BCA_ERR_CUDA;
+    }
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
   }

@@ -42,6 +42,19 @@ def test_decode_grid_count_follows_the_tail_rule():
     assert bench.decode_grids(1, 0, 1, 152) == 0           # nothing to launch
 
 
+def test_prefill_grid_count_follows_the_split_rule():
+    # the pair grid, plus a key-split grid when at most four waves of pair CTAs, past
+    # two whole waves, end in a partly filled one (the launch rule of the prefill call)
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.prefill_grids(32, 12480, 1, 152) == 1     # 8 x 49 x 4 = 1568 CTAs: 10 waves
+    assert bench.prefill_grids(32, 4352, 1, 152) == 2      # 8 x 17 x 4 = 544: 88 left over
+    assert bench.prefill_grids(16, 4096, 2, 152) == 2      # 8 x 16 x 4 = 512: 56 left over
+    assert bench.prefill_grids(32, 2048, 1, 152) == 1      # 8 x 8 x 4 = 256: under two waves
+    assert bench.prefill_grids(8, 9728, 1, 152) == 1       # 4 x 38 x 2 = 304: whole waves
+    assert bench.prefill_grids(3, 40, 1, 152) == 1         # one pair per head
+
+
 def test_reference_arm_line():
     # the reference arm times the oracle on the host and prints the contract's JSON line
     env = dict(os.environ, CUDA_VISIBLE_DEVICES="")

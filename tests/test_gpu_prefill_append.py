@@ -174,3 +174,28 @@ def test_prefill_append_paged_rejects_bad_page():
                        page_table=pt, status=st)
     assert bca.read_status(st) == 5                # BCA_ERR_CAPACITY
     assert (ck.view(torch.int16) == -1).all() and (cv.view(torch.int16) == -1).all()
+
+
+def test_prefill_append_key_split_tail_keeps_the_appending_pair():
+    """A pair grid of 8 x 16 x 4 = 512 CTAs (under four waves of 152): its last 56 in
+    launch order, those of the second head group of sequence 1, become key-split
+    single-tile items.  Sequence 1's last pair (tiles 10-11), which appends its prefix
+    to the cache, lies among them and stays a pair CTA; both calls match the oracle
+    and the cache is bit-exact."""
+    from gpu_cases import assert_close, tile_boundary_rows
+    case = ragged_case(95, [4096, 1500], heads=16)
+    pre = [3000, 1400]
+    cu_p = np.concatenate([[0], np.cumsum(pre)]).astype(np.int32)
+    layers, layer, cap = 1, 0, int(cu_p[-1]) + 64
+    st = _status()
+    out1, lse1, out2, lse2, ck, cv = _run_both(case, cu_p, layers, layer, cap, status=st)
+    assert bca.read_status(st) == 0
+    rows = np.unique(np.concatenate([tile_boundary_rows(case.cu_q, extra=200, seed=3),
+                                     np.arange(4096, 5596)]))   # every row of sequence 1
+    heads = np.array([2, 9, 15])
+    ref = case.reference(rows=rows, heads=heads)
+    assert_close(out1, lse1, *ref, rows=rows, heads=heads, what="prefill")
+    assert_close(out2, lse2, *ref, rows=rows, heads=heads, what="prefill_append")
+    ek, ev = _expected_cache(case.k, case.v, case.cu_k, cu_p, layers, layer, cap)
+    assert np.array_equal(ck.view(torch.int16).cpu().numpy(), ek)
+    assert np.array_equal(cv.view(torch.int16).cpu().numpy(), ev)
