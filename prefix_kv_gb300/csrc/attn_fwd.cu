@@ -708,7 +708,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.kv_empty[s]);
     }
-    if (lane == 0) bulk_wait_all();   // the stores are complete before the CTA ends
+    if (lane == 0) bulk_wait_read_all();   // the stages are read before the CTA ends
    }
   } else {
     regs_increase<kRegsSoftmax>();
@@ -979,7 +979,10 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
                 tma_store_3d(&tm_o, stage, 0, h, row0);
                 tma_store_3d(&tm_o, stage + kHalfBytes, 64, h, row0);
                 bulk_commit_group();
-                bulk_wait_all();   // complete before the CTA ends
+                // only the reads of the staged tile must end before the CTA does;
+                // its global writes complete before the grid does (0.3% prefill,
+                // 0.4% decode against waiting for them here)
+                bulk_wait_read_all();
               }
             } else {
               give_up();

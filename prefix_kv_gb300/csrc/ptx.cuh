@@ -90,10 +90,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 __device__ __forceinline__ void bulk_wait_read_all() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// This thread's committed bulk stores have completed.
-__device__ __forceinline__ void bulk_wait_all() {
-  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
 // ---------------------------------------------------------------- tcgen05
 // Programmatic dependent launch: let the grid launched after this one (with
 // programmatic stream serialization) start once every CTA of this grid has
