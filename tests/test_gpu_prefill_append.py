@@ -176,19 +176,33 @@ def test_prefill_append_paged_rejects_bad_page():
     assert (ck.view(torch.int16) == -1).all() and (cv.view(torch.int16) == -1).all()
 
 
-def test_prefill_append_key_split_tail_keeps_the_appending_pair():
+@pytest.mark.parametrize("paged", [False, True], ids=["contiguous", "paged"])
+def test_prefill_append_key_split_tail_keeps_the_appending_pair(paged):
     """A pair grid of 8 x 16 x 4 = 512 CTAs (under four waves of 152): its last 56 in
     launch order, those of the second head group of sequence 1, become key-split
     single-tile items.  Sequence 1's last pair (tiles 10-11), which appends its prefix
     to the cache, lies among them and stays a pair CTA; both calls match the oracle
-    and the cache is bit-exact."""
+    and the cache is bit-exact (against the oracle's append, or the standalone paged
+    append through the same page table)."""
     from gpu_cases import assert_close, tile_boundary_rows
     case = ragged_case(95, [4096, 1500], heads=16)
     pre = [3000, 1400]
     cu_p = np.concatenate([[0], np.cumsum(pre)]).astype(np.int32)
-    layers, layer, cap = 1, 0, int(cu_p[-1]) + 64
+    d = lambda x: x.to(DEV)
+    ti = lambda x: torch.from_numpy(np.asarray(x, dtype=np.int32)).to(DEV)
+    args = (d(case.q), d(case.k), d(case.v), ti(case.block_id), ti(case.cu_q), ti(case.cu_k),
+            case.max_q, case.max_k)
     st = _status()
-    out1, lse1, out2, lse2, ck, cv = _run_both(case, cu_p, layers, layer, cap, status=st)
+    out1, lse1 = bca.prefill(*args, status=st)
+    if paged:
+        pool = sum((p + 127) // 128 for p in pre) + 5
+        pt = _page_table(pre, pool, 95)
+        ck, cv = _sentinel_cache(1, 16, pool * 128)
+        out2, lse2 = bca.prefill_append(*args, ti(cu_p), ck, cv, 0, page_table=pt, status=st)
+    else:
+        cap = int(cu_p[-1]) + 64
+        ck, cv = _sentinel_cache(1, 16, cap)
+        out2, lse2 = bca.prefill_append(*args, ti(cu_p), ck, cv, 0, status=st)
     assert bca.read_status(st) == 0
     rows = np.unique(np.concatenate([tile_boundary_rows(case.cu_q, extra=200, seed=3),
                                      np.arange(4096, 5596)]))   # every row of sequence 1
@@ -196,6 +210,12 @@ def test_prefill_append_key_split_tail_keeps_the_appending_pair():
     ref = case.reference(rows=rows, heads=heads)
     assert_close(out1, lse1, *ref, rows=rows, heads=heads, what="prefill")
     assert_close(out2, lse2, *ref, rows=rows, heads=heads, what="prefill_append")
-    ek, ev = _expected_cache(case.k, case.v, case.cu_k, cu_p, layers, layer, cap)
-    assert np.array_equal(ck.view(torch.int16).cpu().numpy(), ek)
-    assert np.array_equal(cv.view(torch.int16).cpu().numpy(), ev)
+    if paged:
+        sk, sv = _sentinel_cache(1, 16, pool * 128)
+        bca.prefix_cache_append_paged(d(case.k), d(case.v), ti(case.cu_k), ti(cu_p), pt, sk, sv, 0)
+        assert torch.equal(sk.view(torch.int16), ck.view(torch.int16))
+        assert torch.equal(sv.view(torch.int16), cv.view(torch.int16))
+    else:
+        ek, ev = _expected_cache(case.k, case.v, case.cu_k, cu_p, 1, 0, cap)
+        assert np.array_equal(ck.view(torch.int16).cpu().numpy(), ek)
+        assert np.array_equal(cv.view(torch.int16).cpu().numpy(), ev)
