@@ -140,6 +140,11 @@ size_t bca_prefill_workspace_bytes(int32_t batch, int32_t total_q, int32_t max_s
  * out: device bf16 [total_q, H, 128]; lse: device fp32 [H, total_q];
  * workspace: device, >= bca_prefill_workspace_bytes(batch, total_q, max_seqlen_q).
  * A sequence that fails validation gets no output (its rows are left as they were).
+ * Launches two or three kernels on `stream`: the schedule prep; the query-tile
+ * pairs, which may start while the prep runs (programmatic dependent launch) and
+ * read its records only once it has completed; and, for a pair grid of at most
+ * four waves past two whole ones, the pairs of its last, partly filled wave as
+ * key-split single tiles in a third grid that may start as the pairs drain.
  */
 bca_status bca_prefill(const void* q, const void* k, const void* v, const int32_t* block_id,
                        const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_k,
@@ -231,7 +236,8 @@ bca_status bca_prefill_noalloc(const void* q, const void* k, const void* v,
  * (the segment table is built on the host).  q, k, v, out, lse as in
  * bca_prefill.  workspace: device memory of
  * bca_prefill_piecewise_workspace_bytes (16-byte aligned), reused by the
- * pieces in stream order.  Launches two kernels and one 2-D copy per segment. */
+ * pieces in stream order.  Launches two or three kernels (as bca_prefill) and one
+ * 2-D copy per segment. */
 size_t bca_prefill_piecewise_workspace_bytes(const int32_t* block_id_host,
                                              const int32_t* cu_seqlens_host, int32_t batch,
                                              int32_t num_heads);
