@@ -301,9 +301,10 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     // before this wait.
     // (A key-split item belongs to a grid launched after the pair grid, which it may
     // run beside: it reads the records without that wait.  It starts only after
-    // every pair CTA has started, and the host splits only past two full waves of
-    // pair CTAs, so some pair CTA has ended, after its own wait for the prep.  The
-    // records are read through L2.)
+    // every pair CTA has started.  The host splits only past two full waves of pair
+    // CTAs (one per SM at a time), none of which ends before the prep has completed
+    // (those with nothing to do wait for it too), so one of them has ended, after
+    // the prep, before the last could start.  The records are read through L2.)
     if constexpr (!kSplit) {
       grid_dependency_wait();
       for (int i = 0; i < 2; ++i) {
@@ -1036,6 +1037,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a pair of the last, partly filled wave is done by the key-split grid (never
     // the pair that appends to the cache)
     if (launch_idx >= p.prefill_split_from && !pair_appends(p, b, m_base)) return;
+    // Any other pair CTA ends only after the schedule prep has completed, even with
+    // no rows to do: the key-split grid relies on it.  (One that finds another CTA
+    // has given up ends at once; the split CTAs, which start later, then do too.)
+    if (m_base * kBlockM >= p.cu_q[b + 1] - p.cu_q[b]) {
+      grid_dependency_wait();
+      return;
+    }
     attn_item<false, false, kPagedAppend>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, h, b,
                                           m_base, 2);
   } else if constexpr (!kDecode) {
