@@ -10,8 +10,9 @@
 // softmax warpgroup turns S into P the tensor core runs the other tile's MMAs.
 // Because S_i(j+1) is issued after PV_i(j), the commit that signals S_i(j+1)
 // also covers PV_i(j): the softmax may rescale O_i right after seeing S_i(j+1).
-// Decode items that would fill less than half of a last wave run in a second
-// grid as single query tiles whose key range is split in two: warpgroup i runs
+// Decode items that would fill less than half of a last wave, and the pairs of a
+// short prefill grid's last, partly filled wave, run in a second grid as single
+// query tiles whose key range is split in two: warpgroup i runs
 // the same loop over its part with its own K/V tiles, and warpgroup 0 merges
 // the two partial rows, each against its own reference max, at the end.  Such
 // an item takes ~0.6 of a pair's time, where a single tile on one warpgroup
