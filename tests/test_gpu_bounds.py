@@ -9,8 +9,8 @@ oracle at the parity tolerances, and must be bit-identical to the release
 library's result (the checks change no arithmetic).  The shapes are the ragged
 ones where partial tiles are written: sequence lengths 1, 127, 129 and 1537,
 queries shorter than keys, a prefix that ends inside a tile, an empty prefix,
-paged tables whose last page is partly used, and a decode grid large enough to
-run both the tile-pair grid and the key-split tail.
+paged tables whose last page is partly used, and prefill and decode grids large
+enough to run both the tile-pair grid and the key-split grid.
 """
 import math
 
@@ -138,6 +138,33 @@ def test_bounds_prefill_paged_append_last_page_partial():
         written = ~np.isnan(exp)
         assert np.array_equal(g[written], exp[written])
         assert np.isnan(g[~written]).all()
+
+
+def test_bounds_prefill_key_split_tail():
+    """A pair grid short enough for the key-split grid (32 heads, sequences of 2300 and,
+    bottom-right, 1900 of 2400 keys: 576 pair CTAs, the last 120 split), with the
+    cache append: its last pair of sequence 1 stays a pair CTA.  Sampled rows
+    against the oracle, bit-identical to the release build."""
+    case = ragged_case(203, [2300, 2400], [2300, 1900], heads=32, max_spans=6, max_span=700)
+    pre = [1000, 1700]
+    cp = np.concatenate([[0], np.cumsum(pre)]).astype(np.int32)
+    cap = int(cp[-1]) + 64
+
+    def run(st):
+        ck = torch.full((1, 32, cap, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+        cv = torch.full_like(ck, float("nan"))
+        out, lse = bca.prefill_append(case.q.to(DEV), case.k.to(DEV), case.v.to(DEV),
+                                      _ti(case.block_id), _ti(case.cu_q), _ti(case.cu_k),
+                                      case.max_q, case.max_k, _ti(cp), ck, cv, 0, SCALE,
+                                      status=st)
+        return out, lse, ck, cv
+
+    rel, dbg = _both(run)
+    _same(rel, dbg)
+    rows = np.r_[0:130, 1020:1040, 2170:2300, 2300:2430, 4100:4200]
+    heads = np.array([1, 20, 31])
+    ref_out, ref_lse = case.reference(rows=rows, heads=heads)
+    assert_close(dbg[0], dbg[1], ref_out, ref_lse, rows=rows, heads=heads, what="debug split")
 
 
 # ---------------------------------------------------------------- decode
