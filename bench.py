@@ -192,13 +192,23 @@ def prefill_grids(num_heads, max_q, batch, sms):
     return 1 + int(0 < tail and total - tail >= 2 * sms and total <= 4 * sms)
 
 
-def decode_grids(num_heads, max_q, batch, sms):
+def decode_grids(num_heads, max_q, batch, sms, max_prefix=None):
     """Grids one decode call launches: tile pairs (head x pair x sequence) fill
-    whole waves of the SMs; a last wave at most half full becomes a second grid
-    of key-split single tiles (two CTAs per pair)."""
+    whole waves of the SMs.  With a workspace (``max_prefix`` given), a last,
+    partly filled wave worth balancing becomes two more grids: its pieces of equal
+    key ranges (one range per SM, at least 8 key tiles per range, fewer pairs than
+    ranges, and a range plus 16 key tiles shorter than the wave's cost otherwise)
+    and their merge.  Otherwise a last wave at most half full becomes a second grid
+    of key-split single tiles (two CTAs per pair), each about 0.6 of a pair."""
     pairs = (-(-max_q // 128) + 1) // 2
     items = num_heads * pairs * batch
     tail = items % sms
+    if max_prefix is not None and tail > 0:
+        nkv = -(-max_prefix // 128) + -(-max_q // 128)
+        ranges = min(sms, 256, tail * nkv // 8)
+        otherwise = 0.6 * nkv if 2 * tail <= sms else nkv
+        if ranges > tail and tail * nkv / ranges + 16 < otherwise:
+            return int(items > tail) + 2
     split_from = items - tail if 0 < tail and 2 * tail <= sms else items
     return int(split_from > 0) + int(items > split_from)
 
@@ -248,12 +258,17 @@ class Problem:
         vdt = torch.bfloat16 if self.fp8_mode is None else torch.uint8
         self.cache_k = torch.empty((1, self.H, self.P, 128), dtype=kdt, device=dev)
         self.cache_v = torch.empty((1, self.H, self.P, 128), dtype=vdt, device=dev)
+        # the decode's balanced tail: its partial rows (FP8: after the expanded layers)
+        self.tail_bytes = bca.prefix_decode_workspace_bytes(self.batch, self.H, self.max_n,
+                                                            self.max_p) if wl.decode else 0
+        self.tail_ws = (torch.empty(self.tail_bytes, dtype=torch.uint8, device=dev)
+                        if self.tail_bytes else None)
         if self.fp8_mode is not None:
             self.scale_k = torch.empty((1, self.H, self.P), dtype=torch.float32, device=dev)
             self.scale_v = torch.empty_like(self.scale_k)
             self.dec_ws = torch.empty(
-                bca.prefix_decode_fp8_workspace_bytes(self.fp8_mode, self.H, self.P),
-                dtype=torch.uint8, device=dev)
+                bca.prefix_decode_fp8_workspace_bytes(self.fp8_mode, self.H, self.P) +
+                self.tail_bytes, dtype=torch.uint8, device=dev)
         self.ws = torch.empty(bca.prefill_workspace_bytes(self.batch, self.S, self.max_s),
                               dtype=torch.uint8,
                               device=dev)
@@ -278,7 +293,8 @@ class Problem:
         self.sms = sms
         pre_grids = prefill_grids(self.H, self.max_s, self.batch, sms)
         self.launches = (2 + pre_grids + {None: 0, "v": 1, "kv": 2}[self.fp8_mode] +
-                         decode_grids(self.H, self.max_n, self.batch, sms) if wl.decode
+                         decode_grids(self.H, self.max_n, self.batch, sms,
+                                      self.max_p if self.tail_bytes else None) if wl.decode
                          else 1 + pre_grids)   # prefill only: schedule prep + attention
         # optional Q/K prologue (RMS norm + three-axis RoPE; the prefill-side call also
         # appends): coordinates and rotation table once per layout, outside the step
@@ -396,11 +412,11 @@ class Problem:
             bca.prefix_decode_paged(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"],
                                     self.page_table, d["k_tgt"], d["v_tgt"], d["cu_tgt"],
                                     self.max_n, self.max_p, self.scale, out=self.dout, lse=self.dlse,
-                                    status=self.status)
+                                    status=self.status, workspace=self.tail_ws)
         elif self.fp8_mode is None:
             bca.prefix_decode(d["q_tgt"], self.cache_k, self.cache_v, 0, d["cu_pre"], d["k_tgt"],
                               d["v_tgt"], d["cu_tgt"], self.max_n, self.max_p, self.scale, out=self.dout,
-                              lse=self.dlse, status=self.status)
+                              lse=self.dlse, status=self.status, workspace=self.tail_ws)
         else:
             bca.prefix_decode_fp8(d["q_tgt"], self.cache_k, self.cache_v, self.scale_k,
                                   self.scale_v, 0, d["cu_pre"], d["k_tgt"], d["v_tgt"],
@@ -480,7 +496,7 @@ def _prologue_step(self, d, events=None):
         events[3].record()
     bca.prefix_decode(self.qt_rot, self.cache_k, self.cache_v, 0, d["cu_pre"], self.kt_rot,
                       d["v_tgt"], d["cu_tgt"], self.max_n, self.max_p, self.scale, out=self.dout,
-                      lse=self.dlse, status=self.status)
+                      lse=self.dlse, status=self.status, workspace=self.tail_ws)
     if events:
         events[4].record()
 

@@ -259,10 +259,26 @@ bca_status bca_prefill_piecewise(const void* q, const void* k, const void* v,
  * cache_k/v: device bf16 [num_layers][H][capacity][128]; sequence b's prefix
  * is cache tokens cu_prefix[b] .. cu_prefix[b+1]-1 of layer `layer`;
  * cu_prefix: device int32 [batch+1]; out/lse as in bca_prefill.
- * max_prefix bounds cu_prefix[b+1]-cu_prefix[b].
- * Launches one or two kernels on `stream`: the query-tile pairs, and, when
- * they would leave a last wave at most half full, that wave's pairs as
- * key-split single tiles in a second grid that may start as the first drains.
+ * max_seqlen_q bounds every target length and max_prefix every prefix length
+ * cu_prefix[b+1]-cu_prefix[b]; with the balanced tail below, a sequence whose
+ * prefix and target tiles outnumber those of max_prefix and max_seqlen_q is
+ * reported as BCA_ERR_SEQLENS.
+ *
+ * The query-tile pairs of all (sequence, head) run as one grid.  The pairs of a
+ * last, partly filled wave run in a second grid that may start as the first
+ * drains, in one of two ways:
+ *  - workspace given (device memory of at least
+ *    bca_prefix_decode_workspace_bytes, 16-byte aligned, else BCA_ERR_WORKSPACE):
+ *    the balanced tail.  Those pairs' key tiles are cut into one equal range
+ *    per SM; every piece leaves partial rows (unnormalised fp32 O, row max and
+ *    row sum) in the workspace, and a third, small grid merges each pair's
+ *    pieces into out and lse.  The workspace is scratch, free again once the
+ *    stream passes the call; nothing in it needs initialising.
+ *  - workspace NULL: when the wave would be at most half full, its pairs run
+ *    as key-split single tiles (each tile's keys shared out between the two
+ *    softmax warpgroups of one CTA), otherwise as plain pairs.
+ * Both give the attention of the pages within the same tolerance; they round
+ * differently, so their outputs are not bit-identical.
  */
 bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void* cache_v,
                              int32_t layer, int32_t num_layers, int64_t capacity,
@@ -270,7 +286,17 @@ bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void*
                              const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
                              int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
                              int32_t max_prefix, float softmax_scale, void* out, float* lse,
-                             int32_t* status_dev, void* stream);
+                             void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                             void* stream);
+
+/* Workspace bytes that give the decodes (bca_prefix_decode and its paged and
+ * FP8 forms) the balanced tail on the current device: two partial slots of
+ * 133,120 bytes per SM when (batch, heads, max_seqlen_q, max_prefix) leave a
+ * last, partly filled wave of query-tile pairs that is worth balancing; 0 when
+ * they do not (the decode then needs no workspace) or the arguments are
+ * invalid. */
+size_t bca_prefix_decode_workspace_bytes(int32_t batch, int32_t num_heads, int32_t head_dim,
+                                         int32_t max_seqlen_q, int32_t max_prefix);
 
 /* ------------------------------------------------------------------------ */
 /* Prefix cache append (the "extract" step): clone the first
@@ -342,7 +368,9 @@ size_t bca_prefix_decode_fp8_workspace_bytes(int32_t mode, int32_t num_heads, in
  * (bca_prefix_cache_dequant_fp8) into `workspace`, device memory of at least
  * bca_prefix_decode_fp8_workspace_bytes (16-byte aligned, else
  * BCA_ERR_WORKSPACE), then attended exactly as by bca_prefix_decode; the
- * workspace is scratch, free again once the stream passes the call.  mode,
+ * workspace is scratch, free again once the stream passes the call.  When the
+ * workspace holds bca_prefix_decode_workspace_bytes more bytes after those, the
+ * decode uses them for its balanced tail (else its key-split tail).  mode,
  * cache_k, cache_v, scale_k and scale_v are laid out as in
  * bca_prefix_cache_append_fp8 (scale_k is not read in BCA_FP8_V mode).  All
  * other arguments, layouts and errors are those of bca_prefix_decode; an
@@ -429,7 +457,8 @@ bca_status bca_prefix_cache_append_paged(const void* k, const void* v,
                                          int32_t layer, int32_t num_layers, int32_t num_pages,
                                          int32_t* status_dev, void* stream);
 
-/* bca_prefix_decode with the prefix read through a page table. */
+/* bca_prefix_decode with the prefix read through a page table (workspace as
+ * there: NULL, or bca_prefix_decode_workspace_bytes for the balanced tail). */
 bca_status bca_prefix_decode_paged(const void* q_tgt, const void* cache_k, const void* cache_v,
                                    int32_t layer, int32_t num_layers, int32_t num_pages,
                                    const int32_t* cu_prefix, const int32_t* page_table,
@@ -437,7 +466,8 @@ bca_status bca_prefix_decode_paged(const void* q_tgt, const void* cache_k, const
                                    const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
                                    int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
                                    int32_t max_prefix, float softmax_scale, void* out, float* lse,
-                                   int32_t* status_dev, void* stream);
+                                   void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                                   void* stream);
 
 /* bca_prefix_cache_append_fp8 into a paged cache: codes and scales of prefix
  * token t of sequence b go to page token page_table[b * max_pages + t / 128] *
@@ -461,8 +491,10 @@ size_t bca_prefix_decode_fp8_paged_workspace_bytes(int32_t num_heads, int32_t he
  * dequantised to bf16(fp32(value(code)) * scale), a bf16 K (BCA_FP8_V mode) is
  * copied.  Then the contiguous bf16 decode runs on the gathered rows.
  * prefix_rows >= cu_prefix[batch] bounds the gathered rows (a larger
- * cu_prefix[batch] is BCA_ERR_CAPACITY on the status word).  Other arguments
- * as in bca_prefix_decode_paged and bca_prefix_decode_fp8. */
+ * cu_prefix[batch] is BCA_ERR_CAPACITY on the status word).  Workspace bytes
+ * beyond bca_prefix_decode_fp8_paged_workspace_bytes serve the balanced tail as
+ * in bca_prefix_decode_fp8.  Other arguments as in bca_prefix_decode_paged and
+ * bca_prefix_decode_fp8. */
 bca_status bca_prefix_decode_fp8_paged(
     const void* q_tgt, const void* cache_k, const void* cache_v, int32_t mode,
     const float* scale_k, const float* scale_v, int32_t layer, int32_t num_layers,

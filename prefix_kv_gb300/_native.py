@@ -47,7 +47,8 @@ SIGNATURES = {
                                     c_i32, c_i32, c_i32, c_f32, c_vp, c_vp, c_vp, c_vp]),
     "bca_prefix_decode": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i64, c_vp, c_vp, c_vp,
                                   c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_f32, c_vp,
-                                  c_vp, c_vp, c_vp]),
+                                  c_vp, c_vp, c_size, c_vp, c_vp]),
+    "bca_prefix_decode_workspace_bytes": (c_size, [c_i32, c_i32, c_i32, c_i32, c_i32]),
     "bca_prefix_decode_fp8": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_vp, c_vp, c_i32, c_i32, c_i64,
                                       c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32,
                                       c_i32, c_f32, c_vp, c_vp, c_vp, c_size, c_vp, c_vp]),
@@ -62,7 +63,7 @@ SIGNATURES = {
                                               c_vp]),
     "bca_prefix_decode_paged": (c_i32, [c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_vp, c_vp, c_i32,
                                         c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_i32, c_i32,
-                                        c_f32, c_vp, c_vp, c_vp, c_vp]),
+                                        c_f32, c_vp, c_vp, c_vp, c_size, c_vp, c_vp]),
     "bca_prefix_cache_append_fp8_paged": (c_i32, [c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32,
                                                   c_i32, c_i32, c_i32, c_i32, c_vp, c_vp, c_vp,
                                                   c_vp, c_i32, c_i32, c_i32, c_vp, c_vp]),

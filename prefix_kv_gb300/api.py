@@ -180,10 +180,35 @@ def prefill_append(q, k, v, block_id, cu_seqlens_q, cu_seqlens_k, max_seqlen_q: 
     return out, lse
 
 
+def prefix_decode_workspace_bytes(batch: int, num_heads: int, max_seqlen_q: int, max_prefix: int,
+                                  head_dim: int = 128) -> int:
+    """Bytes of the decode workspace that enables the balanced tail (0: none needed)."""
+    return int(_native.load().bca_prefix_decode_workspace_bytes(batch, num_heads, head_dim,
+                                                                max_seqlen_q, max_prefix))
+
+
+def _tail_workspace(workspace, balanced_tail: bool, batch: int, H: int, max_seqlen_q: int,
+                    max_prefix: int, D: int, device, extra: int = 0):
+    """The caller's workspace, or one allocated here: ``extra`` bytes for the FP8
+    decodes' bf16 layers, then the balanced tail's slots when ``balanced_tail``."""
+    if workspace is not None:
+        return workspace
+    tail = prefix_decode_workspace_bytes(batch, H, max_seqlen_q, max_prefix, D) \
+        if balanced_tail else 0
+    if extra + tail == 0:
+        return None
+    return torch.empty(extra + tail, dtype=torch.uint8, device=device)
+
+
 def prefix_decode(q_tgt, cache_k, cache_v, layer: int, cu_prefix, k_tgt, v_tgt, cu_seqlens_q,
                   max_seqlen_q: int, max_prefix: int, softmax_scale: Optional[float] = None,
-                  out=None, lse=None, status=None, stream=None):
-    """Target queries over [cached prefix; own K/V], no mask.  Cache ``[L, H, cap, 128]``."""
+                  out=None, lse=None, status=None, stream=None, workspace=None,
+                  balanced_tail: bool = True):
+    """Target queries over [cached prefix; own K/V], no mask.  Cache ``[L, H, cap, 128]``.
+
+    ``workspace``: a device uint8 tensor of ``prefix_decode_workspace_bytes`` bytes for
+    the balanced tail, allocated here when omitted; ``balanced_tail=False`` (and no
+    workspace) runs the key-split tail instead."""
     for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
         _need(t, name, torch.bfloat16, 3)
     _need(cache_k, "cache_k", torch.bfloat16, 4)
@@ -205,10 +230,13 @@ def prefix_decode(q_tgt, cache_k, cache_v, layer: int, cu_prefix, k_tgt, v_tgt, 
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
     _need(out, "out", torch.bfloat16, 3)
     _need(lse, "lse", torch.float32, 2)
+    workspace = _tail_workspace(workspace, balanced_tail, batch, H, max_seqlen_q, max_prefix, D,
+                                q_tgt.device)
     code = _native.load().bca_prefix_decode(
         _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), layer, L, cap, _ptr(cu_prefix), _ptr(k_tgt),
         _ptr(v_tgt), _ptr(cu_seqlens_q), batch, H, D, total_q, max_seqlen_q, max_prefix,
-        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream))
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream))
     _native.check(code, "bca_prefix_decode")
     return out, lse
 
@@ -300,11 +328,12 @@ def prefix_cache_dequant_fp8(codes, scales, cu_prefix, layer: int, out=None, sta
 def prefix_decode_fp8(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: int, cu_prefix, k_tgt,
                       v_tgt, cu_seqlens_q, max_seqlen_q: int, max_prefix: int,
                       softmax_scale: Optional[float] = None, mode: str = "v", out=None, lse=None,
-                      workspace=None, status=None, stream=None):
+                      workspace=None, status=None, stream=None, balanced_tail: bool = True):
     """``prefix_decode`` over an FP8 E4M3 cache written by ``prefix_cache_append_fp8``
     in the same ``mode`` (cache and scale layouts as there).  ``workspace``: a
-    device uint8 tensor of ``prefix_decode_fp8_workspace_bytes`` bytes (allocated
-    here when omitted)."""
+    device uint8 tensor of ``prefix_decode_fp8_workspace_bytes`` bytes, plus
+    ``prefix_decode_workspace_bytes`` for the balanced tail (allocated here when
+    omitted)."""
     for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
         _need(t, name, torch.bfloat16, 3)
     m = FP8_MODES[mode]
@@ -332,15 +361,14 @@ def prefix_decode_fp8(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: int, cu_
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
     _need(out, "out", torch.bfloat16, 3)
     _need(lse, "lse", torch.float32, 2)
-    if workspace is None:
-        workspace = torch.empty(prefix_decode_fp8_workspace_bytes(mode, H, cap, D),
-                                dtype=torch.uint8, device=q_tgt.device)
+    workspace = _tail_workspace(workspace, balanced_tail, batch, H, max_seqlen_q, max_prefix, D,
+                                q_tgt.device, prefix_decode_fp8_workspace_bytes(mode, H, cap, D))
     code = _native.load().bca_prefix_decode_fp8(
         _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), m, _ptr(scale_k) if mode == "kv" else None,
         _ptr(scale_v), layer, L, cap, _ptr(cu_prefix), _ptr(k_tgt), _ptr(v_tgt),
         _ptr(cu_seqlens_q), batch, H, D, total_q, max_seqlen_q, max_prefix,
-        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
-        _ptr(status), _stream(stream))
+        float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(status), _stream(stream))
     _native.check(code, "bca_prefix_decode_fp8")
     return out, lse
 
@@ -538,8 +566,9 @@ def prefix_cache_append_paged(k, v, cu_seqlens_k, cu_prefix, page_table, cache_k
 def prefix_decode_paged(q_tgt, cache_k, cache_v, layer: int, cu_prefix, page_table, k_tgt, v_tgt,
                         cu_seqlens_q, max_seqlen_q: int, max_prefix: int,
                         softmax_scale: Optional[float] = None, out=None, lse=None, status=None,
-                        stream=None):
-    """``prefix_decode`` with the prefix read through ``page_table``."""
+                        stream=None, workspace=None, balanced_tail: bool = True):
+    """``prefix_decode`` with the prefix read through ``page_table`` (``workspace`` and
+    ``balanced_tail`` as there)."""
     for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
         _need(t, name, torch.bfloat16, 3)
     _need(cu_prefix, "cu_prefix", torch.int32, 1)
@@ -553,11 +582,14 @@ def prefix_decode_paged(q_tgt, cache_k, cache_v, layer: int, cu_prefix, page_tab
         out = torch.empty_like(q_tgt)
     if lse is None:
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
+    workspace = _tail_workspace(workspace, balanced_tail, batch, H, max_seqlen_q, max_prefix, D,
+                                q_tgt.device)
     code = _native.load().bca_prefix_decode_paged(
         _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), layer, L, n_pages, _ptr(cu_prefix),
         _ptr(page_table), page_table.shape[1], _ptr(k_tgt), _ptr(v_tgt), _ptr(cu_seqlens_q),
         batch, H, D, total_q, max_seqlen_q, max_prefix, float(softmax_scale), _ptr(out),
-        _ptr(lse), _ptr(status), _stream(stream))
+        _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel(), _ptr(status),
+        _stream(stream))
     _native.check(code, "bca_prefix_decode_paged")
     return out, lse
 
@@ -604,10 +636,11 @@ def prefix_decode_fp8_paged(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: in
                             page_table, prefix_rows: int, k_tgt, v_tgt, cu_seqlens_q,
                             max_seqlen_q: int, max_prefix: int,
                             softmax_scale: Optional[float] = None, mode: str = "v", out=None,
-                            lse=None, workspace=None, status=None, stream=None):
+                            lse=None, workspace=None, status=None, stream=None,
+                            balanced_tail: bool = True):
     """Decode over a paged FP8 cache: gather (+ dequantise) the prefixes into a
     workspace packed by ``cu_prefix`` (``prefix_rows >= cu_prefix[-1]``), then
-    the contiguous decode."""
+    the contiguous decode (its balanced tail in the workspace's remaining bytes)."""
     for name, t in (("q_tgt", q_tgt), ("k_tgt", k_tgt), ("v_tgt", v_tgt)):
         _need(t, name, torch.bfloat16, 3)
     m = FP8_MODES[mode]
@@ -623,14 +656,15 @@ def prefix_decode_fp8_paged(q_tgt, cache_k, cache_v, scale_k, scale_v, layer: in
     if lse is None:
         lse = torch.empty((H, total_q), dtype=torch.float32, device=q_tgt.device)
     lib = _native.load()
-    if workspace is None:
-        workspace = torch.empty(lib.bca_prefix_decode_fp8_paged_workspace_bytes(H, D, prefix_rows),
-                                dtype=torch.uint8, device=q_tgt.device)
+    workspace = _tail_workspace(workspace, balanced_tail, batch, H, max_seqlen_q, max_prefix, D,
+                                q_tgt.device,
+                                lib.bca_prefix_decode_fp8_paged_workspace_bytes(H, D, prefix_rows))
     code = lib.bca_prefix_decode_fp8_paged(
         _ptr(q_tgt), _ptr(cache_k), _ptr(cache_v), m, _ptr(scale_k) if mode == "kv" else None,
         _ptr(scale_v), layer, L, cap // PAGE_TOKENS, _ptr(cu_prefix), _ptr(page_table),
         page_table.shape[1], prefix_rows, _ptr(k_tgt), _ptr(v_tgt), _ptr(cu_seqlens_q), batch, H,
         D, total_q, max_seqlen_q, max_prefix, float(softmax_scale), _ptr(out), _ptr(lse),
-        _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream))
+        _ptr(workspace), 0 if workspace is None else workspace.numel(), _ptr(status),
+        _stream(stream))
     _native.check(code, "bca_prefix_decode_fp8_paged")
     return out, lse

@@ -10,13 +10,20 @@
 // softmax warpgroup turns S into P the tensor core runs the other tile's MMAs.
 // Because S_i(j+1) is issued after PV_i(j), the commit that signals S_i(j+1)
 // also covers PV_i(j): the softmax may rescale O_i right after seeing S_i(j+1).
-// Decode items that would fill less than half of a last wave, and the pairs of a
-// short prefill grid's last, partly filled wave, run in a second grid as single
-// query tiles whose key range is split in two: warpgroup i runs
-// the same loop over its part with its own K/V tiles, and warpgroup 0 merges
-// the two partial rows, each against its own reference max, at the end.  Such
-// an item takes ~0.6 of a pair's time, where a single tile on one warpgroup
-// would take 0.7.
+// The pairs of a short prefill grid's last, partly filled wave (and, when the
+// caller gives no workspace, decode pairs that would fill less than half of a
+// last wave) run in a second grid as single query tiles whose key range is
+// split in two: warpgroup i runs the same loop over its part with its own K/V
+// tiles, and warpgroup 0 merges the two partial rows, each against its own
+// reference max, at the end.  Such an item takes ~0.6 of a pair's time, where
+// a single tile on one warpgroup would take 0.7.
+// With a workspace, the decode pairs of a last, partly filled wave are instead
+// cut into as many equal key ranges as there are SMs (a range may end inside
+// one pair and go on in the next; then it is two pieces).  Every piece runs as
+// a pair item over its key tiles and leaves its unnormalised rows, reference
+// max and row sum in the workspace; a merge grid combines the pieces of each
+// pair.  The longer pieces launch first and the shorter ones after them, in
+// the order in which the SMs holding their range's other piece free up.
 // The reference max is taken exactly on the first K tile; afterwards P is
 // formed against it directly and the max is only recomputed (with O and l
 // rescaled) for a tile whose row sum would exceed 2^16.  O and l share the
@@ -52,6 +59,7 @@
 #include "ptx.cuh"
 
 #include <cudaTypedefs.h>
+#include <algorithm>
 #include <mutex>
 
 namespace bca {
@@ -125,7 +133,44 @@ struct FwdParams {
   __nv_bfloat16* out;
   float* lse;
   int32_t* status;
+  // Decode, balanced tail: the pairs decode_split_from.. (tail pairs t = 0, 1, ..),
+  // seg_nkv key tiles each, laid end to end as seg_total = pairs * seg_nkv
+  // iterations and cut into seg_ranges equal ranges; range c is part 0 (up to the
+  // next pair boundary) and, if it crosses one, part 1.  Piece (c, part) leaves its
+  // partial rows in slot 2c + part of seg_ws.  seg_order lists the ranges that
+  // cross a boundary by ascending length of their longer part.
+  int seg_ranges;
+  int seg_nkv;
+  int64_t seg_total;
+  float* seg_ws;
+  uint16_t seg_order[kMaxSegRanges];
 };
+
+// ---- balanced decode tail: ranges, pieces and partial slots ----------------------
+// (the host plans with the same arithmetic)
+__host__ __device__ __forceinline__ int64_t seg_start(int64_t c, int64_t total, int ranges) {
+  return c * total / ranges;
+}
+// Part `part` of range c as virtual iterations [v0, v1); v1 <= v0 when absent.
+__host__ __device__ __forceinline__ void seg_piece(int c, int part, int64_t total, int ranges,
+                                                   int nkv, int64_t& v0, int64_t& v1) {
+  const int64_t s = seg_start(c, total, ranges), e = seg_start(c + 1, total, ranges);
+  const int64_t pb = (s / nkv + 1) * nkv;   // first pair boundary after s
+  if (part == 0) {
+    v0 = s;
+    v1 = e < pb ? e : pb;
+  } else {
+    v0 = pb;
+    v1 = e;
+  }
+}
+// The longer part of range c (0 for a range inside one pair).
+__host__ __device__ __forceinline__ int seg_long_part(int c, int64_t total, int ranges, int nkv) {
+  int64_t a0, a1, b0, b1;
+  seg_piece(c, 0, total, ranges, nkv, a0, a1);
+  seg_piece(c, 1, total, ranges, nkv, b0, b1);
+  return b1 - b0 > a1 - a0 ? 1 : 0;
+}
 
 // Prefill with cache append: the CTA of a sequence's last tile pair also writes the
 // sequence's prefix K/V to the cache (it reads every key tile of the sequence).
@@ -141,16 +186,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 // One work item: head h, sequence b and its query tiles m_base .. m_base + n_qt - 1
 // (kSplit: the single tile m_base for both softmax warpgroups, each over part
-// of the key range; their partial results are merged at the end).
-template <bool kDecode, bool kSplit, bool kPagedAppend>
+// of the key range; their partial results are merged at the end.  kSeg: a decode
+// pair over its key tiles [seg_kt0, seg_kt1) only, whose unnormalised rows, row
+// maxima and sums go to the partial slot seg_slot instead of out and lse).
+template <bool kDecode, bool kSplit, bool kPagedAppend, bool kSeg = false>
 __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                                           const CUtensorMap& tm_v, const CUtensorMap& tm_k2,
                                           const CUtensorMap& tm_v2, const CUtensorMap& tm_o,
                                           const FwdParams& p, FwdSmem& sm,
                                           const int h, const int b, const int m_base,
-                                          const int n_qt) {
+                                          const int n_qt, const int seg_kt0 = 0,
+                                          const int seg_kt1 = 0, float* seg_slot = nullptr) {
   static_assert(!(kSplit && kPagedAppend), "a key-split item never appends");
   static_assert(!kPagedAppend || !kDecode, "the cache append is a prefill option");
+  static_assert(!kSeg || (kDecode && !kSplit), "a balanced-tail piece is a decode pair item");
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   // Another CTA already gave up waiting: do not start new work.
@@ -180,6 +229,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
   int n_pre = 0;       // decode: prefix keys
   int pre0 = 0;        // decode: first cache token of the prefix
   int n_pre_tiles = 0;
+  int koff = 0;        // balanced-tail piece: its first key tile (0 otherwise)
   if constexpr (kDecode) {
     pre0 = p.cu_prefix[b];
     const int pre1 = p.cu_prefix[b + 1];
@@ -204,6 +254,10 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     if (__syncthreads_or(bad)) {
       if (threadIdx.x == 0 && h == 0 && m_base == 0)
         report_status(p.status, n_pre < 0 ? BCA_ERR_SEQLENS : BCA_ERR_CAPACITY);
+      if constexpr (kSeg) {
+        // a row sum of -1 marks the slot's pair as failed for the merge
+        if (threadIdx.x < 2 * kBlockM) seg_slot[kSegSlotO + 2 * threadIdx.x + 1] = -1.f;
+      }
       return;
     }
     const int n_all = n_pre_tiles + (q_len + kBlockN - 1) / kBlockN;
@@ -212,6 +266,13 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       // rest (as many or one more; all of a single tile)
       nkt[1] = n_all / 2;
       nkt[0] = n_all - nkt[1];
+    } else if constexpr (kSeg) {
+      // the piece's key tiles of the pair, up to the sequence's last one (the merge
+      // skips a piece that starts past it, as this one returns without a write)
+      const int n_seg = min(seg_kt1, n_all) - seg_kt0;
+      if (n_seg <= 0) return;
+      koff = seg_kt0;
+      for (int i = 0; i < 2; ++i) nkt[i] = rows_valid[i] > 0 ? n_seg : 0;
     } else {
       for (int i = 0; i < 2; ++i) nkt[i] = rows_valid[i] > 0 ? n_all : 0;
     }
@@ -400,9 +461,9 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
         return true;
       };
       if constexpr (!kSplit) {
-        // K_j, V_j shared by both query tiles: loads 2j and 2j + 1
+        // K_j, V_j shared by both query tiles: loads 2j and 2j + 1 (of key tile koff + j)
         for (int i = 0; i < 2 * nk; ++i)
-          if (!load(i, i & 1, i >> 1)) break;
+          if (!load(i, i & 1, koff + (i >> 1))) break;
       } else {
         // Each warpgroup has its own tiles; loads follow the MMA thread's order of
         // use: K_0(0), K_1(0), then per step j: V_0(j), K_0(j+1), V_1(j), K_1(j+1).
@@ -512,7 +573,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
         // decode).
         bool v_ready = false;   // V(j) landed and fixed ahead of iteration j
         if (n_both > 0 && ok) {
-          ok = landed(1) && fix_tail(0, stage_of(1));
+          ok = landed(1) && fix_tail(koff, stage_of(1));
           v_ready = true;
         }
         for (; j < n_both && ok; ++j) {
@@ -534,7 +595,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
           }
           tc_fence_after();
           issue_pv(1, vs, j, false);
-          if (!(landed(2 * j + 3) && fix_tail(j + 1, stage_of(2 * j + 3)))) {
+          if (!(landed(2 * j + 3) && fix_tail(koff + j + 1, stage_of(2 * j + 3)))) {
             ok = false;
             break;
           }
@@ -542,7 +603,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
         }
         for (; j < nk && ok; ++j) {
           const int vs = stage_of(2 * j + 1), ks = stage_of(2 * j + 2);
-          ok = (v_ready && j == n_both) || (landed(2 * j + 1) && fix_tail(j, vs));
+          ok = (v_ready && j == n_both) || (landed(2 * j + 1) && fix_tail(koff + j, vs));
           bool k_next_ready = false;
           for (int i = 0; i < 2 && ok; ++i) {
             if (j < nkt[i]) {
@@ -606,7 +667,7 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     // The MMA thread names the stage and the first row to clear, after its own
     // wait on the tile's kv_full phase, so this warp never polls a ring barrier.
     int n_tails = 0;
-    for (int g = 0; g < n_kv_tiles; ++g) n_tails += seg_left_of(g) < kBlockN ? 1 : 0;
+    for (int g = koff; g < koff + n_kv_tiles; ++g) n_tails += seg_left_of(g) < kBlockN ? 1 : 0;
     for (int t = 0; t < n_tails; ++t) {
       if (!warp_wait(&sm.fix_req, t & 1, abort_flag)) {
         if (lane == 0) give_up();
@@ -720,9 +781,11 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     const int row = wq * 32 + lane;         // == TMEM lane == row within the tile
     const int n_tiles = nkt[qi];
     // decode: this warpgroup's key tiles, counted from its first one (koff1 for
-    // warpgroup 1 of a key-split item): prefix tiles before tgt0, keys left in the prefix
-    const int tgt0 = n_pre_tiles - (qi == 1 ? koff1 : 0);
-    const int pre_left0 = n_pre - (qi == 1 ? koff1 : 0) * kBlockN;
+    // warpgroup 1 of a key-split item, koff in a balanced-tail piece): prefix tiles
+    // before tgt0, keys left in the prefix
+    const int kfirst = koff + (qi == 1 ? koff1 : 0);
+    const int tgt0 = n_pre_tiles - kfirst;
+    const int pre_left0 = n_pre - kfirst * kBlockN;
     const int row0 = q_seq0 + (m_base + (kSplit ? 0 : qi)) * kBlockM;
     const uint32_t lane_addr = tmem + (static_cast<uint32_t>(wq * 32) << 16);
     const uint32_t s_addr = lane_addr + kColS + qi * 128;
@@ -932,6 +995,27 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
       if (ok && n_tiles > 0) ok = warp_wait(&sm.o_final[qi], 0, abort_flag);
       if (!ok) {
         if (lane == 0) give_up();
+      } else if (kSeg && n_tiles > 0) {
+        // Balanced-tail piece: the row's unnormalised O (against m_ref) and its
+        // (m_ref, l) go to the partial slot; a warp's stores of one column group
+        // cover 32 consecutive rows, 512 contiguous bytes.
+        tc_fence_after();
+        float4* o_part = reinterpret_cast<float4*>(seg_slot) + qi * 32 * kBlockM + row;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld32(o_addr + c * 32, r);
+          if (row_valid) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              o_part[(c * 8 + x) * kBlockM] =
+                  make_float4(__uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                              __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+          }
+        }
+        if (row_valid)
+          reinterpret_cast<float2*>(seg_slot + kSegSlotO)[qi * kBlockM + row] =
+              make_float2(m_ref, l_run);
       } else if (n_tiles > 0) {
         tc_fence_after();
         const float inv_l = 1.f / l_run;
@@ -1014,9 +1098,10 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
 // Decode: a 1-D list of equal-cost tile pairs, the pairs of one head next to
 // each other (they stream the same K/V tiles); the pairs of a last, partly
 // filled wave become single-tile items (kSplit: two CTAs per pair, each with its
-// key range split between the two softmax warpgroups), launched as a second
-// grid that may start as soon as every pair CTA has started.
-template <bool kDecode, bool kSplit, bool kPagedAppend = false>
+// key range split between the two softmax warpgroups), or, with a workspace,
+// balanced-tail pieces (kSeg: one CTA per piece, longer pieces first), launched
+// as a second grid that may start as soon as every pair CTA has started.
+template <bool kDecode, bool kSplit, bool kPagedAppend = false, bool kSeg = false>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
@@ -1063,6 +1148,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     m_base + static_cast<int>(blockIdx.x & 1), 2);
     // do not complete before the pair grid has (work queued after the call sees both)
     grid_dependency_wait();
+  } else if constexpr (kSeg) {
+    // the merge grid launched after this one may start once every piece has
+    grid_launch_dependents();
+    // CTA i < seg_ranges: the longer part of range i; after them, the shorter
+    // parts, longest first (their ranges in seg_order)
+    const int i = blockIdx.x;
+    const int c = i < p.seg_ranges ? i : static_cast<int>(p.seg_order[i - p.seg_ranges]);
+    const int long_part = seg_long_part(c, p.seg_total, p.seg_ranges, p.seg_nkv);
+    const int part = i < p.seg_ranges ? long_part : 1 - long_part;
+    int64_t v0, v1;
+    seg_piece(c, part, p.seg_total, p.seg_ranges, p.seg_nkv, v0, v1);
+    const int t = static_cast<int>(v0 / p.seg_nkv);   // tail pair
+    const int kt0 = static_cast<int>(v0 - static_cast<int64_t>(t) * p.seg_nkv);
+    const int kt1 = static_cast<int>(v1 - static_cast<int64_t>(t) * p.seg_nkv);
+    const int item = p.decode_split_from + t;
+    const int rest = item / p.decode_pairs_per_seq;
+    if (v1 > v0 && BCA_IN_BOUNDS(p.status, c < p.seg_ranges && kt0 >= 0 && kt1 <= p.seg_nkv))
+      attn_item<true, false, false, true>(
+          tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, rest % p.num_heads, rest / p.num_heads,
+          2 * (item % p.decode_pairs_per_seq), 2, kt0, kt1,
+          p.seg_ws + static_cast<size_t>(2 * c + part) * kSegSlotFloats);
+    // do not complete before the pair grid has (work queued after the call sees both)
+    grid_dependency_wait();
   } else if constexpr (!kSplit) {
     grid_launch_dependents();
     const int L = blockIdx.x;
@@ -1079,6 +1187,120 @@ __global__ void __launch_bounds__(kThreads, 1)
     // complete before that grid has, so work queued after both sees its output.
     grid_dependency_wait();
   }
+}
+
+// Merge of the balanced decode tail: CTA (t, i, quarter) combines, for query tile
+// i of tail pair t and 32 of the 128 columns, the partial rows its pieces left in
+// the workspace (in key order), each against its own reference max, online:
+// m = max m_s, O = sum 2^(m_s - m) O_s, l = sum 2^(m_s - m) l_s; out = O / l,
+// lse = (m + log2 l) ln 2.  One thread per row; a warp's loads of one column
+// group are 32 consecutive rows, 512 contiguous bytes, and the next piece's
+// loads are in flight while the current one is added.
+constexpr int kMergeThreads = kBlockM;
+
+__global__ void __launch_bounds__(kMergeThreads)
+    seg_merge_kernel(const __grid_constant__ FwdParams p) {
+  __shared__ int s_c0, s_n, s_part0;
+  const int quarter = blockIdx.x & 3, qi = (blockIdx.x >> 2) & 1, t = blockIdx.x >> 3;
+  const int row = threadIdx.x;
+  const int item = p.decode_split_from + t;
+  const int rest = item / p.decode_pairs_per_seq;
+  const int h = rest % p.num_heads, b = rest / p.num_heads;
+  const int m = 2 * (item % p.decode_pairs_per_seq) + qi;
+  // (inputs only before the wait: nothing here is written by the pieces)
+  const int q_seq0 = p.cu_q[b];
+  const int q_len = p.cu_q[b + 1] - q_seq0;
+  if (q_seq0 < 0 || q_len < 0 || q_seq0 > p.total_q - q_len) return;   // reported by the pieces
+  const int rows_valid = min(kBlockM, q_len - m * kBlockM);
+  if (rows_valid <= 0) return;
+  const int n_pre = p.cu_prefix[b + 1] - p.cu_prefix[b];
+  const int n_all = (n_pre + kBlockN - 1) / kBlockN + (q_len + kBlockN - 1) / kBlockN;
+  if (n_all > p.seg_nkv) {
+    // more keys than max_prefix allowed for: they were planned for no piece
+    if (row == 0 && quarter == 0) report_status(p.status, BCA_ERR_SEQLENS);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    // the ranges holding this pair's key tiles [0, n_all): c0 (its part 1 when it
+    // starts in the previous pair) and the ranges after it that start before n_all
+    const int64_t lo = static_cast<int64_t>(t) * p.seg_nkv, hi = lo + n_all;
+    int c = static_cast<int>(lo * p.seg_ranges / p.seg_total);
+    while (c > 0 && seg_start(c, p.seg_total, p.seg_ranges) > lo) --c;
+    while (c + 1 < p.seg_ranges && seg_start(c + 1, p.seg_total, p.seg_ranges) <= lo) ++c;
+    int n = 1;
+    while (c + n < p.seg_ranges && seg_start(c + n, p.seg_total, p.seg_ranges) < hi) ++n;
+    s_c0 = c;
+    s_n = n;
+    s_part0 = seg_start(c, p.seg_total, p.seg_ranges) < lo ? 1 : 0;
+  }
+  // the pieces (and, through their own waits, the pair grid) have completed after this
+  grid_dependency_wait();
+  __syncthreads();
+  if (p.status != nullptr && *reinterpret_cast<volatile int32_t*>(p.status) == BCA_ERR_TIMEOUT)
+    return;
+  if (row >= rows_valid) return;
+  const int c0 = s_c0, n = s_n;
+  // piece i: slot 2 (c0 + i) + part (part 1 only for the first, when it continues a range)
+  auto slot_of = [&](int i) {
+    return p.seg_ws + static_cast<size_t>(2 * (c0 + i) + (i == 0 ? s_part0 : 0)) * kSegSlotFloats;
+  };
+  const size_t o_off = static_cast<size_t>(qi * 32 + quarter * 8) * kBlockM + row;   // float4 units
+  const size_t ml_off = static_cast<size_t>(qi * kBlockM + row);                       // float2 units
+  float4 o[8];
+  float2 ml;
+  {
+    const float* s0 = slot_of(0);
+    ml = __ldcg(reinterpret_cast<const float2*>(s0 + kSegSlotO) + ml_off);
+#pragma unroll
+    for (int g = 0; g < 8; ++g) o[g] = __ldcg(reinterpret_cast<const float4*>(s0) + o_off + g * kBlockM);
+  }
+  float acc[32];
+#pragma unroll
+  for (int x = 0; x < 32; ++x) acc[x] = 0.f;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool failed = false;
+  for (int i = 0; i < n; ++i) {
+    float4 o_next[8];
+    float2 ml_next = ml;
+    if (i + 1 < n) {
+      const float* sn = slot_of(i + 1);
+      ml_next = __ldcg(reinterpret_cast<const float2*>(sn + kSegSlotO) + ml_off);
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        o_next[g] = __ldcg(reinterpret_cast<const float4*>(sn) + o_off + g * kBlockM);
+    }
+    failed = failed || ml.y < 0.f;   // the pair failed validation (reported by its pieces)
+    const float m_new = fmaxf(m_run, ml.x);
+    const float a_old = ex2_approx(m_run - m_new), a = ex2_approx(ml.x - m_new);
+    l_run = l_run * a_old + ml.y * a;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      acc[4 * g] = acc[4 * g] * a_old + o[g].x * a;
+      acc[4 * g + 1] = acc[4 * g + 1] * a_old + o[g].y * a;
+      acc[4 * g + 2] = acc[4 * g + 2] * a_old + o[g].z * a;
+      acc[4 * g + 3] = acc[4 * g + 3] * a_old + o[g].w * a;
+    }
+    m_run = m_new;
+    if (i + 1 < n) {
+#pragma unroll
+      for (int g = 0; g < 8; ++g) o[g] = o_next[g];
+      ml = ml_next;
+    }
+  }
+  if (failed) return;
+  const float inv_l = 1.f / l_run;
+  const int r = q_seq0 + m * kBlockM + row;
+  if (!BCA_IN_BOUNDS(p.status, r >= 0 && r < p.total_q && h < p.num_heads)) return;
+  uint4* dst = reinterpret_cast<uint4*>(p.out + (static_cast<size_t>(r) * p.num_heads + h) * kHeadDim +
+                                        quarter * 32);
+#pragma unroll
+  for (int x = 0; x < 4; ++x)
+    dst[x] = make_uint4(pack_bf16x2(acc[8 * x] * inv_l, acc[8 * x + 1] * inv_l),
+                        pack_bf16x2(acc[8 * x + 2] * inv_l, acc[8 * x + 3] * inv_l),
+                        pack_bf16x2(acc[8 * x + 4] * inv_l, acc[8 * x + 5] * inv_l),
+                        pack_bf16x2(acc[8 * x + 6] * inv_l, acc[8 * x + 7] * inv_l));
+  if (quarter == 0)
+    p.lse[static_cast<size_t>(h) * p.total_q + r] = (m_run + log2f(l_run)) * 0.69314718055994530942f;
 }
 
 // ---- host side ---------------------------------------------------------------------
@@ -1127,7 +1349,88 @@ bool encode_cache(CUtensorMap* m, const void* base, int num_heads, int64_t capac
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int device_sms() {
+  static int sms = 0;
+  if (sms == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 1;
+  }
+  return sms;
+}
+
+// Balanced decode tail.  The pairs of a last, partly filled wave (all pairs when
+// there are fewer than SMs) are laid end to end, nkv key tiles each, and cut into
+// `ranges` equal ranges, one per SM: at least kMinSegTiles key tiles per range and
+// fewer pairs than ranges (so a range crosses at most one pair boundary, and a
+// piece lies inside one pair).  Only when a range plus kSegOverheadTiles is shorter
+// than what the wave costs otherwise: 0.6 of a pair's key tiles as key-split
+// single tiles (a wave at most half full), else a whole pair.  The overhead, in
+// key-tile iterations of a pair (set-up and partial rows of up to two pieces per
+// SM, and the merge), is measured: on the two-reference edit decode (56 pairs of
+// 98 tiles, 36 per range) the balanced tail saved 13 us over the key-split one,
+// on the text-to-image decode (56 pairs of 34 tiles, 12.5 per range) it lost 5 us.
+constexpr int kMinSegTiles = 8;
+constexpr int kSegOverheadTiles = 16;
+
+struct TailPlan {
+  int64_t split_from;   // first pair of the tail
+  int64_t pairs;
+  int ranges;
+  int nkv;
+  int64_t total;
+  int n_short;          // ranges that cross a pair boundary
+  uint16_t order[kMaxSegRanges];
+};
+
+bool plan_decode_tail(int64_t items, int nkv, TailPlan* tp) {
+  const int sms = device_sms();
+  if (items <= 0 || nkv <= 0) return false;
+  const int64_t pairs = items % sms;
+  if (pairs == 0) return false;
+  const int64_t total = pairs * nkv;
+  const int ranges = static_cast<int>(std::min<int64_t>(std::min(sms, kMaxSegRanges),
+                                                        total / kMinSegTiles));
+  if (ranges <= pairs) return false;
+  const double per_range = static_cast<double>(total) / ranges;
+  const double otherwise = 2 * pairs <= sms ? 0.6 * nkv : static_cast<double>(nkv);
+  if (per_range + kSegOverheadTiles >= otherwise) return false;
+  tp->split_from = items - pairs;
+  tp->pairs = pairs;
+  tp->ranges = ranges;
+  tp->nkv = nkv;
+  tp->total = total;
+  // ranges with two parts, by ascending length of the longer one: their shorter
+  // parts then launch longest first, as the SMs running the longer ones free up
+  int64_t longer[kMaxSegRanges];
+  int n = 0;
+  for (int c = 0; c < ranges; ++c) {
+    int64_t a0, a1, b0, b1;
+    seg_piece(c, 0, total, ranges, nkv, a0, a1);
+    seg_piece(c, 1, total, ranges, nkv, b0, b1);
+    if (b1 > b0) {
+      longer[c] = std::max(a1 - a0, b1 - b0);
+      tp->order[n++] = static_cast<uint16_t>(c);
+    }
+  }
+  std::stable_sort(tp->order, tp->order + n,
+                   [&](uint16_t x, uint16_t y) { return longer[x] < longer[y]; });
+  tp->n_short = n;
+  return true;
+}
+
 }  // namespace
+
+size_t decode_tail_workspace_bytes(int batch, int num_heads, int max_seqlen_q, int max_prefix) {
+  if (batch <= 0 || num_heads <= 0 || max_seqlen_q <= 0 || max_prefix < 0) return 0;
+  const int tiles = (max_seqlen_q + kBlockM - 1) / kBlockM;
+  const int64_t items = static_cast<int64_t>(num_heads) * ((tiles + 1) / 2) * batch;
+  const int nkv = (max_prefix + kBlockN - 1) / kBlockN + tiles;
+  TailPlan tp;
+  if (!plan_decode_tail(items, nkv, &tp)) return 0;
+  return static_cast<size_t>(2 * tp.ranges) * kSegSlotBytes;
+}
 
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
   CUtensorMap tq, tk, tv, tk2, tv2, to;
@@ -1214,13 +1517,7 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     // slower than a pair (two K/V streams, its own set-up), which the last wave's
     // idle SMs pay back in a short grid (text-to-image layer: 226 -> 213 us) but not
     // in a long one (two-reference edit, 10 waves: 1059 -> 1067 us).
-    static int sms = 0;
-    if (sms == 0) {
-      int dev = 0;
-      if (cudaGetDevice(&dev) != cudaSuccess ||
-          cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        sms = 1;
-    }
+    const int sms = device_sms();
     const int pairs = (a.tiles_per_seq + 1) / 2;
     const int64_t total = static_cast<int64_t>(per_group) * pairs * a.batch * groups;
     const int64_t tail = total % sms;
@@ -1261,30 +1558,41 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     const cudaError_t err = cudaGetLastError();
     return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;
   }
-  // Decode: equal-cost pair items; when the last wave would be at most half
-  // full, its pairs become key-split single-tile items (two CTAs each, about
-  // half a pair's time) in a second grid.
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      sms = 1;
-  }
+  // Decode: equal-cost pair items.  The pairs of a last, partly filled wave run
+  // as a balanced tail when the caller gave a workspace for it (pieces, then their
+  // merge); without one, when that wave would be at most half full, they become
+  // key-split single-tile items (two CTAs each, about 0.6 of a pair's time).
+  // Either runs as a second grid that may start as the pair grid drains.
+  const int sms = device_sms();
   const int pps = (a.tiles_per_seq + 1) / 2;
   const int64_t items = static_cast<int64_t>(a.num_heads) * pps * a.batch;
+  TailPlan tp;
+  const int nkv = (a.max_prefix + kBlockN - 1) / kBlockN + a.tiles_per_seq;
+  const bool balanced = a.tail_ws != nullptr && plan_decode_tail(items, nkv, &tp) &&
+                        a.tail_ws_bytes >= static_cast<size_t>(2 * tp.ranges) * kSegSlotBytes;
   const int64_t tail = items % sms;
-  const int64_t split_from = (tail > 0 && 2 * tail <= sms) ? items - tail : items;
-  const int64_t n_split = 2 * (items - split_from);
-  if (split_from > 0x7fffffff || n_split > 0x7fffffff) return BCA_ERR_UNSUPPORTED;
+  const int64_t split_from =
+      balanced ? tp.split_from : ((tail > 0 && 2 * tail <= sms) ? items - tail : items);
+  const int64_t n_second = balanced ? tp.ranges + tp.n_short : 2 * (items - split_from);
+  if (split_from > 0x7fffffff || n_second > 0x7fffffff) return BCA_ERR_UNSUPPORTED;
   p.decode_pairs_per_seq = pps;
   p.decode_split_from = static_cast<int>(split_from);
+  if (balanced) {
+    p.seg_ranges = tp.ranges;
+    p.seg_nkv = tp.nkv;
+    p.seg_total = tp.total;
+    p.seg_ws = static_cast<float*>(a.tail_ws);
+    for (int i = 0; i < tp.n_short; ++i) p.seg_order[i] = tp.order[i];
+  }
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(attn_fwd_kernel<true, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess ||
         cudaFuncSetAttribute(attn_fwd_kernel<true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmemBytes)) != cudaSuccess ||
+        cudaFuncSetAttribute(attn_fwd_kernel<true, false, false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmemBytes)) != cudaSuccess)
       return BCA_ERR_CUDA;
@@ -1295,9 +1603,9 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     attn_fwd_kernel<true, false><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, tk2, tv2, to, p);
     if (cudaGetLastError() != cudaSuccess) return BCA_ERR_CUDA;
   }
-  if (n_split > 0) {
+  if (n_second > 0) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(n_split), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(n_second), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
@@ -1306,9 +1614,19 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = split_from > 0 ? 1 : 0;
-    if (cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true, true>, tq, tk, tv, tk2, tv2, to, p) !=
-        cudaSuccess)
-      return BCA_ERR_CUDA;
+    const cudaError_t e =
+        balanced ? cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true, false, false, true>, tq, tk, tv,
+                                      tk2, tv2, to, p)
+                 : cudaLaunchKernelEx(&cfg, attn_fwd_kernel<true, true>, tq, tk, tv, tk2, tv2, to, p);
+    if (e != cudaSuccess) return BCA_ERR_CUDA;
+    if (balanced) {
+      // the merge, a programmatic dependent of the pieces
+      cfg.gridDim = dim3(static_cast<unsigned>(8 * tp.pairs), 1, 1);   // (pair, tile, quarter)
+      cfg.blockDim = dim3(kMergeThreads, 1, 1);
+      cfg.dynamicSmemBytes = 0;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, seg_merge_kernel, p) != cudaSuccess) return BCA_ERR_CUDA;
+    }
   }
   const cudaError_t err = cudaGetLastError();
   return err == cudaSuccess ? BCA_OK : BCA_ERR_CUDA;

@@ -70,9 +70,13 @@ bca_status decode_layer(const void* q_tgt, const void* k_layer, const void* v_la
                         const void* v_tgt, const int32_t* cu_seqlens_q, int32_t batch,
                         int32_t num_heads, int32_t total_q, int32_t max_seqlen_q,
                         float softmax_scale, void* out, float* lse, int32_t* status_dev,
-                        cudaStream_t stream, const int32_t* page_table = nullptr,
+                        cudaStream_t stream, int32_t max_prefix, void* tail_ws,
+                        size_t tail_ws_bytes, const int32_t* page_table = nullptr,
                         int max_pages = 0) {
   AttnLaunch a{};
+  a.tail_ws = tail_ws;
+  a.tail_ws_bytes = tail_ws_bytes;
+  a.max_prefix = max_prefix;
   a.page_table = page_table;
   a.max_pages = max_pages;
   a.q = q_tgt;
@@ -119,6 +123,30 @@ bca_status check_decode_args(const void* q_tgt, const void* cache_k, const void*
   if (num_heads > 65535 || batch > 65535 || tiles_for(max_seqlen_q) > 65535)
     return BCA_ERR_UNSUPPORTED;
   return BCA_OK;
+}
+
+// A decode workspace is optional: null (with any size) runs the key-split tail;
+// otherwise it must be 16-byte aligned and hold the balanced tail's slots.
+bca_status check_tail_workspace(const void* workspace, size_t workspace_bytes, int32_t batch,
+                                int32_t num_heads, int32_t max_seqlen_q, int32_t max_prefix) {
+  if (workspace == nullptr) return BCA_OK;
+  if (!aligned16(workspace) ||
+      workspace_bytes < decode_tail_workspace_bytes(batch, num_heads, max_seqlen_q, max_prefix))
+    return BCA_ERR_WORKSPACE;
+  return BCA_OK;
+}
+
+// The FP8 decodes' workspace: their bf16 layers first (`used` bytes), then, when
+// it has room for them, the balanced tail's slots (else the key-split tail runs).
+void* tail_after(void* workspace, size_t workspace_bytes, size_t used, int32_t batch,
+                 int32_t num_heads, int32_t max_seqlen_q, int32_t max_prefix, size_t* tail_bytes) {
+  const size_t need = decode_tail_workspace_bytes(batch, num_heads, max_seqlen_q, max_prefix);
+  *tail_bytes = 0;
+  if (need == 0 || workspace == nullptr || !aligned16(workspace) || workspace_bytes < used ||
+      workspace_bytes - used < need)
+    return nullptr;
+  *tail_bytes = workspace_bytes - used;
+  return static_cast<uint8_t*>(workspace) + used;
 }
 
 // Bytes of one layer of a bf16 cache, rounded up to 256.
@@ -329,24 +357,33 @@ bca_status bca_prefill_append_paged(const void* q, const void* k, const void* v,
                       page_table, max_pages, status_dev, stream);
 }
 
+size_t bca_prefix_decode_workspace_bytes(int32_t batch, int32_t num_heads, int32_t head_dim,
+                                         int32_t max_seqlen_q, int32_t max_prefix) {
+  if (head_dim != kHeadDim) return 0;
+  return decode_tail_workspace_bytes(batch, num_heads, max_seqlen_q, max_prefix);
+}
+
 bca_status bca_prefix_decode(const void* q_tgt, const void* cache_k, const void* cache_v,
                              int32_t layer, int32_t num_layers, int64_t capacity,
                              const int32_t* cu_prefix, const void* k_tgt, const void* v_tgt,
                              const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
                              int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
                              int32_t max_prefix, float softmax_scale, void* out, float* lse,
-                             int32_t* status_dev, void* stream) {
+                             void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                             void* stream) {
   bca_status st = check_decode_args(q_tgt, cache_k, cache_v, layer, num_layers, capacity,
                                     cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads,
                                     head_dim, total_q, max_seqlen_q, max_prefix, softmax_scale,
                                     out, lse);
   if (st != BCA_OK || batch == 0 || total_q == 0) return st;
+  st = check_tail_workspace(workspace, workspace_bytes, batch, num_heads, max_seqlen_q, max_prefix);
+  if (st != BCA_OK) return st;
   const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
   return decode_layer(q_tgt, static_cast<const __nv_bfloat16*>(cache_k) + layer * layer_elems,
                       static_cast<const __nv_bfloat16*>(cache_v) + layer * layer_elems, capacity,
                       cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads, total_q,
                       max_seqlen_q, softmax_scale, out, lse, status_dev,
-                      static_cast<cudaStream_t>(stream));
+                      static_cast<cudaStream_t>(stream), max_prefix, workspace, workspace_bytes);
 }
 
 bca_status bca_prefix_decode_paged(const void* q_tgt, const void* cache_k, const void* cache_v,
@@ -356,7 +393,8 @@ bca_status bca_prefix_decode_paged(const void* q_tgt, const void* cache_k, const
                                    const int32_t* cu_seqlens_q, int32_t batch, int32_t num_heads,
                                    int32_t head_dim, int32_t total_q, int32_t max_seqlen_q,
                                    int32_t max_prefix, float softmax_scale, void* out, float* lse,
-                                   int32_t* status_dev, void* stream) {
+                                   void* workspace, size_t workspace_bytes, int32_t* status_dev,
+                                   void* stream) {
   if (num_pages <= 0 || num_pages > (1 << 24) || max_pages < 0) return BCA_ERR_INVALID_ARG;
   const int64_t capacity = static_cast<int64_t>(num_pages) * kBlockN;
   bca_status st = check_decode_args(q_tgt, cache_k, cache_v, layer, num_layers, capacity,
@@ -365,12 +403,15 @@ bca_status bca_prefix_decode_paged(const void* q_tgt, const void* cache_k, const
                                     out, lse);
   if (st != BCA_OK || batch == 0 || total_q == 0) return st;
   if (!page_table) return BCA_ERR_INVALID_ARG;
+  st = check_tail_workspace(workspace, workspace_bytes, batch, num_heads, max_seqlen_q, max_prefix);
+  if (st != BCA_OK) return st;
   const size_t layer_elems = static_cast<size_t>(num_heads) * capacity * kHeadDim;
   return decode_layer(q_tgt, static_cast<const __nv_bfloat16*>(cache_k) + layer * layer_elems,
                       static_cast<const __nv_bfloat16*>(cache_v) + layer * layer_elems, capacity,
                       cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads, total_q,
                       max_seqlen_q, softmax_scale, out, lse, status_dev,
-                      static_cast<cudaStream_t>(stream), page_table, max_pages);
+                      static_cast<cudaStream_t>(stream), max_prefix, workspace, workspace_bytes,
+                      page_table, max_pages);
 }
 
 size_t bca_prefix_decode_fp8_workspace_bytes(int32_t mode, int32_t num_heads, int32_t head_dim,
@@ -444,9 +485,12 @@ bca_status bca_prefix_decode_fp8(const void* q_tgt, const void* cache_k, const v
       k_layer = static_cast<const __nv_bfloat16*>(cache_k) + layer * rows * kHeadDim;
     }
   }
+  size_t tail_bytes = 0;
+  void* tail = tail_after(workspace, workspace_bytes, capacity > 0 ? need : 0, batch, num_heads,
+                          max_seqlen_q, max_prefix, &tail_bytes);
   return decode_layer(q_tgt, k_layer, v_layer, capacity, cu_prefix, k_tgt, v_tgt, cu_seqlens_q,
                       batch, num_heads, total_q, max_seqlen_q, softmax_scale, out, lse,
-                      status_dev, s);
+                      status_dev, s, max_prefix, tail, tail_bytes);
 }
 
 bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* cu_seqlens_k,
@@ -587,9 +631,12 @@ bca_status bca_prefix_decode_fp8_paged(
                           batch, num_heads, capacity, v_out, prefix_rows, status_dev, s) !=
           cudaSuccess)
     return BCA_ERR_CUDA;
+  size_t tail_bytes = 0;
+  void* tail = tail_after(workspace, workspace_bytes, need, batch, num_heads, max_seqlen_q,
+                          max_prefix, &tail_bytes);
   return decode_layer(q_tgt, k_out, v_out, prefix_rows, cu_prefix, k_tgt, v_tgt, cu_seqlens_q,
                       batch, num_heads, total_q, max_seqlen_q, softmax_scale, out, lse,
-                      status_dev, s);
+                      status_dev, s, max_prefix, tail, tail_bytes);
 }
 
 bca_status bca_rope_positions(const int32_t* block_id, const int32_t* cu_seqlens, int32_t batch,

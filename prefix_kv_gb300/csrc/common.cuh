@@ -59,6 +59,19 @@ cudaError_t launch_schedule_prep(const int32_t* block_id, const int32_t* cu_q, c
                                  int32_t* row_end, PrefillTile* tiles, int32_t* status,
                                  cudaStream_t stream);
 
+// Balanced decode tail: at most this many equal key ranges (one per SM), and one
+// partial slot per piece, two per range: the unnormalised fp32 O rows of the two
+// query tiles as [tile][32 column groups of 4][128 rows][4], then (m, l) per row
+// as [tile][128 rows][2] (m in the log2 domain of the scaled scores).
+constexpr int kMaxSegRanges = 256;
+constexpr int kSegSlotO = 2 * 128 * kHeadDim;               // floats of O in a slot
+constexpr int kSegSlotFloats = kSegSlotO + 2 * 128 * 2;
+constexpr size_t kSegSlotBytes = static_cast<size_t>(kSegSlotFloats) * sizeof(float);
+
+// Workspace bytes that let a decode launch run its last, partly filled wave as a
+// balanced tail on the current device (0: this decode has no such tail).
+size_t decode_tail_workspace_bytes(int batch, int num_heads, int max_seqlen_q, int max_prefix);
+
 struct AttnLaunch {
   // tensors
   const void* q;          // [total_q, H, 128]
@@ -83,6 +96,11 @@ struct AttnLaunch {
   void* cache_k;               // prefill with cache append: layer base [H][capacity][128], else null
   void* cache_v;
   int32_t* status;
+  // decode: workspace for the balanced tail (null: the key-split tail instead) and
+  // the bound on the prefix lengths it plans with
+  void* tail_ws;
+  size_t tail_ws_bytes;
+  int max_prefix;
 };
 int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream);  // returns bca_status
 

@@ -128,12 +128,15 @@ class DecodeCase:
         return cls(q[tr].contiguous(), k[tr].contiguous(), v[tr].contiguous(),
                    k[pr].contiguous(), v[pr].contiguous(), wl.cu_target(), wl.cu_prefix(), **kw)
 
-    def run(self, status=None):
+    def run(self, status=None, balanced_tail=True, workspace=None, max_pre=None, out=None,
+            lse=None):
         d = lambda t: t.to(DEV)
         ti = lambda a: torch.from_numpy(a).to(DEV)
         return bca.prefix_decode(d(self.q_tgt), d(self.cache_k), d(self.cache_v), self.layer,
                                  ti(self.cu_pre), d(self.k_tgt), d(self.v_tgt), ti(self.cu_q),
-                                 self.max_q, self.max_pre, SCALE, status=status)
+                                 self.max_q, self.max_pre if max_pre is None else max_pre, SCALE,
+                                 status=status, balanced_tail=balanced_tail, workspace=workspace,
+                                 out=out, lse=lse)
 
     def reference(self, rows=None, heads=None):
         return oracle.prefix_decode(self.q_tgt, self.k_pre, self.v_pre, self.cu_pre, self.k_tgt,

@@ -143,12 +143,26 @@ def test_prefill_append_paged_host_validation(lib):
 
 def test_decode_and_append_host_validation(lib):
     dec = lib.bca_prefix_decode
-    #         q   ck  cv  layer L  cap  cup tk  tv  cq  B  H  D    tq mq mp scale out lse st  s
-    assert dec(16, 16, 16, 0, 1, 64, 16, 16, 16, 16, 1, 2, 96, 8, 8, 8, 0.1, 16, 16, None, None) == 2
-    assert dec(16, 16, 16, 1, 1, 64, 16, 16, 16, 16, 1, 2, 128, 8, 8, 8, 0.1, 16, 16, None, None) == 1
-    assert dec(16, 16, 16, 0, 1, 64, 16, 16, 16, 16, 1, 2, 128, 8, 8, 8, -1.0, 16, 16, None, None) == 1
-    assert dec(16, 16, 16, 0, 1, 64, 16, 16, 16, 16, 1, 2, 128, 0, 8, 8, 0.1, 16, 16, None, None) == 0
-    assert dec(16, 8, 16, 0, 1, 64, 16, 16, 16, 16, 1, 2, 128, 8, 8, 8, 0.1, 16, 16, None, None) == 1
+    #         q   ck  cv  layer L  cap  cup tk  tv  cq  B  H  D    tq mq mp scale out lse ws wsb st s
+    args = [16, 16, 16, 0, 1, 64, 16, 16, 16, 16, 1, 2, 128, 8, 8, 8, 0.1, 16, 16, None, 0, None,
+            None]
+
+    def call(**kw):
+        a = list(args)
+        for name, val in kw.items():
+            a[{"layer": 3, "ck": 1, "D": 12, "tq": 13, "scale": 16, "ws": 19, "wsb": 20}[name]] = val
+        return dec(*a)
+
+    assert call(D=96) == 2
+    assert call(layer=1) == 1
+    assert call(scale=-1.0) == 1
+    assert call(tq=0) == 0
+    assert call(ck=8) == 1
+    assert call(ws=24, wsb=1 << 20) == 4            # a misaligned workspace
+    wsb = lib.bca_prefix_decode_workspace_bytes
+    #          B  H  D    mq    mp
+    assert wsb(1, 2, 64, 1000, 1000) == 0            # head_dim other than 128
+    assert wsb(0, 2, 128, 1000, 1000) == 0 and wsb(1, 2, 128, 0, 1000) == 0
     app = lib.bca_prefix_cache_append
     #          k   v  ck  cp  B  H  D    tk ck  cv  layer L cap st  s
     assert app(16, 16, 16, 16, 1, 2, 64, 8, 16, 16, 0, 1, 64, None, None) == 2
@@ -245,13 +259,15 @@ def test_paged_entry_points_host_validation(lib):
     assert app(16, 16, 16, 16, None, 2, 1, 2, 128, 8, 16, 16, 0, 1, 4, None, None) == 1
     assert app(16, 16, 16, 16, 16, 2, 1, 2, 64, 8, 16, 16, 0, 1, 4, None, None) == 2
     dec = lib.bca_prefix_decode_paged
-    # q ck cv layer L npages cp pt maxp tk tv cq B H D tq mq mp scale out lse st s
-    args = [16, 16, 16, 0, 1, 4, 16, 16, 2, 16, 16, 16, 1, 2, 128, 8, 8, 8, 0.1, 16, 16, None,
-            None]
+    # q ck cv layer L npages cp pt maxp tk tv cq B H D tq mq mp scale out lse ws wsb st s
+    args = [16, 16, 16, 0, 1, 4, 16, 16, 2, 16, 16, 16, 1, 2, 128, 8, 8, 8, 0.1, 16, 16, None, 0,
+            None, None]
     no_pages = list(args); no_pages[5] = 0
     assert dec(*no_pages) == 1
     no_table = list(args); no_table[7] = None
     assert dec(*no_table) == 1
+    odd_ws = list(args); odd_ws[21] = 40; odd_ws[22] = 1 << 20
+    assert dec(*odd_ws) == 4
     cp = lib.bca_pool_copy_rows
     # ck cv layer L H npages src dst rows s
     assert cp(16, 16, 0, 1, 2, 4, 1, 1, 10, None) == 0   # same page: nothing to do

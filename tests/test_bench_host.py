@@ -40,6 +40,13 @@ def test_decode_grid_count_follows_the_tail_rule():
     assert bench.decode_grids(8, 1024, 19, 152) == 1       # 608 pairs: 4 whole waves
     assert bench.decode_grids(8, 1000, 5, 152) == 2        # 160 pairs: 8 left over
     assert bench.decode_grids(1, 0, 1, 152) == 0           # nothing to launch
+    # with a workspace: the balanced tail's pieces and merge behind the pair grid when a
+    # range (plus 16 key tiles of overhead) is shorter than the tail's cost otherwise
+    assert bench.decode_grids(32, 4096, 1, 152, 8384) == 3  # 56 pairs of 98 key tiles: 36 + 16 < 58.8
+    assert bench.decode_grids(32, 4096, 1, 152, 256) == 2   # T2I, 34 key tiles: 12.5 + 16 > 20.4
+    assert bench.decode_grids(4, 1000, 1, 152, 6000) == 2   # 16 pairs, all in the tail
+    assert bench.decode_grids(4, 1000, 1, 152, 1100) == 1   # 17 key tiles per pair: key-split
+    assert bench.decode_grids(32, 16384, 2, 152, 16968) == 1  # 144 pairs of 261: 247 + 16 > 261
 
 
 def test_prefill_grid_count_follows_the_split_rule():

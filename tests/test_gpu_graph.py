@@ -2,7 +2,8 @@
 into a CUDA graph and replayed: the replay's outputs, LSE and cache rows are
 bit-identical to the eager calls'.  Every kernel launches on the caller's stream; the
 prefill's attention grid (a programmatic dependent of the schedule prep), its key-split
-grid and the decode's key-split tail grid are captured as programmatic edges."""
+grid and the decode's balanced-tail grids (the pieces, then their merge) are captured as
+programmatic edges."""
 import pytest
 import torch
 
@@ -37,13 +38,16 @@ def test_step_captured_in_a_cuda_graph(wl):
     lse = torch.empty((H, S), dtype=torch.float32, device=DEV)
     dlse = torch.empty((H, N), dtype=torch.float32, device=DEV)
     ws = torch.empty(bca.prefill_workspace_bytes(1, S, S), dtype=torch.uint8, device=DEV)
+    dws = torch.empty(bca.prefix_decode_workspace_bytes(1, H, N, P), dtype=torch.uint8,
+                      device=DEV)
     st = bca.new_status(DEV)
     results = (out, lse, dout, dlse, ck, cv)
 
     def step():
         bca.prefill_append(q, k, v, bid, cu, cu, S, S, cup, ck, cv, 0, out=out, lse=lse,
                            workspace=ws, status=st)
-        bca.prefix_decode(qt, ck, cv, 0, cup, kt, vt, cut, N, P, out=dout, lse=dlse, status=st)
+        bca.prefix_decode(qt, ck, cv, 0, cup, kt, vt, cut, N, P, out=dout, lse=dlse, status=st,
+                          workspace=dws)
 
     step()
     torch.cuda.synchronize()

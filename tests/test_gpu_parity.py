@@ -434,7 +434,7 @@ def test_decode_rejects_query_offsets_past_total_q():
     code = lib.bca_prefix_decode(q.data_ptr(), ck.data_ptr(), cv.data_ptr(), 0, 1, 2 * P,
                                  cu_p.data_ptr(), kt.data_ptr(), vt.data_ptr(), cu_q.data_ptr(),
                                  2, H, 128, total_q, 200, P, SCALE, out_buf.data_ptr(),
-                                 lse_buf.data_ptr(), st.data_ptr(),
+                                 lse_buf.data_ptr(), None, 0, st.data_ptr(),
                                  torch.cuda.current_stream().cuda_stream)
     assert code == 0
     assert bca.read_status(st) == 8
