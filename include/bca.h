@@ -328,7 +328,8 @@ bca_status bca_prefix_cache_append(const void* k, const void* v, const int32_t* 
  *               bca_prefix_cache_append), cache_v holds E4M3 codes
  *               uint8 [L][H][cap][128], scale_v fp32 [L][H][cap]; scale_k unused.
  *   BCA_FP8_KV: cache_k and cache_v hold E4M3 codes, scale_k and scale_v fp32.
- * Addressing, validation and errors are those of bca_prefix_cache_append. */
+ * Addressing, validation and errors are those of bca_prefix_cache_append; a layer
+ * of H x capacity >= 2^31 rows is BCA_ERR_UNSUPPORTED. */
 enum { BCA_FP8_V = 1, BCA_FP8_KV = 2 };
 
 bca_status bca_prefix_cache_append_fp8(const void* k, const void* v, const int32_t* cu_seqlens_k,
@@ -347,7 +348,8 @@ bca_status bca_prefix_cache_append_fp8(const void* k, const void* v, const int32
  * layer (rows outside the range are not written).  cu_prefix: device int32
  * [batch+1].  When cu_prefix[batch] > capacity (BCA_ERR_CAPACITY) or the range
  * is negative (BCA_ERR_SEQLENS) nothing is written.  Pointers 16-byte aligned
- * (scales 4-byte). */
+ * (scales 4-byte).  More than 65535 heads or a capacity of 2^28 tokens or more
+ * is BCA_ERR_UNSUPPORTED. */
 bca_status bca_prefix_cache_dequant_fp8(const void* codes, const float* scales,
                                         const int32_t* cu_prefix, int32_t batch,
                                         int32_t num_heads, int32_t head_dim, int32_t layer,
@@ -491,7 +493,8 @@ size_t bca_prefix_decode_fp8_paged_workspace_bytes(int32_t num_heads, int32_t he
  * dequantised to bf16(fp32(value(code)) * scale), a bf16 K (BCA_FP8_V mode) is
  * copied.  Then the contiguous bf16 decode runs on the gathered rows.
  * prefix_rows >= cu_prefix[batch] bounds the gathered rows (a larger
- * cu_prefix[batch] is BCA_ERR_CAPACITY on the status word).  Workspace bytes
+ * cu_prefix[batch] is BCA_ERR_CAPACITY on the status word; prefix_rows >= 2^28
+ * is BCA_ERR_UNSUPPORTED).  Workspace bytes
  * beyond bca_prefix_decode_fp8_paged_workspace_bytes serve the balanced tail as
  * in bca_prefix_decode_fp8.  Other arguments as in bca_prefix_decode_paged and
  * bca_prefix_decode_fp8. */

@@ -176,6 +176,7 @@ bca_status append_fp8_impl(const void* k, const void* v, const int32_t* cu_seqle
       (reinterpret_cast<uintptr_t>(scale_v) & 3u) || (reinterpret_cast<uintptr_t>(scale_k) & 3u))
     return BCA_ERR_INVALID_ARG;
   const size_t rows = static_cast<size_t>(num_heads) * capacity;   // per layer
+  if (rows > 0x7fffffffu) return BCA_ERR_UNSUPPORTED;   // (head, token) rows are 32-bit indices
   const size_t k_bytes = quant_k ? 1 : 2;
   cudaError_t e = launch_cache_append_fp8(
       k, v, cu_seqlens_k, cu_prefix, batch, num_heads, total_k, quant_k,
@@ -432,6 +433,8 @@ bca_status bca_prefix_cache_dequant_fp8(const void* codes, const float* scales,
       layer >= num_layers)
     return BCA_ERR_INVALID_ARG;
   if (batch == 0 || capacity == 0) return BCA_OK;
+  // (heads are a grid dimension; 16 chunks per row index a head's rows in 32 bits)
+  if (num_heads > 65535 || capacity >= (int64_t{1} << 28)) return BCA_ERR_UNSUPPORTED;
   if (!codes || !scales || !cu_prefix || !out) return BCA_ERR_INVALID_ARG;
   if (!aligned16(codes) || !aligned16(out) || (reinterpret_cast<uintptr_t>(scales) & 3u))
     return BCA_ERR_INVALID_ARG;
@@ -603,6 +606,7 @@ bca_status bca_prefix_decode_fp8_paged(
   if (mode != BCA_FP8_V && mode != BCA_FP8_KV) return BCA_ERR_INVALID_ARG;
   if (num_pages <= 0 || num_pages > (1 << 24) || max_pages < 0 || prefix_rows < 0)
     return BCA_ERR_INVALID_ARG;
+  if (prefix_rows >= (int64_t{1} << 28)) return BCA_ERR_UNSUPPORTED;
   const int64_t capacity = static_cast<int64_t>(num_pages) * kBlockN;
   bca_status st = check_decode_args(q_tgt, cache_k, cache_v, layer, num_layers, capacity,
                                     cu_prefix, k_tgt, v_tgt, cu_seqlens_q, batch, num_heads,

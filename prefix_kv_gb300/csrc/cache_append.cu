@@ -19,6 +19,8 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 
+#include <algorithm>
+
 namespace bca {
 namespace {
 
@@ -260,17 +262,21 @@ __global__ void __launch_bounds__(256)
     return;
   }
   const int p0 = cu_prefix[0];
-  const int64_t rows = static_cast<int64_t>(cu_prefix[batch] - p0) * num_heads;
-  const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+  // (token, head) rows of the prefix region: at most capacity x heads < 2^31 (host check),
+  // so the row arithmetic is 32-bit (a 64-bit division per row had made the kernel
+  // bound by its instruction issue)
+  const uint32_t rows = static_cast<uint32_t>(cu_prefix[batch] - p0) * static_cast<uint32_t>(num_heads);
+  const uint32_t warps = gridDim.x * (blockDim.x >> 5);
   const int lane16 = threadIdx.x & 15;
   // Row (token, head) of the prefix region -> source vector and cache row.
   struct Where {
     int64_t src, dst_row;
     bool in;   // source token and cache row inside their buffers (bounds-checked build)
   };
-  auto locate = [&](int64_t row) {
-    const int c = static_cast<int>(row / num_heads) + p0;       // cache token
-    const int hh = static_cast<int>(row % num_heads);
+  auto locate = [&](uint32_t row) {
+    const uint32_t c_rel = row / static_cast<uint32_t>(num_heads);
+    const int c = static_cast<int>(c_rel) + p0;                  // cache token
+    const int hh = static_cast<int>(row - c_rel * static_cast<uint32_t>(num_heads));
     int lo = 0, hi = batch - 1;                                  // sequence of c
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -287,14 +293,14 @@ __global__ void __launch_bounds__(256)
   // and two such row pairs per pass, with all four loads issued before any
   // quantisation so that each lane keeps them in flight together.
   constexpr int kPairs = 2;
-  for (int64_t r2 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-       r2 * 2 < rows; r2 += kPairs * warps) {
+  for (uint32_t r2 = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; r2 * 2 < rows;
+       r2 += kPairs * warps) {
     bool live[kPairs];
     int64_t src[kPairs], dst_row[kPairs];
     uint4 vraw[kPairs], kraw[kPairs];
 #pragma unroll
     for (int u = 0; u < kPairs; ++u) {
-      const int64_t row = (r2 + u * warps) * 2 + ((threadIdx.x >> 4) & 1);
+      const uint32_t row = (r2 + u * warps) * 2 + ((threadIdx.x >> 4) & 1);
       live[u] = row < rows;
       const Where w = locate(live[u] ? row : rows - 1);
       if (!w.in) {   // skip the row (bounds-checked build); the lanes stay together
@@ -370,13 +376,32 @@ cudaError_t launch_cache_append_fp8(const void* k, const void* v, const int32_t*
 // Expansion of the E4M3 cache back to bf16 for attention: every element of
 // the stored prefix rows becomes bf16(fp32(value(code)) * scale), the
 // dequantised value of the append's format, written in the bf16 cache layout.
-// HBM-bound: a row is 128 code bytes plus one scale in, 256 bytes out; eight
-// threads share a row, 16 codes each (one 16-byte load, two 16-byte stores).
+// HBM-bound: a row is 128 code bytes plus one scale in, 256 bytes out.  Sixteen
+// threads share a row, 8 codes each, so a warp's 8-byte loads read 256 and its
+// 16-byte stores write 512 contiguous bytes; each thread loads kDequantUnroll
+// such chunks (a grid stride apart) before expanding any.
 namespace bca {
 namespace {
 
+constexpr int kDequantUnroll = 4;
+
+// 8 E4M3 codes (the low byte first) times `scale`, rounded to 8 bf16 values.
+__device__ __forceinline__ uint4 dequant8(uint2 raw, float scale) {
+  const uint32_t w[2] = {raw.x, raw.y};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(w[q] >> (16 * hb)));
+      o[2 * q + hb] = pack_bf16x2(f.x * scale, f.y * scale);
+    }
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 __global__ void __launch_bounds__(256)
-    cache_dequant_fp8_kernel(const uint4* __restrict__ codes, const float* __restrict__ scales,
+    cache_dequant_fp8_kernel(const uint2* __restrict__ codes, const float* __restrict__ scales,
                              const int32_t* __restrict__ cu_prefix, int batch, int num_heads,
                              int64_t capacity, uint4* __restrict__ out, int32_t* status) {
   const int p0 = cu_prefix[0], p1 = cu_prefix[batch];
@@ -385,32 +410,31 @@ __global__ void __launch_bounds__(256)
       report_status(status, p1 > capacity ? BCA_ERR_CAPACITY : BCA_ERR_SEQLENS);
     return;
   }
-  const int64_t tokens = p1 - p0;
-  const int64_t chunks = tokens * num_heads * 8;        // 16-code chunks to expand
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
-       c += stride) {
-    const int64_t row_in = c >> 3;                       // (head, token) row among the prefix rows
-    const int hh = static_cast<int>(row_in / tokens);
-    const int64_t row = static_cast<int64_t>(hh) * capacity + p0 + (row_in - hh * tokens);
-    const int x = static_cast<int>(c & 7);
-    if (!BCA_IN_BOUNDS(status, hh < num_heads && row >= 0 &&
-                                   row < static_cast<int64_t>(num_heads) * capacity))
-      continue;
-    const uint4 raw = __ldcs(codes + row * 8 + x);
-    const float sc = __ldg(scales + row);
-    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-    uint32_t o[8];
+  // a grid of (chunk range, head): head h's prefix rows are contiguous, rows
+  // h * capacity + p0 .. h * capacity + p1 - 1, 16 chunks of 8 codes each
+  const int hh = blockIdx.y;
+  const int64_t row0 = static_cast<int64_t>(hh) * capacity + p0;
+  const uint32_t chunks = static_cast<uint32_t>(p1 - p0) * 16u;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < chunks;
+       base += stride * kDequantUnroll) {
+    uint2 raw[kDequantUnroll];
+    float sc[kDequantUnroll];
+    int64_t at[kDequantUnroll];   // chunk index in the layer, -1: none
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-#pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(w[q] >> (16 * hb)));
-        o[2 * q + hb] = pack_bf16x2(f.x * sc, f.y * sc);
+    for (int u = 0; u < kDequantUnroll; ++u) {
+      const uint32_t c = base + u * stride;
+      at[u] = -1;
+      if (c < chunks && BCA_IN_BOUNDS(status, hh < num_heads)) {
+        const int64_t row = row0 + (c >> 4);
+        at[u] = row * 16 + (c & 15);
+        raw[u] = __ldcs(codes + at[u]);
+        sc[u] = __ldg(scales + row);
       }
     }
-    out[row * 16 + 2 * x] = make_uint4(o[0], o[1], o[2], o[3]);
-    out[row * 16 + 2 * x + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+    for (int u = 0; u < kDequantUnroll; ++u)
+      if (at[u] >= 0) out[at[u]] = dequant8(raw[u], sc[u]);
   }
 }
 
@@ -423,8 +447,10 @@ cudaError_t launch_cache_dequant_fp8(const void* codes_layer, const float* scale
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  cache_dequant_fp8_kernel<<<sms * 8, 256, 0, stream>>>(
-      static_cast<const uint4*>(codes_layer), scales_layer, cu_prefix, batch, num_heads, capacity,
+  // about one wave of 8 CTAs per SM over all heads
+  const int per_head = std::max(1, (sms * 8 + num_heads - 1) / num_heads);
+  cache_dequant_fp8_kernel<<<dim3(per_head, num_heads), 256, 0, stream>>>(
+      static_cast<const uint2*>(codes_layer), scales_layer, cu_prefix, batch, num_heads, capacity,
       static_cast<uint4*>(out_layer), status);
   return cudaGetLastError();
 }
@@ -457,50 +483,54 @@ __global__ void __launch_bounds__(256)
   if (check_pages(page_table, max_pages, cu_prefix, batch, capacity) != 0) s_bad = BCA_ERR_CAPACITY;
   __syncthreads();
   if (s_bad != 0) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) report_status(status, s_bad);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) report_status(status, s_bad);
     return;
   }
+  // a grid of (chunk range, head); 16 chunks of 8 values per row, as in the expansion
+  const int hh = blockIdx.y;
   const int p0 = cu_prefix[0];
-  const int64_t tokens = cu_prefix[batch] - p0;
-  const int64_t chunks = tokens * num_heads * 8;         // 16-value chunks (32 bf16 bytes out)
-  for (int64_t ch = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; ch < chunks;
-       ch += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t row_in = ch >> 3;
-    const int hh = static_cast<int>(row_in / tokens);
-    const int c = static_cast<int>(row_in - hh * tokens) + p0;   // packed prefix row
-    int lo = 0, hi = batch - 1;                                   // its sequence
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (cu_prefix[mid] <= c) lo = mid; else hi = mid - 1;
-    }
-    const int64_t src_row =
-        static_cast<int64_t>(hh) * capacity + cache_token(page_table, max_pages, cu_prefix, lo,
-                                                          c - cu_prefix[lo]);
-    const int64_t dst_row = static_cast<int64_t>(hh) * out_rows + c;
-    const int x = static_cast<int>(ch & 7);
-    if (!BCA_IN_BOUNDS(status, hh < num_heads && src_row >= 0 &&
-                                   src_row < static_cast<int64_t>(num_heads) * capacity &&
-                                   c >= 0 && c < out_rows))
-      continue;
-    if constexpr (kFp8) {
-      const uint4 raw = __ldcs(static_cast<const uint4*>(src) + src_row * 8 + x);
-      const float sc = __ldg(scales + src_row);
-      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t o[8];
+  const uint32_t chunks = static_cast<uint32_t>(cu_prefix[batch] - p0) * 16u;
+  const uint32_t stride = gridDim.x * blockDim.x;
+  for (uint32_t base = blockIdx.x * blockDim.x + threadIdx.x; base < chunks;
+       base += stride * kDequantUnroll) {
+    int64_t src_at[kDequantUnroll], dst_at[kDequantUnroll];   // -1: none
+    uint2 raw8[kDequantUnroll];
+    uint4 raw16[kDequantUnroll];
+    float sc[kDequantUnroll];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-#pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          const float2 f = e4m3x2_to_float2(static_cast<uint16_t>(w[q] >> (16 * hb)));
-          o[2 * q + hb] = pack_bf16x2(f.x * sc, f.y * sc);
-        }
+    for (int u = 0; u < kDequantUnroll; ++u) {
+      const uint32_t ch = base + u * stride;
+      dst_at[u] = -1;
+      if (ch >= chunks) continue;
+      const int c = static_cast<int>(ch >> 4) + p0;   // packed prefix row
+      int lo = 0, hi = batch - 1;                       // its sequence
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cu_prefix[mid] <= c) lo = mid; else hi = mid - 1;
       }
-      out[dst_row * 16 + 2 * x] = make_uint4(o[0], o[1], o[2], o[3]);
-      out[dst_row * 16 + 2 * x + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-    } else {
-      const uint4* s4 = static_cast<const uint4*>(src);
-      out[dst_row * 16 + 2 * x] = __ldcs(s4 + src_row * 16 + 2 * x);
-      out[dst_row * 16 + 2 * x + 1] = __ldcs(s4 + src_row * 16 + 2 * x + 1);
+      const int64_t src_row = static_cast<int64_t>(hh) * capacity +
+                              cache_token(page_table, max_pages, cu_prefix, lo, c - cu_prefix[lo]);
+      if (!BCA_IN_BOUNDS(status, hh < num_heads && src_row >= 0 &&
+                                     src_row < static_cast<int64_t>(num_heads) * capacity &&
+                                     c >= 0 && c < out_rows))
+        continue;
+      const int x = static_cast<int>(ch & 15);
+      src_at[u] = src_row * 16 + x;
+      dst_at[u] = (static_cast<int64_t>(hh) * out_rows + c) * 16 + x;
+      if constexpr (kFp8) {
+        raw8[u] = __ldcs(static_cast<const uint2*>(src) + src_at[u]);
+        sc[u] = __ldg(scales + src_row);
+      } else {
+        raw16[u] = __ldcs(static_cast<const uint4*>(src) + src_at[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kDequantUnroll; ++u) {
+      if (dst_at[u] < 0) continue;
+      if constexpr (kFp8)
+        out[dst_at[u]] = dequant8(raw8[u], sc[u]);
+      else
+        out[dst_at[u]] = raw16[u];
     }
   }
 }
@@ -514,12 +544,13 @@ cudaError_t launch_cache_gather(bool fp8, const void* src_layer, const float* sc
   int dev = 0, sms = 152;
   if (cudaGetDevice(&dev) == cudaSuccess)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const dim3 grid(std::max(1, (sms * 8 + num_heads - 1) / num_heads), num_heads);
   if (fp8)
-    cache_gather_kernel<true><<<sms * 8, 256, 0, stream>>>(
+    cache_gather_kernel<true><<<grid, 256, 0, stream>>>(
         src_layer, scales_layer, cu_prefix, page_table, max_pages, batch, num_heads, capacity,
         static_cast<uint4*>(out), out_rows, status);
   else
-    cache_gather_kernel<false><<<sms * 8, 256, 0, stream>>>(
+    cache_gather_kernel<false><<<grid, 256, 0, stream>>>(
         src_layer, scales_layer, cu_prefix, page_table, max_pages, batch, num_heads, capacity,
         static_cast<uint4*>(out), out_rows, status);
   return cudaGetLastError();
