@@ -10,7 +10,8 @@ library's result (the checks change no arithmetic).  The shapes are the ragged
 ones where partial tiles are written: sequence lengths 1, 127, 129 and 1537,
 queries shorter than keys, a prefix that ends inside a tile, an empty prefix,
 paged tables whose last page is partly used, and prefill and decode grids large
-enough to run both the tile-pair grid and the key-split grid.
+enough to run both the tile-pair grid and the key-split grid, or the decode's
+balanced tail (its pieces and their merge).
 """
 import math
 
@@ -169,11 +170,14 @@ def test_bounds_prefill_key_split_tail():
 
 # ---------------------------------------------------------------- decode
 
-@pytest.mark.parametrize("pre,tgt,H", [
-    ([0, 27, 300], [1, 127, 129], 3),     # empty prefix, prefix ending mid-tile, 1-row target
-    ([8384], [1200], 32),                 # 160 tile pairs: the pair grid and the key-split tail
+@pytest.mark.parametrize("pre,tgt,H,balanced", [
+    ([0, 27, 300], [1, 127, 129], 3, True),   # empty prefix, prefix ending mid-tile, 1-row target
+    # 160 tile pairs: the pair grid, then 8 pairs of 76 key tiles as the balanced tail
+    # (pieces and merge) or, without a workspace, as key-split tiles
+    ([8384], [1200], 32, True),
+    ([8384], [1200], 32, False),
 ])
-def test_bounds_decode(pre, tgt, H):
+def test_bounds_decode(pre, tgt, H, balanced):
     kp = W.randn_bf16((sum(pre), H, 128), 211)
     vp = W.randn_bf16((sum(pre), H, 128), 212)
     qt = W.randn_bf16((sum(tgt), H, 128), 213)
@@ -182,7 +186,7 @@ def test_bounds_decode(pre, tgt, H):
     cq = np.concatenate([[0], np.cumsum(tgt)])
     cp = np.concatenate([[0], np.cumsum(pre)])
     case = DecodeCase(qt, kt, vt, kp, vp, cq, cp, layers=2, layer=1, cache_fill=float("nan"))
-    rel, dbg = _both(lambda st: case.run(status=st))
+    rel, dbg = _both(lambda st: case.run(status=st, balanced_tail=balanced))
     _same(rel, dbg)
     rows = None
     if sum(tgt) > 600:   # sampled rows: the tile edges and the last tile
