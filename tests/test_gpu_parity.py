@@ -382,7 +382,8 @@ def test_decode_pair_grid_and_tail_ragged():
     assert_close(out, lse, *case.reference(), what="pairs+tail")
 
 
-# heads 28-31 hold the last 56 tile pairs, which run as the key-split tail grid
+# heads 28-31 hold the last 56 tile pairs, the decode's last partial wave: the balanced
+# tail's pieces and merge on the edit workload, key-split tiles on text-to-image
 @pytest.mark.parametrize("wl,heads", [(W.t2i_1024(), [1, 30]), (W.edit_two_ref(), [2, 17, 31])],
                          ids=lambda x: getattr(x, "name", ""))
 def test_decode_full_size(wl, heads):
