@@ -22,8 +22,8 @@
 // one pair and go on in the next; then it is two pieces).  Every piece runs as
 // a pair item over its key tiles and leaves its unnormalised rows, reference
 // max and row sum in the workspace; a merge grid combines the pieces of each
-// pair.  The longer pieces launch first and the shorter ones after them, in
-// the order in which the SMs holding their range's other piece free up.
+// pair.  The longer pieces launch first and the shorter ones after them,
+// longest first.
 // The reference max is taken exactly on the first K tile; afterwards P is
 // formed against it directly and the max is only recomputed (with O and l
 // rescaled) for a tile whose row sum would exceed 2^16.  O and l share the
@@ -1402,7 +1402,9 @@ bool plan_decode_tail(int64_t items, int nkv, TailPlan* tp) {
   tp->nkv = nkv;
   tp->total = total;
   // ranges with two parts, by ascending length of the longer one: their shorter
-  // parts then launch longest first, as the SMs running the longer ones free up
+  // parts then launch longest first, after every longer part (an SM whose longer
+  // part was short frees first; the hardware need not give it that range's other
+  // part, and a per-CTA timeline showed it mostly does not, at little cost)
   int64_t longer[kMaxSegRanges];
   int n = 0;
   for (int c = 0; c < ranges; ++c) {
