@@ -158,3 +158,84 @@ def test_workspace_too_small_is_rejected():
     with pytest.raises(_native.BcaError) as e:
         case.run(workspace=ws)
     assert e.value.code == 4                             # BCA_ERR_WORKSPACE
+
+
+# ------------------------------------------------ the paged and FP8 decodes use it too
+
+def _ti(a):
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(a, dtype=np.int32))).to(DEV)
+
+
+def test_balanced_tail_paged_ragged():
+    """Paged decode of the ragged batch through a shuffled page table over a pool 1.5x the
+    prefix pages: against the oracle, and bit-identical to the contiguous decode (the
+    pieces read the same rows in the same order)."""
+    seed, H, pre, tgt = CASES["ragged"]
+    case = _case(seed, H, pre, tgt)
+    if _tail_bytes(case) == 0:
+        pytest.skip("no balanced tail for this shape on this device")
+    need = [(p + 127) // 128 for p in pre]
+    n_pages = sum(need) + sum(need) // 2
+    perm = np.random.default_rng(seed).permutation(n_pages).astype(np.int32)
+    pt = np.full((len(pre), max(need)), -1, np.int32)
+    at = 0
+    for b, n in enumerate(need):
+        pt[b, :n] = perm[at:at + n]
+        at += n
+    ck = torch.full((2, H, n_pages * 128, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+    cv = torch.full_like(ck, float("nan"))
+    st = bca.new_status(DEV)
+    bca.prefix_cache_append_paged(case.k_pre.to(DEV), case.v_pre.to(DEV), _ti(case.cu_pre),
+                                  _ti(case.cu_pre), _ti(pt), ck, cv, 1, status=st)
+    out, lse = bca.prefix_decode_paged(case.q_tgt.to(DEV), ck, cv, 1, _ti(case.cu_pre), _ti(pt),
+                                       case.k_tgt.to(DEV), case.v_tgt.to(DEV), _ti(case.cu_q),
+                                       case.max_q, case.max_pre, status=st)
+    assert bca.read_status(st) == 0
+    assert_close(out, lse, *case.reference(), what="paged balanced tail")
+    out_c, lse_c = case.run(status=st)
+    assert bca.read_status(st) == 0
+    assert torch.equal(out.view(torch.int16), out_c.view(torch.int16))
+    assert torch.equal(lse.view(torch.int32), lse_c.view(torch.int32))
+
+
+@pytest.mark.parametrize("mode", ["v", "kv"])
+def test_balanced_tail_fp8_ragged(mode):
+    """FP8 decode of the ragged batch, the tail's slots after the expanded layers in the
+    workspace: against the oracle over the dequantised cache, and against the FP8 decode
+    that runs the key-split tail (a workspace without room for the slots)."""
+    from oracle import fp8 as ofp8
+    import oracle
+    seed, H, pre, tgt = CASES["ragged"]
+    case = _case(seed, H, pre, tgt)
+    if _tail_bytes(case) == 0:
+        pytest.skip("no balanced tail for this shape on this device")
+    cap = int(case.cu_pre[-1]) + 64
+    kdt = torch.uint8 if mode == "kv" else torch.bfloat16
+    ck = torch.zeros((1, H, cap, 128), dtype=kdt, device=DEV)
+    cv = torch.zeros((1, H, cap, 128), dtype=torch.uint8, device=DEV)
+    sk = torch.zeros((1, H, cap), dtype=torch.float32, device=DEV)
+    sv = torch.zeros_like(sk)
+    st = bca.new_status(DEV)
+    cp, cq = _ti(case.cu_pre), _ti(case.cu_q)
+    bca.prefix_cache_append_fp8(case.k_pre.to(DEV), case.v_pre.to(DEV), cp, cp, ck, cv,
+                                sk if mode == "kv" else None, sv, 0, mode=mode, status=st)
+    qt, kt, vt = case.q_tgt.to(DEV), case.k_tgt.to(DEV), case.v_tgt.to(DEV)
+    args = (qt, ck, cv, sk if mode == "kv" else None, sv, 0, cp, kt, vt, cq, case.max_q,
+            case.max_pre)
+    out, lse = bca.prefix_decode_fp8(*args, mode=mode, status=st)
+    assert bca.read_status(st) == 0
+    vc, vs = ofp8.quantize_rows(case.v_pre)
+    vh = torch.from_numpy(ofp8.dequantize_rows(vc, vs)).to(torch.bfloat16)
+    if mode == "kv":
+        kc, ks = ofp8.quantize_rows(case.k_pre)
+        kh = torch.from_numpy(ofp8.dequantize_rows(kc, ks)).to(torch.bfloat16)
+    else:
+        kh = case.k_pre
+    ref = oracle.prefix_decode(case.q_tgt, kh, vh, case.cu_pre, case.k_tgt, case.v_tgt,
+                               case.cu_q, 1.0 / np.sqrt(128))
+    assert_close(out, lse, *ref, what=f"fp8 {mode} balanced tail")
+    layers = torch.empty(bca.prefix_decode_fp8_workspace_bytes(mode, H, cap), dtype=torch.uint8,
+                         device=DEV)
+    out2, lse2 = bca.prefix_decode_fp8(*args, mode=mode, status=st, workspace=layers)
+    assert bca.read_status(st) == 0
+    assert_close(out2, lse2, *ref, what=f"fp8 {mode} key-split tail")
