@@ -239,3 +239,26 @@ def test_balanced_tail_fp8_ragged(mode):
     out2, lse2 = bca.prefix_decode_fp8(*args, mode=mode, status=st, workspace=layers)
     assert bca.read_status(st) == 0
     assert_close(out2, lse2, *ref, what=f"fp8 {mode} key-split tail")
+
+
+@pytest.mark.parametrize("H,tgt", [
+    (3, [200, 0, 129]),   # a small batch with a zero-length target: pair grid only
+    (1, [8000]),          # 32 pairs of 63 key tiles: the balanced tail
+])
+def test_decode_over_an_empty_cache(H, tgt):
+    """No sequence has a prefix and the cache has capacity 0: the decode is plain
+    attention of the targets over their own keys."""
+    import oracle
+    qt, kt, vt = (W.randn_bf16((sum(tgt), H, 128), s) for s in (51, 52, 53))
+    cq = np.concatenate([[0], np.cumsum(tgt)]).astype(np.int32)
+    cp = np.zeros(len(tgt) + 1, np.int32)
+    empty = torch.empty((1, H, 0, 128), dtype=torch.bfloat16, device=DEV)
+    if H == 1:
+        assert bca.prefix_decode_workspace_bytes(len(tgt), H, max(tgt), 0) > 0
+    st = bca.new_status(DEV)
+    out, lse = bca.prefix_decode(qt.to(DEV), empty, empty, 0, _ti(cp), kt.to(DEV), vt.to(DEV),
+                                 _ti(cq), max(tgt), 0, status=st)
+    assert bca.read_status(st) == 0
+    kp = torch.empty((0, H, 128), dtype=torch.bfloat16)
+    ref = oracle.prefix_decode(qt, kp, kp, cp, kt, vt, cq, 1.0 / np.sqrt(128))
+    assert_close(out, lse, *ref, what=f"empty cache {tgt}")
