@@ -262,3 +262,20 @@ def test_decode_over_an_empty_cache(H, tgt):
     kp = torch.empty((0, H, 128), dtype=torch.bfloat16)
     ref = oracle.prefix_decode(qt, kp, kp, cp, kt, vt, cq, 1.0 / np.sqrt(128))
     assert_close(out, lse, *ref, what=f"empty cache {tgt}")
+
+
+def test_workspace_bytes_follow_the_tail_plan():
+    """Two 133,120-byte slots per key range, one range per SM, when the last wave is worth
+    balancing (the edit decode's 56 pairs of 98 key tiles); none for a last wave whose
+    ranges would be too short (the text-to-image decode: 56 pairs of 34 tiles), for a
+    decode of whole waves, or for arguments out of range."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    items = 32 * 16                           # 32 heads x 16 pairs of 4096 target rows
+    if not (0 < items % sms and items % sms < sms // 2 and sms <= 256):
+        pytest.skip(f"{sms} SMs: the edit decode has no short last wave")
+    assert bca.prefix_decode_workspace_bytes(1, 32, 4096, 8384) == 2 * sms * 133120
+    assert bca.prefix_decode_workspace_bytes(1, 32, 4096, 256) == 0
+    assert bca.prefix_decode_workspace_bytes(sms, 2, 256, 8384) == 0     # 2 x sms pairs
+    assert bca.prefix_decode_workspace_bytes(0, 32, 4096, 8384) == 0
+    assert bca.prefix_decode_workspace_bytes(1, 32, 4096, -1) == 0
+    assert bca.prefix_decode_workspace_bytes(1, 32, 4096, 8384, head_dim=64) == 0
