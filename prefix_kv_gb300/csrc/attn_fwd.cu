@@ -126,9 +126,11 @@ struct FwdParams {
   __nv_bfloat16* cache_v;
   int decode_pairs_per_seq;   // decode: tile pairs per sequence (grid decoding)
   int decode_split_from;      // decode: first item split into single-tile items
-  int64_t prefill_split_from; // prefill: first pair CTA, in the grid's launch order
-                              //   (x fastest, then y, then z), done as two key-split
-                              //   single-tile items instead; >= the grid size: none
+  int64_t prefill_split_from; // prefill: the pair CTAs from this index on, counted with
+                              //   the head in group fastest, then the sequence x head
+                              //   group, then the tile pair (cheapest pairs last), are
+                              //   done as two key-split single-tile items instead;
+                              //   >= the grid size: none
   int prefill_x, prefill_y;   // prefill: x and y extents of the pair grid
   __nv_bfloat16* out;
   float* lse;
@@ -363,10 +365,12 @@ __device__ __forceinline__ void attn_item(const CUtensorMap& tm_q, const CUtenso
     // before this wait.
     // (A key-split item belongs to a grid launched after the pair grid, which it may
     // run beside: it reads the records without that wait.  It starts only after
-    // every pair CTA has started.  The host splits only past two full waves of pair
-    // CTAs (one per SM at a time), none of which ends before the prep has completed
-    // (those with nothing to do wait for it too), so one of them has ended, after
-    // the prep, before the last could start.  The records are read through L2.)
+    // every pair CTA has started.  The host splits only when at least two full waves
+    // of pair CTAs keep their pairs (one CTA per SM at a time), none of which ends
+    // before the prep has completed (those with nothing to do wait for it too), so
+    // one of them has ended, after the prep, before the last could start; the pair
+    // CTAs that hand their pair to the split grid return at once, wherever they sit
+    // in launch order.  The records are read through L2.)
     if constexpr (!kSplit) {
       grid_dependency_wait();
       for (int i = 0; i < 2; ++i) {
@@ -1118,11 +1122,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int h = blockIdx.x + (blockIdx.z % p.head_groups) * gridDim.x;   // groups are full
     const int b = blockIdx.z / p.head_groups;
     const int m_base = 2 * (static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y));
-    const int64_t launch_idx =
-        blockIdx.x + static_cast<int64_t>(gridDim.x) * (blockIdx.y + static_cast<int64_t>(gridDim.y) * blockIdx.z);
-    // a pair of the last, partly filled wave is done by the key-split grid (never
-    // the pair that appends to the cache)
-    if (launch_idx >= p.prefill_split_from && !pair_appends(p, b, m_base)) return;
+    // The pairs of the split set (the cheapest of every head group) are done by the
+    // key-split grid (never the pair that appends to the cache).
+    const int64_t split_idx =
+        blockIdx.x + static_cast<int64_t>(gridDim.x) * (blockIdx.z + static_cast<int64_t>(gridDim.z) * blockIdx.y);
+    if (split_idx >= p.prefill_split_from && !pair_appends(p, b, m_base)) return;
     // Any other pair CTA ends only after the schedule prep has completed, even with
     // no rows to do: the key-split grid relies on it.  (One that finds another CTA
     // has given up ends at once; the split CTAs, which start later, then do too.)
@@ -1133,13 +1137,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_item<false, false, kPagedAppend>(tm_q, tm_k, tm_v, tm_k2, tm_v2, tm_o, p, sm, h, b,
                                           m_base, 2);
   } else if constexpr (!kDecode) {
-    // Prefill key split: CTA 2i + s does query tile s of the pair CTA at launch
-    // index prefill_split_from + i of the pair grid.
-    const int64_t launch_idx = p.prefill_split_from + blockIdx.x / 2;
-    const int x = static_cast<int>(launch_idx % p.prefill_x);
-    const int64_t yz = launch_idx / p.prefill_x;
-    const int y = static_cast<int>(yz % p.prefill_y);
-    const int z = static_cast<int>(yz / p.prefill_y);
+    // Prefill key split: CTA 2i + s does query tile s of the pair CTA at split index
+    // prefill_split_from + i of the pair grid (head in group fastest, then sequence x
+    // head group, then tile pair).
+    const int64_t split_idx = p.prefill_split_from + blockIdx.x / 2;
+    const int x = static_cast<int>(split_idx % p.prefill_x);
+    const int64_t zy = split_idx / p.prefill_x;
+    const int n_z = p.batch * p.head_groups;
+    const int z = static_cast<int>(zy % n_z);
+    const int y = static_cast<int>(zy / n_z);
     const int h = x + (z % p.head_groups) * p.prefill_x;
     const int b = z / p.head_groups;
     const int m_base = 2 * (p.prefill_y - 1 - y);
@@ -1509,12 +1515,19 @@ int launch_attention(const AttnLaunch& a, bool decode, cudaStream_t stream) {
       groups = 1;
     }
     p.head_groups = groups;
-    // The pair CTAs of a last, partly filled wave (in launch order: the cheapest
-    // pairs of the last head group) become key-split single-tile items, two CTAs
-    // each, in a second grid that may start as soon as every pair CTA has started.
-    // Only past two full waves of pair CTAs: before every pair CTA has started, at
-    // least one must have ended, which it cannot do before the schedule prep has
-    // completed; the split grid reads the prep's records without waiting for it.
+    // The pair CTAs of a last, partly filled wave become key-split single-tile
+    // items, two CTAs each, in a second grid that may start as soon as every pair
+    // CTA has started.  They are the pairs with the highest pair index (the cheapest:
+    // row ends never decrease along a sequence) across all head groups, not the last
+    // CTAs in launch order (the cheapest pairs of the last group): on the
+    // text-to-image layer that is all 32 two-tile text pairs and 56 image pairs,
+    // against 80 image pairs and 8 text pairs, whose 160 heavy split items did not
+    // fit one wave of 152 SMs.  The pair grid keeps its head groups outermost, so
+    // that the CTAs in flight share the K/V of a few heads in L2.
+    // Only when at least two full waves of pair CTAs keep their pairs: before every
+    // pair CTA has started, one of those must have ended, which it cannot do before
+    // the schedule prep has completed; the split grid reads the prep's records
+    // without waiting for it.
     // And only for grids of at most four waves: a split item does its keys ~40%
     // slower than a pair (two K/V streams, its own set-up), which the last wave's
     // idle SMs pay back in a short grid (text-to-image layer: 226 -> 213 us) but not
