@@ -141,13 +141,16 @@ def test_bounds_prefill_paged_append_last_page_partial():
         assert np.isnan(g[~written]).all()
 
 
-def test_bounds_prefill_key_split_tail():
-    """A pair grid short enough for the key-split grid (32 heads, sequences of 2300 and,
-    bottom-right, 1900 of 2400 keys: 576 pair CTAs, the last 120 split), with the
-    cache append: its last pair of sequence 1 stays a pair CTA.  Sampled rows
-    against the oracle, bit-identical to the release build."""
-    case = ragged_case(203, [2300, 2400], [2300, 1900], heads=32, max_spans=6, max_span=700)
-    pre = [1000, 1700]
+@pytest.mark.parametrize("kv,ql,pre", [([2300, 2400], [2300, 1900], [1000, 1700]),
+                                       ([2300, 260], [2300, 200], [1000, 150])],
+                         ids=["long", "short-second"])
+def test_bounds_prefill_key_split_tail(kv, ql, pre):
+    """A pair grid short enough for the key-split grid (32 heads, a sequence of 2300 and
+    a bottom-right one: 576 pair CTAs, the 120 cheapest pairs split), with the cache
+    append.  With a 200-row second sequence its only pair, which appends, is among the
+    cheapest and stays a pair CTA, and the split items past its end have no rows.
+    Sampled rows against the oracle, bit-identical to the release build."""
+    case = ragged_case(203, kv, ql, heads=32, max_spans=6, max_span=700)
     cp = np.concatenate([[0], np.cumsum(pre)]).astype(np.int32)
     cap = int(cp[-1]) + 64
 
@@ -162,7 +165,7 @@ def test_bounds_prefill_key_split_tail():
 
     rel, dbg = _both(run)
     _same(rel, dbg)
-    rows = np.r_[0:130, 1020:1040, 2170:2300, 2300:2430, 4100:4200]
+    rows = np.r_[0:130, 1020:1040, 2170:2300, 2300:2430, (4100 if ql[1] > 1800 else 2430):2300 + ql[1]]
     heads = np.array([1, 20, 31])
     ref_out, ref_lse = case.reference(rows=rows, heads=heads)
     assert_close(dbg[0], dbg[1], ref_out, ref_lse, rows=rows, heads=heads, what="debug split")

@@ -311,15 +311,18 @@ def test_prefill_full_size_sampled_rows(wl):
     assert_close(out, lse, *ref, rows=rows, heads=heads, what=wl.name)
 
 
-def test_prefill_key_split_tail_ragged():
-    """32 heads, sequences of 2300 and (bottom-right) 1900 of 2400 keys: a pair grid of
-    8 x 9 x 8 = 576 CTAs, whose last 120 in launch order (sequence 1, heads 16-31) run
-    as key-split single tiles: a ragged last tile (108 rows), items past the
-    sequence's end, rows that see no key of warpgroup 1's half, random layouts."""
-    case = ragged_case(31, [2300, 2400], [2300, 1900], heads=32, max_spans=6, max_span=700)
+@pytest.mark.parametrize("kv,ql", [([2300, 2400], [2300, 1900]), ([2300, 260], [2300, 200])],
+                         ids=["long", "short-second"])
+def test_prefill_key_split_tail_ragged(kv, ql):
+    """32 heads, a sequence of 2300 and a bottom-right one: a pair grid of 8 x 9 x 8 =
+    576 CTAs, whose 120 cheapest pairs (the first two tile pairs of every sequence and
+    head) run as key-split single tiles: rows that see no key of warpgroup 1's half,
+    random layouts.  With a 200-row second sequence its only pair (a ragged second
+    tile of 72 rows) is among them, and so are items past that sequence's end."""
+    case = ragged_case(31, kv, ql, heads=32, max_spans=6, max_span=700)
     out, lse = case.run()
     rows = np.unique(np.concatenate([tile_boundary_rows(case.cu_q[:2], extra=64, seed=2),
-                                     np.arange(2300, 4200)]))   # every row of sequence 1
+                                     np.arange(2300, 2300 + ql[1])]))   # every row of sequence 1
     heads = np.array([0, 17, 24, 31])
     ref = case.reference(rows=rows, heads=heads)
     assert_close(out, lse, *ref, rows=rows, heads=heads, what="key-split tail")

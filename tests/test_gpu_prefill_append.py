@@ -178,15 +178,16 @@ def test_prefill_append_paged_rejects_bad_page():
 
 @pytest.mark.parametrize("paged", [False, True], ids=["contiguous", "paged"])
 def test_prefill_append_key_split_tail_keeps_the_appending_pair(paged):
-    """A pair grid of 8 x 16 x 4 = 512 CTAs (under four waves of 152): its last 56 in
-    launch order, those of the second head group of sequence 1, become key-split
-    single-tile items.  Sequence 1's last pair (tiles 10-11), which appends its prefix
-    to the cache, lies among them and stays a pair CTA; both calls match the oracle
+    """A pair grid of 8 x 16 x 4 = 512 CTAs (under four waves of 152): its 56 cheapest
+    pairs (the first tile pair of every sequence and head, and the second of most)
+    become key-split single-tile items.  Sequence 1 has 200 rows: its only pair, which
+    appends its prefix to the cache, lies among them and stays a pair CTA (its second
+    pairs, past its end, are split items with no rows); both calls match the oracle
     and the cache is bit-exact (against the oracle's append, or the standalone paged
     append through the same page table)."""
     from gpu_cases import assert_close, tile_boundary_rows
-    case = ragged_case(95, [4096, 1500], heads=16)
-    pre = [3000, 1400]
+    case = ragged_case(95, [4096, 200], heads=16)
+    pre = [3000, 150]
     cu_p = np.concatenate([[0], np.cumsum(pre)]).astype(np.int32)
     d = lambda x: x.to(DEV)
     ti = lambda x: torch.from_numpy(np.asarray(x, dtype=np.int32)).to(DEV)
@@ -205,7 +206,7 @@ def test_prefill_append_key_split_tail_keeps_the_appending_pair(paged):
         out2, lse2 = bca.prefill_append(*args, ti(cu_p), ck, cv, 0, status=st)
     assert bca.read_status(st) == 0
     rows = np.unique(np.concatenate([tile_boundary_rows(case.cu_q, extra=200, seed=3),
-                                     np.arange(4096, 5596)]))   # every row of sequence 1
+                                     np.arange(4096, 4296)]))   # every row of sequence 1
     heads = np.array([2, 9, 15])
     ref = case.reference(rows=rows, heads=heads)
     assert_close(out1, lse1, *ref, rows=rows, heads=heads, what="prefill")
